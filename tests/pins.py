@@ -1,0 +1,287 @@
+"""Pins for the CPU oracle: checks against things other than the oracle itself.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` and raises ``AssertionError`` when the
+oracle disagrees with what the pages or the mathematics fix:
+
+* a library routine (torch fp64 ``scaled_dot_product_attention``, torch's
+  float32 -> bf16 conversion),
+* closed forms (context length 1 returns V; identical keys or a zero scale return
+  the mean of V; two tokens give a sigmoid mix),
+* invariants (paged == dense on scattered blocks -- the mini-vLLM README's M4
+  test; any permutation of the physical pool leaves the output unchanged,
+  enumerated exhaustively on a tiny pool; cached decode == recompute -- the
+  llm-stack KV-cache gate; NaN in slots nobody owns changes nothing),
+* the flash-decoding algebra (merging per-range log-sum-exp results equals the
+  unsplit softmax, for every split).
+
+The same functions run against deliberately broken oracle builds, each of which
+must fail at least one pin.
+"""
+
+from __future__ import annotations
+
+import itertools
+import math
+
+import torch
+import torch.nn.functional as F
+
+from paged_kv_decode_mapping_gb300 import workloads as W
+
+
+def _case(B=3, Hq=8, Hkv=2, D=16, BS=4, lens=(1, 7, 13), seed=11, pool_factor=1.5, write="last"):
+    w = W.small_workload(B=B, Hq=Hq, Hkv=Hkv, D=D, BS=BS, lens=lens, seed=seed,
+                         pool_factor=pool_factor, write=write)
+    return W.make_inputs(w)
+
+
+def _gather(cache: torch.Tensor, table_row: torch.Tensor, L: int, g: int) -> torch.Tensor:
+    """Dense [L, D] rows of kv head g via torch advanced indexing."""
+    BS = cache.shape[2]
+    t = torch.arange(L)
+    phys = table_row.long()[t // BS]
+    return cache[phys, g, t % BS, :].double()
+
+
+def _sdpa_reference(inp) -> torch.Tensor:
+    """torch fp64 SDPA (not causal) per sequence on gathered K/V, GQA via repeat_interleave."""
+    q, kc, vc = inp["q"], inp["k_cache"], inp["v_cache"]
+    B, Hq, D = q.shape
+    Hkv = kc.shape[1]
+    G = Hq // Hkv
+    out = torch.zeros(B, Hq, D, dtype=torch.float64)
+    for b in range(B):
+        L = int(inp["context_lens"][b])
+        if L == 0:
+            continue
+        K = torch.stack([_gather(kc, inp["block_tables"][b], L, g) for g in range(Hkv)])
+        V = torch.stack([_gather(vc, inp["block_tables"][b], L, g) for g in range(Hkv)])
+        K = K.repeat_interleave(G, dim=0)[None]  # [1, Hq, L, D]
+        V = V.repeat_interleave(G, dim=0)[None]
+        qq = q[b].double()[None, :, None, :]  # [1, Hq, 1, D]
+        o = F.scaled_dot_product_attention(qq, K, V, is_causal=False, scale=inp["scale"])
+        out[b] = o[0, :, 0, :]
+    return out
+
+
+def _decode(o, inp, **kw):
+    return o.decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_tables"],
+                    inp["context_lens"], inp["scale"], **kw)
+
+
+# --------------------------------------------------------------------------- bf16
+def pin_bf16_widening(o):
+    """bf16 -> double equals torch's exact bf16 -> float64 for all 65536 patterns."""
+    bits = torch.arange(-32768, 32768, dtype=torch.int32).to(torch.int16)
+    ref = bits.view(torch.bfloat16).double()
+    for i in range(0, 65536, 257):  # a spread-out sample through ctypes, all sign/exponent mixes
+        got = o.bf16_to_double(int(bits[i]) & 0xFFFF)
+        r = float(ref[i])
+        assert (math.isnan(got) and math.isnan(r)) or got == r, (i, got, r)
+
+
+def pin_bf16_rounding(o):
+    """double -> bf16 (RNE) equals torch's float32 -> bf16 on float32 inputs, incl. ties."""
+    g = torch.Generator().manual_seed(5)
+    xs = torch.cat([
+        torch.randn(3000, generator=g) * torch.exp2(torch.randint(-30, 30, (3000,), generator=g).float()),
+        # exact ties: a bf16 value plus half an ulp (both parities of the last kept bit)
+        (torch.arange(1, 300, dtype=torch.int32) << 16 | 0x8000).view(torch.float32),
+        (torch.arange(0x3F80, 0x3FF0, dtype=torch.int32) << 16 | 0x8000).view(torch.float32),
+        torch.tensor([0.0, -0.0, 1e-40, -1e-40, 3.0e38, 65504.0, 1.0 / 3.0]),
+    ])
+    ref = xs.to(torch.bfloat16).view(torch.int16)
+    for x, r in zip(xs.tolist(), ref.tolist()):
+        got = o.double_to_bf16(x)
+        assert got == (r & 0xFFFF), (x, hex(got), hex(r & 0xFFFF))
+
+
+# ------------------------------------------------------------------------- write
+def pin_write(o):
+    """Written slots hold exactly the input bits; every other byte is unchanged;
+    negative slots are skipped; slot 0 and a slot in the last block are honoured."""
+    inp = _case(B=2, Hq=4, Hkv=2, D=8, BS=4, lens=(6, 9), write="none")
+    NB = inp["num_blocks"]
+    g = torch.Generator().manual_seed(3)
+    slots = torch.tensor([0, -1, NB * 4 - 1, 5, 17], dtype=torch.int64)
+    k = torch.randn(len(slots), 2, 8, generator=g).to(torch.bfloat16)
+    v = torch.randn(len(slots), 2, 8, generator=g).to(torch.bfloat16)
+    kc, vc = o.kv_write(k, v, slots, inp["k_cache"], inp["v_cache"])
+    ek, ev = inp["k_cache"].clone(), inp["v_cache"].clone()
+    for i, s in enumerate(slots.tolist()):
+        if s >= 0:
+            ek[s // 4, :, s % 4, :] = k[i]
+            ev[s // 4, :, s % 4, :] = v[i]
+    assert torch.equal(kc.view(torch.int16), ek.view(torch.int16))
+    assert torch.equal(vc.view(torch.int16), ev.view(torch.int16))
+
+
+# --------------------------------------------------------------------- attention
+def pin_sdpa(o):
+    """Oracle == torch fp64 SDPA (non-causal) on the gathered copy, GQA and MHA."""
+    for kw in (dict(), dict(Hq=4, Hkv=4, lens=(3, 16, 9)), dict(Hq=6, Hkv=2, D=8, BS=2,
+                                                                 lens=(5, 1, 12))):
+        inp = _case(**kw)
+        got = _decode(o, inp)
+        ref = _sdpa_reference(inp)
+        assert torch.allclose(got, ref, atol=1e-12, rtol=1e-12), (got - ref).abs().max()
+
+
+def pin_paged_equals_dense(o):
+    """Scattered blocks give the same output as one contiguous, in-order copy."""
+    inp = _case(lens=(5, 11, 16))
+    B, BS = 3, 4
+    Hkv, D = inp["k_cache"].shape[1], inp["k_cache"].shape[3]
+    nblk = [(int(L) + BS - 1) // BS for L in inp["context_lens"]]
+    NB = sum(nblk)
+    kd = torch.zeros(NB, Hkv, BS, D, dtype=torch.bfloat16)
+    vd = torch.zeros_like(kd)
+    tables = torch.zeros(B, max(nblk), dtype=torch.int32)
+    nxt = 0
+    for b in range(B):
+        L = int(inp["context_lens"][b])
+        for t in range(L):
+            blk, off = nxt + t // BS, t % BS
+            src = int(inp["block_tables"][b, t // BS])
+            kd[blk, :, off] = inp["k_cache"][src, :, t % BS]
+            vd[blk, :, off] = inp["v_cache"][src, :, t % BS]
+        tables[b, :nblk[b]] = torch.arange(nxt, nxt + nblk[b], dtype=torch.int32)
+        nxt += nblk[b]
+    dense = dict(inp, k_cache=kd, v_cache=vd, block_tables=tables)
+    assert torch.equal(_decode(o, inp), _decode(o, dense))
+
+
+def pin_pool_permutations(o):
+    """Brute force: every permutation of a 6-block pool (rewrite pool + tables) leaves
+    the output bit-identical."""
+    inp = _case(B=2, Hq=4, Hkv=2, D=4, BS=2, lens=(5, 3), pool_factor=1.2)
+    NB = inp["k_cache"].shape[0]
+    assert NB == 6
+    ref = _decode(o, inp)
+    tab = inp["block_tables"]
+    for perm in itertools.permutations(range(NB)):
+        p = torch.tensor(perm)
+        kc = torch.empty_like(inp["k_cache"])
+        vc = torch.empty_like(inp["v_cache"])
+        kc[p] = inp["k_cache"]
+        vc[p] = inp["v_cache"]
+        nt = torch.where(tab >= 0, p[tab.clamp(min=0).long()].to(torch.int32), tab)
+        got = _decode(o, dict(inp, k_cache=kc, v_cache=vc, block_tables=nt))
+        assert torch.equal(got, ref), perm
+
+
+def pin_length_one(o):
+    """Context length 1: the output is the single cached V row, exactly."""
+    inp = _case(lens=(1, 1, 1))
+    got = _decode(o, inp)
+    G = inp["q"].shape[1] // inp["k_cache"].shape[1]
+    for b in range(3):
+        phys = int(inp["block_tables"][b, 0])
+        for h in range(inp["q"].shape[1]):
+            assert torch.equal(got[b, h], inp["v_cache"][phys, h // G, 0].double()), (b, h)
+
+
+def pin_identical_keys_and_zero_scale(o):
+    """All keys equal, or scale 0: uniform weights, so the output is the mean of V."""
+    inp = _case(lens=(4, 9, 13))
+    kc = inp["k_cache"].clone()
+    kc[:] = kc[0, :, :1, :]  # one key row repeated everywhere (per kv head)
+    for case in (dict(inp, k_cache=kc), dict(inp, scale=0.0)):
+        got = _decode(o, case)
+        G = inp["q"].shape[1] // inp["k_cache"].shape[1]
+        for b in range(3):
+            L = int(inp["context_lens"][b])
+            for h in range(inp["q"].shape[1]):
+                Vd = _gather(inp["v_cache"], inp["block_tables"][b], L, h // G)
+                assert torch.allclose(got[b, h], Vd.mean(0), atol=1e-13), (b, h)
+
+
+def pin_two_tokens(o):
+    """Two tokens: out = sigmoid(s1 - s2) v1 + sigmoid(s2 - s1) v2."""
+    inp = _case(lens=(2, 2, 2))
+    got = _decode(o, inp)
+    G = inp["q"].shape[1] // inp["k_cache"].shape[1]
+    for b in range(3):
+        for h in range(inp["q"].shape[1]):
+            K = _gather(inp["k_cache"], inp["block_tables"][b], 2, h // G)
+            V = _gather(inp["v_cache"], inp["block_tables"][b], 2, h // G)
+            qd = inp["q"][b, h].double()
+            s1, s2 = inp["scale"] * float(qd @ K[0]), inp["scale"] * float(qd @ K[1])
+            sig = 1.0 / (1.0 + math.exp(-(s1 - s2)))
+            ref = sig * V[0] + (1.0 - sig) * V[1]
+            assert torch.allclose(got[b, h], ref, atol=1e-13), (b, h)
+
+
+def pin_context_zero(o):
+    """An empty context gives a zero output (no NaN)."""
+    inp = _case(lens=(0, 5, 0))
+    got = _decode(o, inp)
+    assert torch.equal(got[0], torch.zeros_like(got[0])) and torch.equal(got[2], torch.zeros_like(got[2]))
+    assert torch.isfinite(got).all()
+
+
+def pin_nan_poison(o):
+    """NaN in every slot no sequence owns leaves the output finite and unchanged."""
+    w = W.small_workload(B=3, Hq=8, Hkv=2, D=16, BS=4, lens=(3, 10, 13), seed=11)
+    clean = W.make_inputs(w)
+    dirty = W.make_inputs(w, poison=True)
+    assert torch.isnan(dirty["k_cache"].float()).any()
+    a, b = _decode(o, clean), _decode(o, dirty)
+    assert torch.isfinite(b).all() and torch.equal(a, b)
+
+
+def pin_partitions(o):
+    """Flash-decoding algebra: merging the per-range (o, lse) of any split equals the
+    unsplit output; one range is the identity; ranges past the end weigh nothing."""
+    inp = _case(lens=(1, 7, 13))
+    full = _decode(o, inp)
+    for b in range(3):
+        L = int(inp["context_lens"][b])
+        for h in (0, 3, 7):
+            for P in (1, 2, 3, 5, 13, 64):
+                n = (L + P - 1) // P + 1  # one extra, empty range
+                op, lse = o.decode_partitions(b, h, n, P, inp["q"], inp["k_cache"],
+                                              inp["v_cache"], inp["block_tables"],
+                                              inp["context_lens"], inp["scale"])
+                assert lse[-1] == -math.inf and torch.equal(op[-1], torch.zeros_like(op[-1]))
+                got = o.lse_combine(op, lse)
+                assert torch.allclose(got, full[b, h], atol=1e-13), (b, h, P)
+            # lse of the whole range is the log of the softmax normaliser of the scaled scores
+            op, lse = o.decode_partitions(b, h, 1, 10_000, inp["q"], inp["k_cache"],
+                                          inp["v_cache"], inp["block_tables"],
+                                          inp["context_lens"], inp["scale"])
+            G = inp["q"].shape[1] // inp["k_cache"].shape[1]
+            K = _gather(inp["k_cache"], inp["block_tables"][b], L, h // G)
+            s = inp["scale"] * (K @ inp["q"][b, h].double())
+            assert abs(float(lse[0]) - float(torch.logsumexp(s, 0))) < 1e-12
+            assert torch.allclose(o.lse_combine(op, lse), op[0], atol=1e-15)
+
+
+def pin_cached_equals_recompute(o):
+    """Writing a sequence's K/V one token per step through the slot mapping, then
+    decoding, equals attention recomputed over all tokens at once."""
+    BS, Hkv, D, Hq = 4, 2, 8, 4
+    L = 11
+    g = torch.Generator().manual_seed(9)
+    Kall = torch.randn(L, Hkv, D, generator=g).to(torch.bfloat16)
+    Vall = torch.randn(L, Hkv, D, generator=g).to(torch.bfloat16)
+    q = torch.randn(1, Hq, D, generator=g).to(torch.bfloat16)
+    NB = 5
+    table = torch.tensor([[3, 0, 4]], dtype=torch.int32)
+    kc = torch.zeros(NB, Hkv, BS, D, dtype=torch.bfloat16)
+    vc = torch.zeros_like(kc)
+    for t in range(L):
+        slot = int(table[0, t // BS]) * BS + t % BS
+        kc, vc = o.kv_write(Kall[t:t + 1], Vall[t:t + 1], torch.tensor([slot]), kc, vc)
+    got = o.decode(q, kc, vc, table, torch.tensor([L], dtype=torch.int32), 0.5)
+    K = Kall.double().permute(1, 0, 2).repeat_interleave(Hq // Hkv, 0)[None]
+    V = Vall.double().permute(1, 0, 2).repeat_interleave(Hq // Hkv, 0)[None]
+    ref = F.scaled_dot_product_attention(q.double()[:, :, None, :], K, V, scale=0.5)[:, :, 0]
+    assert torch.allclose(got, ref, atol=1e-12)
+
+
+ALL_PINS = [
+    pin_bf16_widening, pin_bf16_rounding, pin_write, pin_sdpa, pin_paged_equals_dense,
+    pin_pool_permutations, pin_length_one, pin_identical_keys_and_zero_scale, pin_two_tokens,
+    pin_context_zero, pin_nan_poison, pin_partitions, pin_cached_equals_recompute,
+]
