@@ -1,0 +1,444 @@
+"""Benchmark of one paged-KV decode step on GB300: slot write + decode attention.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 2]
+
+A step is one pass of the whole hot path over one batch of synthetic input: the
+slot-mapping KV write of the step's new tokens, then decode attention as the
+launcher plans it (one kernel, or the split kernel + the log-sum-exp combine).
+
+Default workload: decode B=16, context 2048, 32 query / 8 kv heads, head_dim 64,
+bf16, block_size 16, block tables drawn from a shuffled pool of 2560 blocks, 16
+new tokens written per step.
+
+Timing (ours): inputs are resident in HBM; the pool is replicated R times so that
+the copies together exceed 3x the L2 size, and step i uses copy i mod R (so every
+step reads its K/V from DRAM, not L2).  The K timed steps are replayed from CUDA
+graphs (one graph of R steps, one of the remainder), bracketed by a barrier and
+torch.cuda.synchronize() and timed with CUDA events on the launching stream; the
+max over ranks is reported.  `value` is algorithmic HBM bytes per step / time,
+in GB/s (whole job: all ranks' bytes / the slowest rank's time).
+
+`roofline` covers the dominant kernel (the decode/split kernel), timed alone by
+the same method; `e2e` runs the same step eagerly through the public API with the
+step's inputs copied from pinned host memory and the output read back each step;
+`cpu_baseline` is the CPU oracle (fp64, all host cores) on the same workload.
+
+`--impl reference` times that oracle as the reference arm (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_decode_mapping_gb300 import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention µs/step and achieved HBM GB/s (% of GB300 peak)"
+
+
+# ----------------------------------------------------------------------------- bytes
+def algorithmic_bytes(inp: dict) -> dict:
+    """Bytes the operations must move, per step (no re-reads, no workspace)."""
+    w = inp["workload"]
+    lens = inp["context_lens"].long()
+    nblk = (lens + w.BS - 1) // w.BS
+    kv = int(lens.sum()) * w.Hkv * w.D * 2 * 2             # K and V rows read once
+    qo = w.B * w.Hq * w.D * 2                                # q read, out written (each)
+    tables = 4 * int(nblk.sum()) + 4 * w.B                   # table entries + context_lens
+    T = int(inp["slot_mapping"].numel())
+    write = 2 * (2 * T * w.Hkv * w.D * 2) + 8 * T            # k/v read + cache rows written + slots
+    decode = kv + qo + tables                                # what the decode kernel reads
+    return {"kv": kv, "decode_kernel": decode, "step": decode + qo + write, "write": write}
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- setup
+def measured_peaks() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+def recorded_traffic(kernel_source: str) -> float | None:
+    """Per-launch DRAM bytes of the decode kernel from the committed ncu summary, if it
+    was taken on the current kernel source (same sha256); else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_decode_kernel_workload2.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    sha = hashlib.sha256(open(kernel_source, "rb").read()).hexdigest()
+    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_tr or m_sha.group(1) != sha:
+        return None
+    return float(m_tr.group(1))
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_max(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def time_oracle(inp: dict, budget_s: float, max_reps: int = 1000) -> dict:
+    """Oracle write+decode on the host cores for up to ~budget_s: GB/s of algorithmic bytes."""
+    import oracle
+
+    orc = oracle.get()
+    nbytes = algorithmic_bytes(inp)["step"]
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        orc.step(inp)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= max_reps:
+            break
+    per = el / reps
+    return {"value": nbytes / per / 1e9, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{reps} full write+decode steps of the workload, fp64, OpenMP over "
+                      f"(sequence, head) rows on {os.cpu_count()} threads; {per * 1e3:.1f} ms/step"}
+
+
+def run_reference(args, w) -> None:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+
+    inp = W.make_inputs(w)
+    orc = oracle.get()
+    B, Hq = w.B, w.Hq
+    rows_all = torch.tensor([[b, h] for b in range(B) for h in range(Hq)], dtype=torch.int32)
+    # calibrate one full step, then size each step's sample so the run stays within ~2 minutes
+    t0 = time.perf_counter()
+    orc.step(inp)
+    t_full = time.perf_counter() - t0
+    budget = 120.0
+    frac = min(1.0, budget / max(1e-9, t_full * (args.steps + args.warmup)))
+    n_rows = max(1, int(round(frac * len(rows_all))))
+    step_bytes = algorithmic_bytes(inp)["step"]
+    kv_cache, v_cache = orc.kv_write(inp["k_new"], inp["v_new"], inp["slot_mapping"],
+                                     inp["k_cache"], inp["v_cache"])
+
+    def one(i):
+        sel = rows_all[(torch.arange(n_rows) + i * n_rows) % len(rows_all)]
+        if n_rows == len(rows_all):
+            orc.step(inp)
+            return step_bytes
+        orc.decode(inp["q"], kv_cache, v_cache, inp["block_tables"], inp["context_lens"],
+                   inp["scale"], rows=sel)
+        return step_bytes * n_rows / len(rows_all)  # the sampled share of the step
+
+    for i in range(args.warmup):
+        one(i)
+    t0 = time.perf_counter()
+    nbytes = 0
+    for i in range(args.steps):
+        nbytes += one(i)
+    el = time.perf_counter() - t0
+    value = nbytes / el / 1e9
+    sample = (f"each step: the full write+decode step" if n_rows == len(rows_all) else
+              f"each step: {n_rows} of {len(rows_all)} (sequence, query head) rows of the decode, "
+              f"round robin") + f"; fp64 oracle, {os.cpu_count()} threads"
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "impl": "reference", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_dict(w, inp, args, world=1),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(w, inp, args, world: int) -> dict:
+    return {"workload": w.name, "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv,
+            "head_dim": w.D, "block_size": w.BS, "context": f"{w.lens}:{int(inp['context_lens'].min())}"
+            f"..{int(inp['context_lens'].max())}", "pool_blocks": inp["num_blocks"],
+            "new_tokens_per_step": int(inp["slot_mapping"].numel()), "seed": w.seed,
+            "l2": "rotating pool copies > 3x L2 between steps", "parallelism": f"replicas x{world}"}
+
+
+# ----------------------------------------------------------------------------- ours
+def run_ours(args, w) -> None:
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=device)
+    from paged_kv_decode_mapping_gb300 import binding as B
+
+    inp = W.make_inputs(w, seed=w.seed + 7919 * rank)
+    nb = algorithmic_bytes(inp)
+    Bn, Hq, D = inp["q"].shape
+    NB, Hkv, BS, _ = inp["k_cache"].shape
+    max_len = inp["max_context_len"]
+    scale = inp["scale"]
+    P = B.paged_decode_plan(Bn, Hkv, max_len)
+
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    pool_bytes = 2 * inp["k_cache"].numel() * 2
+    R = max(2, math.ceil(3 * l2 / pool_bytes))
+    kcs = [inp["k_cache"].to(device) for _ in range(R)]
+    vcs = [inp["v_cache"].to(device) for _ in range(R)]
+    q = inp["q"].to(device)
+    bt = inp["block_tables"].to(device)
+    cl = inp["context_lens"].to(device)
+    kn, vn, sm = inp["k_new"].to(device), inp["v_new"].to(device), inp["slot_mapping"].to(device)
+    out = torch.empty_like(q)
+    ws_bytes = B.paged_decode_workspace_size(Bn, Hq, Hkv, D, max_len)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=device)
+    n_parts = math.ceil(max_len / P) if P else 0
+    if P:
+        o_part = torch.empty(Bn, Hq, n_parts, D, dtype=torch.float32, device=device)
+        lse_part = torch.empty(Bn, Hq, n_parts, dtype=torch.float32, device=device)
+
+    def step(r):
+        B.paged_kv_write(kn, vn, sm, kcs[r], vcs[r])
+        B.paged_decode_attention(out, q, kcs[r], vcs[r], bt, cl, max_len, scale, workspace=ws)
+
+    def decode_only(r):
+        if P:
+            B.paged_decode_split(o_part, lse_part, q, kcs[r], vcs[r], bt, cl, max_len, scale, P)
+        else:
+            B.paged_decode_attention(out, q, kcs[r], vcs[r], bt, cl, max_len, scale, workspace=ws)
+
+    stream = torch.cuda.Stream(device)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            step(i % R)
+            decode_only(i % R)
+    torch.cuda.synchronize()
+    assert B.pkv_device_errors() == 0
+
+    def graphs_for(fn):
+        full = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(full, stream=stream):
+            for r in range(R):
+                fn(r)
+        rem = args.steps % R
+        part = None
+        if rem:
+            part = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(part, stream=stream):
+                for r in range(rem):
+                    fn(r)
+        return full, part
+
+    def timed(full, part) -> float:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(args.steps // R):
+                full.replay()
+            if part is not None:
+                part.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return e0.elapsed_time(e1) / 1e3  # seconds
+
+    g_step = graphs_for(step)
+    g_dec = graphs_for(decode_only)
+    for g in (g_step, g_dec):  # warm replays of the graphs themselves
+        with torch.cuda.stream(stream):
+            g[0].replay()
+        torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    t_step = timed(*g_step)
+    clk = clocks.stop()
+    t_dec = timed(*g_dec)
+    t_step_max = reduce_max(t_step, world, device)
+    bytes_all = reduce_sum(nb["step"] * args.steps, world, device)
+    value = bytes_all / t_step_max / 1e9
+    us_step = t_step_max / args.steps * 1e6
+    dec_s = t_dec / args.steps
+    achieved = nb["decode_kernel"] / dec_s / 1e9
+
+    # end to end through the public API: pinned host inputs in, output back, every step
+    host = {k: inp[k].pin_memory() for k in ("q", "k_new", "v_new", "slot_mapping",
+                                               "block_tables", "context_lens")}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    dq, dkn, dvn, dsm, dbt, dcl = (torch.empty_like(t, device=device) for t in host.values())
+    e2e_steps = max(20, min(args.steps, 2000))
+
+    def e2e_step(r):
+        for dst, src in zip((dq, dkn, dvn, dsm, dbt, dcl), host.values()):
+            dst.copy_(src, non_blocking=True)
+        B.paged_kv_write(dkn, dvn, dsm, kcs[r], vcs[r])
+        B.paged_decode_attention(out, dq, kcs[r], vcs[r], dbt, dcl, max_len, scale, workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            e2e_step(i % R)
+        barrier(world)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(e2e_steps):
+            e2e_step(i % R)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    t_e2e = reduce_max(e0.elapsed_time(e1) / 1e3 / e2e_steps, world, device)
+    e2e_value = reduce_sum(nb["step"], world, device) / t_e2e / 1e9
+
+    peaks = measured_peaks()
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if peak else "fallback"
+    peak = peak or 6800.0
+    traffic = recorded_traffic(os.path.join(ROOT, "paged_kv_decode_mapping_gb300", "csrc", "pkv_decode.cu"))
+    launches_per_step = 1 + (2 if P else 1)
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+        return
+    cpu = time_oracle(inp, budget_s=args.cpu_budget) if (world == 1 and args.cpu_budget > 0) else None
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": us_step / 1e3, "us_per_step": us_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config_dict(w, inp, args, world),
+        "hbm_frac_of_peak": value / peak,
+        "plan": {"partition_tokens": P, "n_parts": n_parts, "pool_copies": R},
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel" + (" (split)" if P else ""),
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_src} hbm_gbs (copy, burst)",
+                     "bytes_per_launch": nb["decode_kernel"], "us_per_launch": dec_s * 1e6,
+                     "traffic": traffic},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "us_per_step": t_e2e * 1e6},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=2, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle time for the cpu_baseline object (0: skip)")
+    args = ap.parse_args()
+    w = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

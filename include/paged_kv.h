@@ -1,0 +1,191 @@
+/*
+ * paged_kv.h -- C ABI of the paged-KV decode library (libpkv.so, GB300 / sm_103a).
+ *
+ * One decode step of a paged KV cache, as the pages describe it:
+ *  - "mini-vLLM" LLM-Inference-Engine README, paged KV-cache paragraph: the KV
+ *    cache is a fixed pool of physical blocks of block_size token slots; a
+ *    per-sequence block table maps logical positions to physical blocks.
+ *  - "vLLM-Style Llama Inference Engine with Tensor Parallelism", Features and
+ *    scope / How it works: each step writes the new tokens' K/V into the paged
+ *    cache through a slot mapping, then one-token decode runs paged attention
+ *    with grouped-query heads; split-K decode is named there as the step beyond.
+ *  - "llm-stack", Serving engine: the decode query is not causally masked.
+ *
+ * Conventions shared by every entry point
+ *  - bf16 tensors are passed as pointers to their raw 16-bit patterns (pkv_bf16).
+ *  - Every pointer is DEVICE memory on the current CUDA device and is owned by
+ *    the caller; the library allocates nothing and keeps no pointer after the
+ *    call returns.  `stream` is a cudaStream_t (NULL = the legacy default
+ *    stream); all work is enqueued asynchronously on it.
+ *  - Layouts are dense and row-major (C order):
+ *      k_cache, v_cache : [num_blocks][num_kv_heads][block_size][head_dim]
+ *      q, out           : [num_seqs][num_q_heads][head_dim]
+ *      k, v (new)       : [num_tokens][num_kv_heads][head_dim]
+ *      slot_mapping     : [num_tokens] int64, slot = block * block_size + offset
+ *      block_tables     : [num_seqs][max_blocks_per_seq] int32 physical block ids
+ *      context_lens     : [num_seqs] int32, tokens in the cache per sequence
+ *                         (including any token written this step)
+ *    Query head h reads kv head h / (num_q_heads / num_kv_heads).
+ *  - Return value: PKV_OK (0) or a negative PKV_ERR_* code.  Argument errors are
+ *    found on the host before anything is enqueued; pkv_last_error() then holds
+ *    a message for the calling thread.  Bad device-side values (a block id out of
+ *    range, a slot past the pool, a context length over the table's capacity)
+ *    never cause an out-of-bounds access: the kernels skip or clamp them and
+ *    raise a bit in a per-device error word, read with pkv_device_errors().
+ */
+#ifndef PAGED_KV_H
+#define PAGED_KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t pkv_bf16; /* raw bfloat16 bits */
+
+/* Shape of the paged KV pool. */
+typedef struct pkv_cache_desc {
+  int64_t num_blocks;   /* physical blocks in the pool (> 0) */
+  int32_t block_size;   /* token slots per block: a power of two, 8 .. 256 */
+  int32_t num_kv_heads; /* kv heads (> 0) */
+  int32_t head_dim;     /* elements per head: 64 or 128 for attention; any multiple of 8 for the write */
+} pkv_cache_desc;
+
+enum {
+  PKV_OK = 0,
+  PKV_ERR_NULL = -1,        /* a required pointer is NULL */
+  PKV_ERR_SHAPE = -2,       /* inconsistent or out-of-range sizes */
+  PKV_ERR_UNSUPPORTED = -3, /* valid but not built: head_dim, block_size or group size */
+  PKV_ERR_WORKSPACE = -4,   /* workspace missing or smaller than required */
+  PKV_ERR_ALIGN = -5,       /* a pointer is not 16-byte aligned */
+  PKV_ERR_CUDA = -6,        /* a CUDA runtime call or launch failed */
+  PKV_ERR_DEVICE = -7       /* pkv_device_errors() found a device-side error bit */
+};
+
+/* Device error bits reported by pkv_device_errors(). */
+enum {
+  PKV_DEVERR_BLOCK_ID = 1,     /* a block table entry outside [0, num_blocks): read as block 0 */
+  PKV_DEVERR_SLOT = 2,         /* a slot >= num_blocks * block_size: that token was skipped */
+  PKV_DEVERR_CONTEXT_LEN = 4,  /* context_len < 0 or over the table/max_context_len: clamped */
+  PKV_DEVERR_TIMEOUT = 8       /* a pipeline wait gave up (should never happen): output invalid */
+};
+
+/*
+ * paged_kv_write -- the slot-mapping write ("vLLM-Style Llama Inference Engine",
+ * Features and scope: slot mappings; "mini-vLLM" README: the per-sequence K/V
+ * write into the block pool that page names as overhead).
+ *
+ * For every token i < num_tokens and kv head h, if slot_mapping[i] >= 0:
+ *   k_cache[slot / BS][h][slot % BS][:] = k[i][h][:]   (bit copy; v alike).
+ * Negative slots are padding and are skipped.  Two tokens with the same slot in
+ * one call leave either one's value (undefined which).  head_dim must be a
+ * multiple of 8 (16-byte rows); k, v, k_cache and v_cache 16-byte aligned.
+ * num_tokens == 0 is a no-op.
+ */
+int paged_kv_write(const pkv_bf16 *k, const pkv_bf16 *v, const int64_t *slot_mapping,
+                   int64_t num_tokens, pkv_bf16 *k_cache, pkv_bf16 *v_cache,
+                   const pkv_cache_desc *cache, void *stream);
+
+/*
+ * paged_decode_plan -- the launcher's split choice ("vLLM-Style Llama Inference
+ * Engine", Features and scope, where split-K decode is the named next step).
+ *
+ * Returns the partition size in tokens (a multiple of 64) that
+ * paged_decode_attention will use, or 0 for a single pass per (sequence, kv
+ * head).  It depends only on its arguments: short contexts take one pass; longer
+ * ones are cut into partitions so that the grid covers the GPU several times.
+ * num_sms <= 0 queries the current device.  Pure host function.
+ */
+int32_t paged_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t max_context_len,
+                          int32_t num_sms);
+
+/*
+ * paged_decode_workspace_size -- bytes of workspace paged_decode_attention needs
+ * for these sizes on the current device (0 when the plan is a single pass).
+ * Equals paged_decode_split_workspace_size(..., paged_decode_plan(...)).
+ */
+size_t paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                   int32_t head_dim, int32_t max_context_len);
+
+/* Bytes of o_part + lse_part (padded to 256 B) for an explicit partition size. */
+size_t paged_decode_split_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                         int32_t max_context_len, int32_t partition_tokens);
+
+/*
+ * paged_decode_attention -- single-token GQA decode attention over the paged
+ * cache ("vLLM-Style Llama Inference Engine", How it works: one-token decode uses
+ * a custom paged attention; "mini-vLLM" README, M4 test row: it must match dense
+ * attention on scattered blocks).
+ *
+ * For each sequence b and query head h (g = h / (num_q_heads/num_kv_heads)):
+ *   L = context_lens[b];  for t < L:  K_t = k_cache[block_tables[b][t/BS]][g][t%BS]
+ *   s_t = scale * <q[b][h], K_t>;  p = softmax(s);  out[b][h] = bf16(sum_t p_t V_t)
+ * in fp32 arithmetic on bf16 inputs, rounded to bf16 (nearest even).  No causal
+ * mask.  L == 0 gives zeros.  Table entries at or past ceil(L / BS) are not read.
+ * max_context_len must be >= every context_lens[b] (it sizes the grid and the
+ * workspace without a device-to-host read) and <= max_blocks_per_seq * BS.
+ *
+ * Supported: head_dim 64 or 128; block_size a power of two in [8, 256];
+ * num_q_heads / num_kv_heads (the group) from 1 to 8.  q, k_cache, v_cache and
+ * workspace 16-byte aligned; out 4-byte aligned.
+ *
+ * The work is split as paged_decode_plan() says: either one kernel, or
+ * paged_decode_split() into `workspace` followed by paged_decode_combine().
+ * `workspace` may be NULL when paged_decode_workspace_size() is 0.
+ */
+int paged_decode_attention(pkv_bf16 *out, const pkv_bf16 *q, const pkv_bf16 *k_cache,
+                           const pkv_bf16 *v_cache, const int32_t *block_tables,
+                           int32_t max_blocks_per_seq, const int32_t *context_lens,
+                           int32_t max_context_len, int32_t num_seqs, int32_t num_q_heads,
+                           const pkv_cache_desc *cache, float scale, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/*
+ * paged_decode_split -- flash-decoding partition kernel (split-K over the keys;
+ * the FlashAttention-2 online-softmax algebra that the first page references).
+ *
+ * Partition r of sequence b covers tokens [r*P, min((r+1)*P, L)) with
+ * P = partition_tokens (a positive multiple of 64).  For each (b, h, r) with a
+ * non-empty range it writes
+ *   o_part  [num_seqs][num_q_heads][n_parts][head_dim] fp32 : the range's
+ *                                  softmax-normalised output sum_t p_t V_t,
+ *   lse_part[num_seqs][num_q_heads][n_parts]           fp32 : ln sum_t exp(s_t),
+ * where n_parts = ceil(max_context_len / P).  Entries of empty ranges
+ * (r*P >= L) are not written.  Same preconditions as paged_decode_attention.
+ */
+int paged_decode_split(float *o_part, float *lse_part, const pkv_bf16 *q,
+                       const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                       const int32_t *block_tables, int32_t max_blocks_per_seq,
+                       const int32_t *context_lens, int32_t max_context_len, int32_t num_seqs,
+                       int32_t num_q_heads, const pkv_cache_desc *cache, float scale,
+                       int32_t partition_tokens, void *stream);
+
+/*
+ * paged_decode_combine -- log-sum-exp merge of the partitions written by
+ * paged_decode_split (same layouts, same partition_tokens and max_context_len):
+ *   M = max_r lse_r,  w_r = exp(lse_r - M),  out = bf16(sum_r w_r o_r / sum_r w_r)
+ * over the ceil(L / P) non-empty ranges of each sequence; L == 0 gives zeros.
+ */
+int paged_decode_combine(pkv_bf16 *out, const float *o_part, const float *lse_part,
+                         const int32_t *context_lens, int32_t max_context_len, int32_t num_seqs,
+                         int32_t num_q_heads, int32_t head_dim, int32_t partition_tokens,
+                         void *stream);
+
+/*
+ * pkv_device_errors -- synchronises the current device, then ORs the device error
+ * words of every kernel family into *flags (PKV_DEVERR_* bits; 0 = none seen since
+ * the last clear).  clear != 0 resets them.  Returns PKV_OK, or PKV_ERR_CUDA if
+ * the synchronisation or copy failed.  `flags` is HOST memory.
+ */
+int pkv_device_errors(uint32_t *flags, int clear);
+
+/* Message for the last error returned on the calling thread ("" if none). */
+const char *pkv_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_KV_H */

@@ -1,0 +1,218 @@
+"""Thin ctypes binding of libpkv.so: argument marshalling only.
+
+Every function has the name of the C entry point it calls (``include/paged_kv.h``),
+takes torch CUDA tensors, checks their dtypes/shapes/contiguity, and passes raw
+device pointers, sizes and the current CUDA stream.  All computation happens in
+the library's kernels; there is no fallback.  Importing this module raises if
+``libpkv.so`` has not been built.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpkv.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+PKV_OK = 0
+ERRORS = {-1: "PKV_ERR_NULL", -2: "PKV_ERR_SHAPE", -3: "PKV_ERR_UNSUPPORTED",
+          -4: "PKV_ERR_WORKSPACE", -5: "PKV_ERR_ALIGN", -6: "PKV_ERR_CUDA", -7: "PKV_ERR_DEVICE"}
+DEVERR = {1: "BLOCK_ID", 2: "SLOT", 4: "CONTEXT_LEN", 8: "TIMEOUT"}
+
+
+class PkvError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        msg = _lib.pkv_last_error().decode(errors="replace")
+        super().__init__(f"{where}: {ERRORS.get(code, code)}: {msg}")
+        self.code = code
+
+
+class pkv_cache_desc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int64), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+_P = ctypes.c_void_p
+_i32, _i64, _f32, _sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+_D = ctypes.POINTER(pkv_cache_desc)
+
+_lib.paged_kv_write.argtypes = [_P, _P, _P, _i64, _P, _P, _D, _P]
+_lib.paged_kv_write.restype = ctypes.c_int
+_lib.paged_decode_plan.argtypes = [_i32, _i32, _i32, _i32]
+_lib.paged_decode_plan.restype = _i32
+_lib.paged_decode_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32]
+_lib.paged_decode_workspace_size.restype = _sz
+_lib.paged_decode_split_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32]
+_lib.paged_decode_split_workspace_size.restype = _sz
+_lib.paged_decode_attention.argtypes = [_P, _P, _P, _P, _P, _i32, _P, _i32, _i32, _i32, _D, _f32,
+                                        _P, _sz, _P]
+_lib.paged_decode_attention.restype = ctypes.c_int
+_lib.paged_decode_split.argtypes = [_P, _P, _P, _P, _P, _P, _i32, _P, _i32, _i32, _i32, _D, _f32,
+                                    _i32, _P]
+_lib.paged_decode_split.restype = ctypes.c_int
+_lib.paged_decode_combine.argtypes = [_P, _P, _P, _P, _i32, _i32, _i32, _i32, _i32, _P]
+_lib.paged_decode_combine.restype = ctypes.c_int
+_lib.pkv_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
+_lib.pkv_device_errors.restype = ctypes.c_int
+_lib.pkv_last_error.argtypes = []
+_lib.pkv_last_error.restype = ctypes.c_char_p
+
+
+def lib() -> ctypes.CDLL:
+    return _lib
+
+
+def _check(rc: int, where: str):
+    if rc != PKV_OK:
+        raise PkvError(rc, where)
+
+
+def _stream(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: int):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name}: expected {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
+def cache_desc(k_cache: torch.Tensor) -> pkv_cache_desc:
+    NB, Hkv, BS, D = k_cache.shape
+    return pkv_cache_desc(NB, BS, Hkv, D)
+
+
+def paged_kv_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                   k_cache: torch.Tensor, v_cache: torch.Tensor, stream=None) -> None:
+    """k/v [T, Hkv, D] bf16 are copied into k_cache/v_cache [NB, Hkv, BS, D] at their slots."""
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    if k.shape != v.shape or k_cache.shape != v_cache.shape:
+        raise ValueError("k/v or k_cache/v_cache shapes differ")
+    if k.shape[0] != slot_mapping.shape[0] or tuple(k.shape[1:]) != (k_cache.shape[1], k_cache.shape[3]):
+        raise ValueError("k [T, Hkv, D] does not match slot_mapping [T] / cache [NB, Hkv, BS, D]")
+    d = cache_desc(k_cache)
+    _check(_lib.paged_kv_write(_ptr(k), _ptr(v), _ptr(slot_mapping), k.shape[0], _ptr(k_cache),
+                               _ptr(v_cache), ctypes.byref(d), _stream(stream)), "paged_kv_write")
+
+
+def paged_decode_plan(num_seqs: int, num_kv_heads: int, max_context_len: int, num_sms: int = 0) -> int:
+    return int(_lib.paged_decode_plan(num_seqs, num_kv_heads, max_context_len, num_sms))
+
+
+def paged_decode_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                                max_context_len: int) -> int:
+    return int(_lib.paged_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                max_context_len))
+
+
+def paged_decode_split_workspace_size(num_seqs: int, num_q_heads: int, head_dim: int,
+                                      max_context_len: int, partition_tokens: int) -> int:
+    return int(_lib.paged_decode_split_workspace_size(num_seqs, num_q_heads, head_dim,
+                                                      max_context_len, partition_tokens))
+
+
+def _decode_checks(q, k_cache, v_cache, block_tables, context_lens):
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    if k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    B = q.shape[0]
+    if block_tables.shape[0] != B or context_lens.shape[0] != B or q.shape[2] != k_cache.shape[3]:
+        raise ValueError("q [B, Hq, D], block_tables [B, M], context_lens [B], cache [NB, Hkv, BS, D] disagree")
+
+
+def paged_decode_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                           v_cache: torch.Tensor, block_tables: torch.Tensor,
+                           context_lens: torch.Tensor, max_context_len: int, scale: float,
+                           workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """out [B, Hq, D] bf16 = paged GQA decode attention (split + combine when the plan says so).
+
+    ``workspace`` (uint8, CUDA) may be omitted; then a buffer of
+    ``paged_decode_workspace_size`` bytes is taken from torch's caching allocator.
+    """
+    _decode_checks(q, k_cache, v_cache, block_tables, context_lens)
+    _need(out, "out", torch.bfloat16, 3)
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    B, Hq, D = q.shape
+    need = paged_decode_workspace_size(B, Hq, k_cache.shape[1], D, max_context_len)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    d = cache_desc(k_cache)
+    _check(_lib.paged_decode_attention(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                       _ptr(block_tables), block_tables.shape[1],
+                                       _ptr(context_lens), int(max_context_len), B, Hq,
+                                       ctypes.byref(d), float(scale), _ptr(workspace), ws_bytes,
+                                       _stream(stream)), "paged_decode_attention")
+
+
+def paged_decode_split(o_part: torch.Tensor, lse_part: torch.Tensor, q: torch.Tensor,
+                       k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                       context_lens: torch.Tensor, max_context_len: int, scale: float,
+                       partition_tokens: int, stream=None) -> None:
+    """o_part [B, Hq, n, D] fp32 and lse_part [B, Hq, n] fp32 for n = ceil(max_len / P)."""
+    _decode_checks(q, k_cache, v_cache, block_tables, context_lens)
+    _need(o_part, "o_part", torch.float32, 4)
+    _need(lse_part, "lse_part", torch.float32, 3)
+    B, Hq, D = q.shape
+    n = -(-int(max_context_len) // int(partition_tokens)) if partition_tokens > 0 else 0
+    if tuple(o_part.shape) != (B, Hq, n, D) or tuple(lse_part.shape) != (B, Hq, n):
+        raise ValueError(f"o_part must be {(B, Hq, n, D)} and lse_part {(B, Hq, n)}")
+    d = cache_desc(k_cache)
+    _check(_lib.paged_decode_split(_ptr(o_part), _ptr(lse_part), _ptr(q), _ptr(k_cache),
+                                   _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+                                   _ptr(context_lens), int(max_context_len), B, Hq,
+                                   ctypes.byref(d), float(scale), int(partition_tokens),
+                                   _stream(stream)), "paged_decode_split")
+
+
+def paged_decode_combine(out: torch.Tensor, o_part: torch.Tensor, lse_part: torch.Tensor,
+                         context_lens: torch.Tensor, max_context_len: int, partition_tokens: int,
+                         stream=None) -> None:
+    _need(out, "out", torch.bfloat16, 3)
+    _need(o_part, "o_part", torch.float32, 4)
+    _need(lse_part, "lse_part", torch.float32, 3)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    B, Hq, D = out.shape
+    _check(_lib.paged_decode_combine(_ptr(out), _ptr(o_part), _ptr(lse_part), _ptr(context_lens),
+                                     int(max_context_len), B, Hq, D, int(partition_tokens),
+                                     _stream(stream)), "paged_decode_combine")
+
+
+def pkv_device_errors(clear: bool = True) -> int:
+    """Synchronises the device and returns the device error bits (PKV_DEVERR_*)."""
+    f = ctypes.c_uint32(0)
+    _check(_lib.pkv_device_errors(ctypes.byref(f), 1 if clear else 0), "pkv_device_errors")
+    return int(f.value)
+
+
+def pkv_last_error() -> str:
+    return _lib.pkv_last_error().decode(errors="replace")

@@ -1,0 +1,334 @@
+"""CUDA path vs the CPU oracle, through the C ABI.
+
+Bar: the KV write is bit-exact (the whole pool is compared, so no other byte may
+change); attention is within |gpu - oracle| <= 1e-2 + 2^-8 |oracle| elementwise.
+The 1e-2 absolute bound is the stated target; the 2^-8 |oracle| term is the bf16
+output's own half-ulp, which only exceeds 1e-2 where |out| > 2.56 (a bf16 value
+can be no closer than that to the fp64 result).  Attention inputs carry NaN in
+every slot no sequence owns, so reading one shows up.
+"""
+
+import dataclasses
+import math
+
+import pytest
+import torch
+
+from paged_kv_decode_mapping_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+ATOL = 1e-2
+RTOL = 2.0 ** -8
+
+
+@pytest.fixture(scope="module")
+def B():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_decode_mapping_gb300 import build
+
+    build.build()
+    from paged_kv_decode_mapping_gb300 import binding
+
+    binding.pkv_device_errors(clear=True)
+    return binding
+
+
+def dev(inp):
+    return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+
+
+def check_attention(got: torch.Tensor, ref: torch.Tensor, tag: str) -> float:
+    got = got.cpu().double()
+    assert torch.isfinite(got).all(), f"{tag}: non-finite output"
+    err = (got - ref).abs()
+    bad = err > ATOL + RTOL * ref.abs()
+    assert not bool(bad.any()), f"{tag}: {int(bad.sum())} outputs out of tolerance, max |diff| {err.max():.3e}"
+    return float(err.max())
+
+
+def step(B, g):
+    """One decode step as the benchmark runs it: slot write, then attention (launcher's plan)."""
+    B.paged_kv_write(g["k_new"], g["v_new"], g["slot_mapping"], g["k_cache"], g["v_cache"])
+    out = torch.empty_like(g["q"])
+    B.paged_decode_attention(out, g["q"], g["k_cache"], g["v_cache"], g["block_tables"],
+                             g["context_lens"], g["max_context_len"], g["scale"])
+    return out
+
+
+def assert_no_device_errors(B):
+    flags = B.pkv_device_errors(clear=True)
+    assert flags == 0, f"device error bits {flags:#x}"
+
+
+# --------------------------------------------------------------- full workloads
+@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
+def test_workload_step_matches_oracle(B, oracle, wid):
+    w = W.WORKLOADS[wid]
+    inp = W.make_inputs(w, poison=True)
+    g = dev(inp)
+    out = step(B, g)
+    torch.cuda.synchronize()
+    assert_no_device_errors(B)
+    ref, kc_ref, vc_ref = oracle.step(inp)
+    # KV write: every byte of both pools
+    assert torch.equal(g["k_cache"].cpu().view(torch.int16), kc_ref.view(torch.int16))
+    assert torch.equal(g["v_cache"].cpu().view(torch.int16), vc_ref.view(torch.int16))
+    e = check_attention(out, ref, w.name)
+    assert e <= ATOL or ref.abs().max() > 2.56, f"{w.name}: max |diff| {e}"
+
+
+@pytest.mark.parametrize("wid", [2, 5])
+def test_workload_explicit_partition(B, oracle, wid):
+    """The workload's own partition size (512 tokens for the long-context case) through the
+    explicit split + combine entry points."""
+    w = W.WORKLOADS[wid]
+    inp = W.make_inputs(dataclasses.replace(w, write="none"), poison=True)
+    g = dev(inp)
+    P = 512
+    n = math.ceil(inp["max_context_len"] / P)
+    Bn, Hq, D = inp["q"].shape
+    o_part = torch.empty(Bn, Hq, n, D, device="cuda")
+    lse = torch.empty(Bn, Hq, n, device="cuda")
+    B.paged_decode_split(o_part, lse, g["q"], g["k_cache"], g["v_cache"], g["block_tables"],
+                         g["context_lens"], inp["max_context_len"], inp["scale"], P)
+    out = torch.empty_like(g["q"])
+    B.paged_decode_combine(out, o_part, lse, g["context_lens"], inp["max_context_len"], P)
+    torch.cuda.synchronize()
+    assert_no_device_errors(B)
+    ref = oracle.decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_tables"],
+                        inp["context_lens"], inp["scale"])
+    check_attention(out, ref, w.name)
+    # sampled partials against the oracle's per-range results
+    for (b, h) in [(0, 0), (Bn - 1, Hq - 1), (Bn // 2, Hq // 3)]:
+        ro, rl = oracle.decode_partitions(b, h, n, P, inp["q"], inp["k_cache"], inp["v_cache"],
+                                          inp["block_tables"], inp["context_lens"], inp["scale"])
+        assert torch.allclose(o_part[b, h].cpu().double(), ro, atol=2e-3), (b, h)
+        assert torch.allclose(lse[b, h].cpu().double(), rl, atol=2e-3, rtol=1e-5), (b, h)
+
+
+# ------------------------------------------------------------------ small grid
+GRID = []
+for D in (64, 128):
+    for BS in (8, 16, 32, 128):
+        for (Hq, Hkv) in ((2, 2), (8, 2), (16, 2)):
+            GRID.append((D, BS, Hq, Hkv))
+GRID += [(128, 16, 24, 8), (64, 16, 32, 8), (64, 32, 6, 2), (128, 32, 10, 2), (64, 256, 14, 2),
+         (64, 64, 4, 4)]
+
+
+@pytest.mark.parametrize("D,BS,Hq,Hkv", GRID)
+def test_small_cases(B, oracle, D, BS, Hq, Hkv):
+    lens = (1, 15, 16, 17, 63, 64, 65, 130, 700, 1025)
+    w = W.small_workload(B=len(lens), Hq=Hq, Hkv=Hkv, D=D, BS=BS, lens=lens, seed=D + BS + Hq)
+    inp = W.make_inputs(w, poison=True)
+    g = dev(inp)
+    out = step(B, g)
+    ref, kc_ref, vc_ref = oracle.step(inp)
+    assert torch.equal(g["k_cache"].cpu().view(torch.int16), kc_ref.view(torch.int16))
+    check_attention(out, ref, f"auto plan D={D} BS={BS} G={Hq // Hkv}")
+    # every explicit partition size over the same (updated) cache
+    for P in (64, 128, 320, 1088):
+        n = math.ceil(inp["max_context_len"] / P)
+        o_part = torch.empty(w.B, Hq, n, D, device="cuda")
+        lse = torch.empty(w.B, Hq, n, device="cuda")
+        B.paged_decode_split(o_part, lse, g["q"], g["k_cache"], g["v_cache"], g["block_tables"],
+                             g["context_lens"], inp["max_context_len"], inp["scale"], P)
+        o2 = torch.empty_like(g["q"])
+        B.paged_decode_combine(o2, o_part, lse, g["context_lens"], inp["max_context_len"], P)
+        check_attention(o2, ref, f"P={P} D={D} BS={BS} G={Hq // Hkv}")
+    assert_no_device_errors(B)
+
+
+def test_single_pass_large_batch(B, oracle):
+    """Many (sequence, kv head) units and contexts up to 512 take the single-pass kernel."""
+    lens = tuple(int(x) for x in torch.randint(1, 513, (160,), generator=torch.Generator().manual_seed(4)))
+    w = W.small_workload(B=160, Hq=16, Hkv=4, D=64, BS=16, lens=lens, seed=5)
+    assert B.paged_decode_plan(160, 4, max(lens)) == 0
+    inp = W.make_inputs(w, poison=True)
+    g = dev(inp)
+    out = step(B, g)
+    ref, _, _ = oracle.step(inp)
+    check_attention(out, ref, "single pass B=160")
+    assert_no_device_errors(B)
+
+
+def test_split_partials_match_oracle(B, oracle):
+    w = W.small_workload(B=3, Hq=12, Hkv=4, D=128, BS=16, lens=(5, 300, 1000), seed=8, write="none")
+    inp = W.make_inputs(w, poison=True)
+    g = dev(inp)
+    P = 128
+    n = math.ceil(1000 / P)
+    o_part = torch.full((3, 12, n, 128), float("nan"), device="cuda")
+    lse = torch.full((3, 12, n), float("nan"), device="cuda")
+    B.paged_decode_split(o_part, lse, g["q"], g["k_cache"], g["v_cache"], g["block_tables"],
+                         g["context_lens"], 1000, inp["scale"], P)
+    for b in range(3):
+        L = int(inp["context_lens"][b])
+        for h in range(12):
+            ro, rl = oracle.decode_partitions(b, h, n, P, inp["q"], inp["k_cache"], inp["v_cache"],
+                                              inp["block_tables"], inp["context_lens"], inp["scale"])
+            k = math.ceil(L / P)
+            assert torch.allclose(o_part[b, h, :k].cpu().double(), ro[:k], atol=2e-3), (b, h)
+            assert torch.allclose(lse[b, h, :k].cpu().double(), rl[:k], atol=2e-3, rtol=1e-5), (b, h)
+            assert torch.isnan(lse[b, h, k:].cpu()).all(), "empty ranges must not be written"
+    assert_no_device_errors(B)
+
+
+def test_combine_alone(B, oracle):
+    """The combine kernel on partials computed by the oracle."""
+    w = W.small_workload(B=2, Hq=4, Hkv=2, D=64, BS=16, lens=(900, 1), seed=9, write="none")
+    inp = W.make_inputs(w)
+    P = 64
+    n = math.ceil(900 / P)
+    o_part = torch.zeros(2, 4, n, 64, dtype=torch.float64)
+    lse = torch.zeros(2, 4, n, dtype=torch.float64)
+    for b in range(2):
+        for h in range(4):
+            o_part[b, h], lse[b, h] = oracle.decode_partitions(
+                b, h, n, P, inp["q"], inp["k_cache"], inp["v_cache"], inp["block_tables"],
+                inp["context_lens"], inp["scale"])
+    out = torch.empty(2, 4, 64, dtype=torch.bfloat16, device="cuda")
+    B.paged_decode_combine(out, o_part.float().cuda(), lse.float().cuda(),
+                           inp["context_lens"].cuda(), 900, P)
+    ref = torch.stack([torch.stack([oracle.lse_combine(o_part[b, h, :math.ceil(int(inp['context_lens'][b]) / P)],
+                                                       lse[b, h, :math.ceil(int(inp['context_lens'][b]) / P)])
+                                    for h in range(4)]) for b in range(2)])
+    check_attention(out, ref, "combine")
+
+
+# ------------------------------------------------------------------ edge cases
+def test_empty_and_length_one(B, oracle):
+    w = W.small_workload(B=4, Hq=8, Hkv=2, D=64, BS=16, lens=(0, 1, 0, 1), seed=12, write="none")
+    inp = W.make_inputs(w, poison=True)
+    g = dev(inp)
+    out = step(B, g)
+    o = out.cpu()
+    assert torch.equal(o[0], torch.zeros_like(o[0])) and torch.equal(o[2], torch.zeros_like(o[2]))
+    for b in (1, 3):  # one token: the output is that V row, bit for bit
+        phys = int(inp["block_tables"][b, 0])
+        for h in range(8):
+            assert torch.equal(o[b, h].view(torch.int16), inp["v_cache"][phys, h // 4, 0].view(torch.int16))
+    # split path with empty sequences: combine writes zeros
+    o_part = torch.empty(4, 8, 1, 64, device="cuda")
+    lse = torch.empty(4, 8, 1, device="cuda")
+    B.paged_decode_split(o_part, lse, g["q"], g["k_cache"], g["v_cache"], g["block_tables"],
+                         g["context_lens"], 1, inp["scale"], 64)
+    o2 = torch.full_like(g["q"], float("nan"))
+    B.paged_decode_combine(o2, o_part, lse, g["context_lens"], 1, 64)
+    assert torch.equal(o2.cpu().view(torch.int16), o.view(torch.int16))
+    assert_no_device_errors(B)
+
+
+def test_identical_keys_give_mean_of_v(B, oracle):
+    w = W.small_workload(B=2, Hq=8, Hkv=2, D=128, BS=32, lens=(333, 1200), seed=13, write="none")
+    inp = W.make_inputs(w)
+    inp["k_cache"][:] = inp["k_cache"][0, :, :1, :]
+    g = dev(inp)
+    out = step(B, g)
+    ref = oracle.decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_tables"],
+                        inp["context_lens"], inp["scale"])
+    check_attention(out, ref, "identical keys")
+    assert float(ref.abs().max()) < 0.5  # a mean of hundreds of N(0,1) values
+
+
+def test_pool_permutation_invariance(B):
+    """Moving the physical blocks (and rewriting the tables) changes no output bit."""
+    w = W.small_workload(B=3, Hq=24, Hkv=8, D=128, BS=16, lens=(100, 517, 2000), seed=14, write="none")
+    inp = W.make_inputs(w)
+    g = dev(inp)
+    out1 = step(B, g)
+    NB = inp["num_blocks"]
+    p = torch.randperm(NB, generator=torch.Generator().manual_seed(1))
+    kc = torch.empty_like(inp["k_cache"])
+    vc = torch.empty_like(inp["v_cache"])
+    kc[p] = inp["k_cache"]
+    vc[p] = inp["v_cache"]
+    tab = inp["block_tables"]
+    nt = torch.where(tab >= 0, p[tab.clamp(min=0).long()].to(torch.int32), tab)
+    g2 = dev(dict(inp, k_cache=kc, v_cache=vc, block_tables=nt))
+    out2 = step(B, g2)
+    assert torch.equal(out1.cpu().view(torch.int16), out2.cpu().view(torch.int16))
+
+
+def test_cached_decode_equals_recompute(B, oracle):
+    """Appending one token per step through the slot write, then decoding, equals the
+    oracle over the finished cache (the llm-stack KV-cache gate, on the GPU path)."""
+    w = W.small_workload(B=2, Hq=8, Hkv=2, D=64, BS=16, lens=(40, 90), seed=15, write="none")
+    inp = W.make_inputs(w)
+    gen = torch.Generator().manual_seed(2)
+    steps = 24
+    g = dev(inp)
+    lens = inp["context_lens"].clone() - steps
+    for s in range(steps):
+        kn = torch.randn(2, 2, 64, generator=gen).to(torch.bfloat16)
+        vn = torch.randn(2, 2, 64, generator=gen).to(torch.bfloat16)
+        slots = torch.tensor([int(inp["block_tables"][b, int(lens[b]) // 16]) * 16 + int(lens[b]) % 16
+                              for b in range(2)], dtype=torch.int64)
+        inp["k_cache"], inp["v_cache"] = oracle.kv_write(kn, vn, slots, inp["k_cache"], inp["v_cache"])
+        B.paged_kv_write(kn.cuda(), vn.cuda(), slots.cuda(), g["k_cache"], g["v_cache"])
+        lens += 1
+        out = torch.empty_like(g["q"])
+        B.paged_decode_attention(out, g["q"], g["k_cache"], g["v_cache"], g["block_tables"],
+                                 lens.to(torch.int32).cuda(), int(lens.max()), inp["scale"])
+        ref = oracle.decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_tables"],
+                            lens.to(torch.int32), inp["scale"])
+        check_attention(out, ref, f"step {s}")
+    assert torch.equal(g["k_cache"].cpu().view(torch.int16), inp["k_cache"].view(torch.int16))
+
+
+def test_write_skips_negative_slots_and_keeps_other_bytes(B, oracle):
+    w = W.small_workload(B=2, Hq=4, Hkv=4, D=128, BS=8, lens=(9, 30), seed=16, write="none")
+    inp = W.make_inputs(w)
+    NB = inp["num_blocks"]
+    slots = torch.tensor([0, -1, 7, NB * 8 - 1, -5, 13], dtype=torch.int64)
+    gen = torch.Generator().manual_seed(3)
+    kn = torch.randn(6, 4, 128, generator=gen).to(torch.bfloat16)
+    vn = torch.randn(6, 4, 128, generator=gen).to(torch.bfloat16)
+    kc, vc = inp["k_cache"].cuda(), inp["v_cache"].cuda()
+    B.paged_kv_write(kn.cuda(), vn.cuda(), slots.cuda(), kc, vc)
+    ek, ev = oracle.kv_write(kn, vn, slots, inp["k_cache"], inp["v_cache"])
+    assert torch.equal(kc.cpu().view(torch.int16), ek.view(torch.int16))
+    assert torch.equal(vc.cpu().view(torch.int16), ev.view(torch.int16))
+    assert_no_device_errors(B)
+
+
+def test_non_default_stream(B, oracle):
+    w = W.small_workload(B=2, Hq=8, Hkv=2, D=64, BS=16, lens=(700, 50), seed=17)
+    inp = W.make_inputs(w, poison=True)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        g = dev(inp)
+        out = step(B, g)
+    s.synchronize()
+    ref, _, _ = oracle.step(inp)
+    check_attention(out, ref, "side stream")
+
+
+# --------------------------------------------------------------- device errors
+def test_device_error_bits(B):
+    """Out-of-range block ids, slots and lengths are caught by the kernels' own bounds
+    checks: they raise a bit, never read or write outside the buffers."""
+    w = W.small_workload(B=2, Hq=8, Hkv=2, D=64, BS=16, lens=(40, 90), seed=18, write="none")
+    inp = W.make_inputs(w)
+    g = dev(inp)
+    B.pkv_device_errors(clear=True)
+    bad_tab = g["block_tables"].clone()
+    bad_tab[1, 2] = inp["num_blocks"] + 5
+    out = torch.empty_like(g["q"])
+    B.paged_decode_attention(out, g["q"], g["k_cache"], g["v_cache"], bad_tab, g["context_lens"],
+                             90, inp["scale"])
+    assert B.pkv_device_errors(clear=True) & 1
+    slots = torch.tensor([inp["num_blocks"] * 16 + 3], dtype=torch.int64, device="cuda")
+    kn = torch.zeros(1, 2, 64, dtype=torch.bfloat16, device="cuda")
+    before = g["k_cache"].clone()
+    B.paged_kv_write(kn, kn, slots, g["k_cache"], g["v_cache"])
+    assert B.pkv_device_errors(clear=True) & 2
+    assert torch.equal(before.view(torch.int16), g["k_cache"].view(torch.int16))
+    lens = g["context_lens"].clone()
+    lens[0] = 1000  # past the table's capacity: clamped
+    B.paged_decode_attention(out, g["q"], g["k_cache"], g["v_cache"], g["block_tables"], lens,
+                             90, inp["scale"])
+    assert B.pkv_device_errors(clear=True) & 4
+    assert B.pkv_device_errors(clear=True) == 0
