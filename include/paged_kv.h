@@ -174,6 +174,39 @@ int paged_decode_combine(pkv_bf16 *out, const float *o_part, const float *lse_pa
                          void *stream);
 
 /*
+ * paged_decode_attention_noalloc -- paged_decode_attention for callers that cannot
+ * allocate device memory.  (No counterpart in the paper: this is a library service.)
+ *
+ * Who needs it: code that may not call cudaMalloc or any allocator -- a host
+ * application or plugin framework that owns all device memory and gives out none,
+ * a latency-critical loop where an allocation (which can synchronise the device and
+ * take unbounded time) is not allowed, or a caller with no allocator of its own.
+ * Such callers cannot pass the workspace that paged_decode_attention needs when it
+ * splits long contexts.
+ *
+ * Same arguments and result as paged_decode_attention, without the workspace: the
+ * partition workspace lives in a fixed array of PKV_NOALLOC_SCRATCH_BYTES compiled
+ * into the library (every GPU that loads the library holds it until the process
+ * exits).  The call allocates nothing.
+ *  - Sizes whose plan needs more than PKV_NOALLOC_SCRATCH_BYTES of workspace
+ *    (paged_decode_workspace_size) are rejected with PKV_ERR_WORKSPACE and a message;
+ *    use paged_decode_attention with your own workspace for those.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) and caches it; make that first call outside any CUDA
+ *    stream capture.
+ *  - All calls share the one array, which keeps whatever the previous call left in
+ *    it; nothing in it has to start at zero.  Calls that overlap on the GPU (on
+ *    different streams, or from different threads without ordering) race on the
+ *    array and give wrong results: order them on one stream.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+int paged_decode_attention_noalloc(pkv_bf16 *out, const pkv_bf16 *q, const pkv_bf16 *k_cache,
+                                   const pkv_bf16 *v_cache, const int32_t *block_tables,
+                                   int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                   int32_t max_context_len, int32_t num_seqs, int32_t num_q_heads,
+                                   const pkv_cache_desc *cache, float scale, void *stream);
+
+/*
  * pkv_device_errors -- synchronises the current device, then ORs the device error
  * words of every kernel family into *flags (PKV_DEVERR_* bits; 0 = none seen since
  * the last clear).  clear != 0 resets them.  Returns PKV_OK, or PKV_ERR_CUDA if

@@ -62,6 +62,10 @@ _lib.paged_decode_split.argtypes = [_P, _P, _P, _P, _P, _P, _i32, _P, _i32, _i32
 _lib.paged_decode_split.restype = ctypes.c_int
 _lib.paged_decode_combine.argtypes = [_P, _P, _P, _P, _i32, _i32, _i32, _i32, _i32, _P]
 _lib.paged_decode_combine.restype = ctypes.c_int
+_lib.paged_decode_attention_noalloc.argtypes = [_P, _P, _P, _P, _P, _i32, _P, _i32, _i32, _i32,
+                                                _D, _f32, _P]
+_lib.paged_decode_attention_noalloc.restype = ctypes.c_int
+NOALLOC_SCRATCH_BYTES = 32 << 20  # PKV_NOALLOC_SCRATCH_BYTES in include/paged_kv.h
 _lib.pkv_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
 _lib.pkv_device_errors.restype = ctypes.c_int
 _lib.pkv_last_error.argtypes = []
@@ -172,6 +176,24 @@ def paged_decode_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Te
                                        _ptr(context_lens), int(max_context_len), B, Hq,
                                        ctypes.byref(d), float(scale), _ptr(workspace), ws_bytes,
                                        _stream(stream)), "paged_decode_attention")
+
+
+def paged_decode_attention_noalloc(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                                   v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                   context_lens: torch.Tensor, max_context_len: int, scale: float,
+                                   stream=None) -> None:
+    """paged_decode_attention without a workspace: the library's fixed scratch array is used."""
+    _decode_checks(q, k_cache, v_cache, block_tables, context_lens)
+    _need(out, "out", torch.bfloat16, 3)
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    B, Hq, D = q.shape
+    d = cache_desc(k_cache)
+    _check(_lib.paged_decode_attention_noalloc(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                               _ptr(block_tables), block_tables.shape[1],
+                                               _ptr(context_lens), int(max_context_len), B, Hq,
+                                               ctypes.byref(d), float(scale), _stream(stream)),
+           "paged_decode_attention_noalloc")
 
 
 def paged_decode_split(o_part: torch.Tensor, lse_part: torch.Tensor, q: torch.Tensor,

@@ -1,0 +1,83 @@
+// pkv_noalloc.cu -- paged_decode_attention for callers that cannot allocate device memory.
+//
+// paged_decode_attention needs a caller-provided workspace when the launcher splits
+// long contexts into partitions.  Some callers have no way to provide one: code that
+// runs where device allocation is forbidden or unsafe -- a host framework or plugin
+// that owns all device memory and hands out none, a real-time loop that must not call
+// cudaMalloc (it can synchronise the device and its latency is unbounded), or a
+// caller without a CUDA allocator of its own.  This entry point serves them: it runs
+// the same kernels with the partition workspace placed in a fixed array compiled into
+// the library, so the call itself allocates nothing.
+//
+// The array below is a file-scope __device__ variable.  Every GPU that loads the
+// library holds kNoAllocScratchBytes of it until the process exits.  In host code its
+// name is only a host-side stand-in, so its device address is fetched once per device
+// with cudaGetSymbolAddress and cached.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = PKV_NOALLOC_SCRATCH_BYTES;  // 32 MiB
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices];
+
+// Device address of g_noalloc_scratch on the current device (looked up once per device).
+int scratch_address(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_error(e, "paged_decode_attention_noalloc: cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices)
+    return set_error(PKV_ERR_CUDA, "paged_decode_attention_noalloc: device index %d", dev);
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p)
+      return cuda_error(e, "paged_decode_attention_noalloc: cudaGetSymbolAddress(scratch)");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+PKV_API int paged_decode_attention_noalloc(pkv_bf16 *out, const pkv_bf16 *q,
+                                           const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                                           const int32_t *block_tables,
+                                           int32_t max_blocks_per_seq,
+                                           const int32_t *context_lens, int32_t max_context_len,
+                                           int32_t num_seqs, int32_t num_q_heads,
+                                           const pkv_cache_desc *cache, float scale,
+                                           void *stream) {
+  using namespace pkv;
+  if (!cache) return set_error(PKV_ERR_NULL, "paged_decode_attention_noalloc: cache descriptor is NULL");
+  if (num_seqs < 0 || num_q_heads <= 0 || cache->num_kv_heads <= 0 || max_context_len < 0)
+    return set_error(PKV_ERR_SHAPE, "paged_decode_attention_noalloc: bad sizes");
+  // The size the launcher's plan needs, checked before any device call.
+  const size_t need = paged_decode_workspace_size(num_seqs, num_q_heads, cache->num_kv_heads,
+                                                  cache->head_dim, max_context_len);
+  if (need > kNoAllocScratchBytes)
+    return set_error(PKV_ERR_WORKSPACE,
+                     "paged_decode_attention_noalloc: these sizes need %zu bytes of partition "
+                     "workspace, more than the library's fixed %zu-byte scratch; call "
+                     "paged_decode_attention with a workspace instead",
+                     need, kNoAllocScratchBytes);
+  // First call on this device: look up the array's device address (see the header).
+  void *scratch = nullptr;
+  int rc = scratch_address(&scratch);
+  if (rc) return rc;
+  return paged_decode_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                context_lens, max_context_len, num_seqs, num_q_heads, cache,
+                                scale, scratch, need > 0 ? kNoAllocScratchBytes : 0, stream);
+}
