@@ -2,9 +2,11 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 2]
 
-A step is one pass of the whole hot path over one batch of synthetic input: the
-slot-mapping KV write of the step's new tokens, then decode attention as the
-launcher plans it (one kernel, or the split kernel + the log-sum-exp combine).
+A step is one pass of the whole hot path over one batch of synthetic input, through
+paged_decode_step: the slot-mapping KV write of the step's new tokens, then decode
+attention (launched as a programmatic dependent of the write) as the
+launcher plans it (one kernel: one CTA per partition; split sequences are merged by
+their last partition).
 
 Default workload: decode B=16, context 2048, 32 query / 8 kv heads, head_dim 64,
 bf16, block_size 16, block tables drawn from a shuffled pool of 2560 blocks, 16
@@ -18,7 +20,7 @@ torch.cuda.synchronize() and timed with CUDA events on the launching stream; the
 max over ranks is reported.  `value` is algorithmic HBM bytes per step / time,
 in GB/s (whole job: all ranks' bytes / the slowest rank's time).
 
-`roofline` covers the dominant kernel (the decode/split kernel), timed alone by
+`roofline` covers the dominant kernel (the decode kernel), timed alone by
 the same method; `e2e` runs the same step eagerly through the public API with the
 step's inputs copied from pinned host memory and the output read back each step;
 `cpu_baseline` is the CPU oracle (fp64, all host cores) on the same workload.
@@ -268,7 +270,7 @@ def run_ours(args, w) -> None:
     NB, Hkv, BS, _ = inp["k_cache"].shape
     max_len = inp["max_context_len"]
     scale = inp["scale"]
-    P = B.paged_decode_plan(Bn, Hkv, max_len)
+    P = B.paged_decode_plan(Bn, Hq, Hkv, D, max_len)
 
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     pool_bytes = 2 * inp["k_cache"].numel() * 2
@@ -281,21 +283,13 @@ def run_ours(args, w) -> None:
     kn, vn, sm = inp["k_new"].to(device), inp["v_new"].to(device), inp["slot_mapping"].to(device)
     out = torch.empty_like(q)
     ws_bytes = B.paged_decode_workspace_size(Bn, Hq, Hkv, D, max_len)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=device)
-    n_parts = math.ceil(max_len / P) if P else 0
-    if P:
-        o_part = torch.empty(Bn, Hq, n_parts, D, dtype=torch.float32, device=device)
-        lse_part = torch.empty(Bn, Hq, n_parts, dtype=torch.float32, device=device)
+    ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=device)  # counters start at 0
 
     def step(r):
-        B.paged_kv_write(kn, vn, sm, kcs[r], vcs[r])
-        B.paged_decode_attention(out, q, kcs[r], vcs[r], bt, cl, max_len, scale, workspace=ws)
+        B.paged_decode_step(out, q, kn, vn, sm, kcs[r], vcs[r], bt, cl, max_len, scale, workspace=ws)
 
     def decode_only(r):
-        if P:
-            B.paged_decode_split(o_part, lse_part, q, kcs[r], vcs[r], bt, cl, max_len, scale, P)
-        else:
-            B.paged_decode_attention(out, q, kcs[r], vcs[r], bt, cl, max_len, scale, workspace=ws)
+        B.paged_decode_attention(out, q, kcs[r], vcs[r], bt, cl, max_len, scale, workspace=ws)
 
     stream = torch.cuda.Stream(device)
     torch.cuda.synchronize()
@@ -365,8 +359,8 @@ def run_ours(args, w) -> None:
     def e2e_step(r):
         for dst, src in zip((dq, dkn, dvn, dsm, dbt, dcl), host.values()):
             dst.copy_(src, non_blocking=True)
-        B.paged_kv_write(dkn, dvn, dsm, kcs[r], vcs[r])
-        B.paged_decode_attention(out, dq, kcs[r], vcs[r], dbt, dcl, max_len, scale, workspace=ws)
+        B.paged_decode_step(out, dq, dkn, dvn, dsm, kcs[r], vcs[r], dbt, dcl, max_len, scale,
+                            workspace=ws)
         out_h.copy_(out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
@@ -389,7 +383,7 @@ def run_ours(args, w) -> None:
     peak_src = "measured" if peak else "fallback"
     peak = peak or 6800.0
     traffic = recorded_traffic(os.path.join(ROOT, "paged_kv_decode_mapping_gb300", "csrc", "pkv_decode.cu"))
-    launches_per_step = 1 + (2 if P else 1)
+    launches_per_step = 2  # kv_write_kernel + decode_kernel (merge fused)
 
     if rank != 0:
         if world > 1:
@@ -404,8 +398,8 @@ def run_ours(args, w) -> None:
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": config_dict(w, inp, args, world),
         "hbm_frac_of_peak": value / peak,
-        "plan": {"partition_tokens": P, "n_parts": n_parts, "pool_copies": R},
-        "roofline": {"bound": "hbm", "kernel": "decode_kernel" + (" (split)" if P else ""),
+        "plan": {"partition_tokens": P, "n_parts": math.ceil(max_len / P), "pool_copies": R},
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel (partitions + fused merge)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_src} hbm_gbs (copy, burst)",
                      "bytes_per_launch": nb["decode_kernel"], "us_per_launch": dec_s * 1e6,

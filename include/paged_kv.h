@@ -92,24 +92,27 @@ int paged_kv_write(const pkv_bf16 *k, const pkv_bf16 *v, const int64_t *slot_map
  * paged_decode_plan -- the launcher's split choice ("vLLM-Style Llama Inference
  * Engine", Features and scope, where split-K decode is the named next step).
  *
- * Returns the partition size in tokens (a multiple of 64) that
- * paged_decode_attention will use, or 0 for a single pass per (sequence, kv
- * head).  It depends only on its arguments: short contexts take one pass; longer
- * ones are cut into partitions so that the grid covers the GPU several times.
- * num_sms <= 0 queries the current device.  Pure host function.
+ * Returns the partition size P in tokens (a multiple of 64) that
+ * paged_decode_attention cuts each (sequence, kv head) into; one CTA streams one
+ * partition.  With few (sequence, kv head) units, P is chosen so that the
+ * partitions make about one wave of CTAs on this GPU; with many, P = 1024.  P is
+ * never below min(max_context_len, 512) rounded up to 64, so short contexts stay
+ * whole.  0 for empty or unsupported sizes.  num_sms <= 0 queries the current
+ * device.  Pure host function.
  */
-int32_t paged_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t max_context_len,
-                          int32_t num_sms);
+int32_t paged_decode_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                          int32_t head_dim, int32_t max_context_len, int32_t num_sms);
 
 /*
- * paged_decode_workspace_size -- bytes of workspace paged_decode_attention needs
- * for these sizes on the current device (0 when the plan is a single pass).
- * Equals paged_decode_split_workspace_size(..., paged_decode_plan(...)).
+ * paged_decode_workspace_size -- bytes of workspace paged_decode_attention needs for
+ * these sizes on the current device: a completion counter per (sequence, kv head),
+ * then the partition results of paged_decode_split's layout for P =
+ * paged_decode_plan(...).  0 for empty sizes.
  */
 size_t paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                    int32_t head_dim, int32_t max_context_len);
 
-/* Bytes of o_part + lse_part (padded to 256 B) for an explicit partition size. */
+/* Bytes of o_part + lse_part (padded to 256 B) of paged_decode_split for a partition size. */
 size_t paged_decode_split_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
                                          int32_t max_context_len, int32_t partition_tokens);
 
@@ -129,11 +132,16 @@ size_t paged_decode_split_workspace_size(int32_t num_seqs, int32_t num_q_heads, 
  *
  * Supported: head_dim 64 or 128; block_size a power of two in [8, 256];
  * num_q_heads / num_kv_heads (the group) from 1 to 8.  q, k_cache, v_cache and
- * workspace 16-byte aligned; out 4-byte aligned.
+ * workspace 16-byte aligned; out 8-byte aligned.
  *
- * The work is split as paged_decode_plan() says: either one kernel, or
- * paged_decode_split() into `workspace` followed by paged_decode_combine().
- * `workspace` may be NULL when paged_decode_workspace_size() is 0.
+ * One kernel launch (see paged_decode_plan): a sequence that fits one partition is
+ * written directly; otherwise each partition stores its result in the workspace and
+ * the last partition of that (sequence, kv head) to finish merges them (an atomic
+ * ticket; no CTA waits for another).
+ * `workspace` must hold paged_decode_workspace_size() bytes and must be ZERO-FILLED
+ * before its first use (it holds completion counters); every call that completes
+ * leaves it ready for the next one.  Calls that share a workspace must not overlap
+ * on the GPU.
  */
 int paged_decode_attention(pkv_bf16 *out, const pkv_bf16 *q, const pkv_bf16 *k_cache,
                            const pkv_bf16 *v_cache, const int32_t *block_tables,
@@ -141,6 +149,25 @@ int paged_decode_attention(pkv_bf16 *out, const pkv_bf16 *q, const pkv_bf16 *k_c
                            int32_t max_context_len, int32_t num_seqs, int32_t num_q_heads,
                            const pkv_cache_desc *cache, float scale, void *workspace,
                            size_t workspace_bytes, void *stream);
+
+/*
+ * paged_decode_step -- one whole decode step: paged_kv_write(k, v, slot_mapping,
+ * num_tokens, ...) into the caches, then paged_decode_attention over the updated
+ * caches ("vLLM-Style Llama Inference Engine", How it works: each rank writes its
+ * new K/V into the paged cache, then one-token decode runs paged attention).
+ *
+ * Arguments, layouts, workspace rules and results are those of the two calls; both
+ * are checked before either is enqueued.  The attention kernel is launched as a
+ * programmatic dependent of the write kernel: its set-up (reading q, context_lens
+ * and block_tables) overlaps the write, and it reads the caches only after the
+ * write's stores are visible.
+ */
+int paged_decode_step(pkv_bf16 *out, const pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v,
+                      const int64_t *slot_mapping, int64_t num_tokens, pkv_bf16 *k_cache,
+                      pkv_bf16 *v_cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                      const int32_t *context_lens, int32_t max_context_len, int32_t num_seqs,
+                      int32_t num_q_heads, const pkv_cache_desc *cache, float scale,
+                      void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * paged_decode_split -- flash-decoding partition kernel (split-K over the keys;
@@ -195,9 +222,10 @@ int paged_decode_combine(pkv_bf16 *out, const float *o_part, const float *lse_pa
  *    (cudaGetSymbolAddress) and caches it; make that first call outside any CUDA
  *    stream capture.
  *  - All calls share the one array, which keeps whatever the previous call left in
- *    it; nothing in it has to start at zero.  Calls that overlap on the GPU (on
- *    different streams, or from different threads without ordering) race on the
- *    array and give wrong results: order them on one stream.
+ *    it.  The part that must start at zero (the completion counters) is cleared by
+ *    each call on its stream before the kernel runs.  Calls that overlap on the GPU
+ *    (on different streams, or from different threads without ordering) race on
+ *    the array and give wrong results: order them on one stream.
  */
 #define PKV_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 int paged_decode_attention_noalloc(pkv_bf16 *out, const pkv_bf16 *q, const pkv_bf16 *k_cache,

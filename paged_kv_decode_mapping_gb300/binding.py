@@ -48,7 +48,7 @@ _D = ctypes.POINTER(pkv_cache_desc)
 
 _lib.paged_kv_write.argtypes = [_P, _P, _P, _i64, _P, _P, _D, _P]
 _lib.paged_kv_write.restype = ctypes.c_int
-_lib.paged_decode_plan.argtypes = [_i32, _i32, _i32, _i32]
+_lib.paged_decode_plan.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
 _lib.paged_decode_plan.restype = _i32
 _lib.paged_decode_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32]
 _lib.paged_decode_workspace_size.restype = _sz
@@ -57,6 +57,9 @@ _lib.paged_decode_split_workspace_size.restype = _sz
 _lib.paged_decode_attention.argtypes = [_P, _P, _P, _P, _P, _i32, _P, _i32, _i32, _i32, _D, _f32,
                                         _P, _sz, _P]
 _lib.paged_decode_attention.restype = ctypes.c_int
+_lib.paged_decode_step.argtypes = [_P, _P, _P, _P, _P, _i64, _P, _P, _P, _i32, _P, _i32, _i32,
+                                   _i32, _D, _f32, _P, _sz, _P]
+_lib.paged_decode_step.restype = ctypes.c_int
 _lib.paged_decode_split.argtypes = [_P, _P, _P, _P, _P, _P, _i32, _P, _i32, _i32, _i32, _D, _f32,
                                     _i32, _P]
 _lib.paged_decode_split.restype = ctypes.c_int
@@ -123,8 +126,11 @@ def paged_kv_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
                                _ptr(v_cache), ctypes.byref(d), _stream(stream)), "paged_kv_write")
 
 
-def paged_decode_plan(num_seqs: int, num_kv_heads: int, max_context_len: int, num_sms: int = 0) -> int:
-    return int(_lib.paged_decode_plan(num_seqs, num_kv_heads, max_context_len, num_sms))
+def paged_decode_plan(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                      max_context_len: int, num_sms: int = 0) -> int:
+    """Partition size (tokens) paged_decode_attention cuts each (sequence, kv head) into."""
+    return int(_lib.paged_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                      max_context_len, num_sms))
 
 
 def paged_decode_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
@@ -158,8 +164,8 @@ def paged_decode_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Te
                            workspace: Optional[torch.Tensor] = None, stream=None) -> None:
     """out [B, Hq, D] bf16 = paged GQA decode attention (split + combine when the plan says so).
 
-    ``workspace`` (uint8, CUDA) may be omitted; then a buffer of
-    ``paged_decode_workspace_size`` bytes is taken from torch's caching allocator.
+    ``workspace`` (uint8, CUDA, zero-filled before its first use) may be omitted; then a
+    zeroed buffer of ``paged_decode_workspace_size`` bytes is taken from torch's allocator.
     """
     _decode_checks(q, k_cache, v_cache, block_tables, context_lens)
     _need(out, "out", torch.bfloat16, 3)
@@ -168,7 +174,7 @@ def paged_decode_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Te
     B, Hq, D = q.shape
     need = paged_decode_workspace_size(B, Hq, k_cache.shape[1], D, max_context_len)
     if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     d = cache_desc(k_cache)
     _check(_lib.paged_decode_attention(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
@@ -176,6 +182,32 @@ def paged_decode_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Te
                                        _ptr(context_lens), int(max_context_len), B, Hq,
                                        ctypes.byref(d), float(scale), _ptr(workspace), ws_bytes,
                                        _stream(stream)), "paged_decode_attention")
+
+
+def paged_decode_step(out: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                      slot_mapping: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      block_tables: torch.Tensor, context_lens: torch.Tensor,
+                      max_context_len: int, scale: float, workspace: Optional[torch.Tensor] = None,
+                      stream=None) -> None:
+    """One decode step: the slot write of k/v, then attention over the updated caches."""
+    _decode_checks(q, k_cache, v_cache, block_tables, context_lens)
+    _need(out, "out", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1)
+    if out.shape != q.shape or k.shape != v.shape or k.shape[0] != slot_mapping.shape[0]:
+        raise ValueError("out/q, k/v or slot_mapping shapes disagree")
+    B, Hq, D = q.shape
+    need = paged_decode_workspace_size(B, Hq, k_cache.shape[1], D, max_context_len)
+    if workspace is None and need > 0:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    d = cache_desc(k_cache)
+    _check(_lib.paged_decode_step(_ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(slot_mapping),
+                                  k.shape[0], _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                  block_tables.shape[1], _ptr(context_lens), int(max_context_len),
+                                  B, Hq, ctypes.byref(d), float(scale), _ptr(workspace), ws_bytes,
+                                  _stream(stream)), "paged_decode_step")
 
 
 def paged_decode_attention_noalloc(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,

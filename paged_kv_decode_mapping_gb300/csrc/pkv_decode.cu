@@ -1,5 +1,6 @@
-// pkv_decode.cu -- paged decode attention: single-pass / flash-decoding partition
-// kernel, log-sum-exp combine kernel, and the host launcher.
+// pkv_decode.cu -- paged decode attention: the flash-decoding partition kernel (fused
+// with its merge for paged_decode_attention; partials only for paged_decode_split),
+// the log-sum-exp combine kernel of paged_decode_combine, and the host launcher.
 //
 // What is computed ("mini-vLLM" README, paged KV-cache paragraph and M4 test row;
 // "vLLM-Style Llama Inference Engine", Features and scope / How it works;
@@ -7,25 +8,30 @@
 //   for sequence b, query head h, kv head g = h / G, positions t < L_b:
 //     K_t = k_cache[block_tables[b][t / BS]][g][t % BS],  s_t = scale * <q, K_t>,
 //     out = sum_t softmax(s)_t V_t.
-// The flash-decoding split and its merge follow the online-softmax algebra of
-// FlashAttention-2 (the reference the first page lists).
+// Splitting the keys of one (b, g) into partitions and merging the partitions'
+// (output, log-sum-exp) follows the online-softmax algebra of FlashAttention-2 (the
+// reference the first page lists).
 //
 // Design (GB300, sm_103a).  The path is HBM-bound: each K/V byte is read once and
-// feeds G fused multiply-adds per query head group.  One CTA owns one (sequence,
-// kv head, partition) and reads every K/V row of that range exactly once for all
-// G query heads of the group.
+// feeds G fused multiply-adds per query head group.  A CTA streams K/V rows of one
+// kv head for all G query heads of the group at once.
 //  * Staging: a producer warp walks the block table and issues 2-D/3-D tiled TMA
 //    loads (cp.async.bulk.tensor, 128-byte swizzle, L2 evict-first) of whole KV
-//    blocks into a ring of STAGES shared-memory stages of 64 keys each; mbarriers
-//    with transaction counts signal "full", consumer arrivals signal "empty".
-//  * Compute: four consumer warps take 16 keys of each stage.  The tiny products
-//    S^T = K_tile . Q^T (16 keys x 8 heads x D) and O^T += V^T . P^T run on the
-//    tensor pipe (mma.sync m16n8k16, bf16 in, fp32 accumulate); the query group is
-//    padded to 8 heads.  P is fed as a bf16 hi + lo pair, so the products keep
-//    ~16 significant bits.  Online softmax in fp32 (base 2), warp-shuffle maxima.
-//  * Each warp keeps its own running (m, l, O); the four are merged through shared
-//    memory at the end.  Single pass: bf16 output.  Split: normalised fp32 o_part
-//    and natural-log lse_part, merged by combine_kernel.
+//    blocks into a ring of shared-memory stages of 64 keys; mbarriers with
+//    transaction counts signal "full", consumer-warp arrivals signal "empty".
+//  * Compute: four consumer warps take 16 keys of each stage.  S^T = K_tile . Q^T
+//    (16 keys x 8 heads x D) and O^T += V^T . P^T run on the tensor pipe
+//    (mma.sync m16n8k16, bf16 in, fp32 accumulate); the group is padded to 8 heads;
+//    P enters as a bf16 hi + lo pair (~16 significant bits).  Online softmax in fp32
+//    (base 2) with warp-shuffle maxima; each warp keeps its own (m, l, O), merged
+//    through shared memory at the end of a segment.
+//  * decode_kernel: one CTA per (sequence, kv head, partition of P tokens); the
+//    launcher sizes P so that few (sequence, kv head) units still fill about one wave
+//    of long partitions, and many units take 1024-token partitions.  For
+//    paged_decode_attention it runs fused: a sequence with one partition writes bf16
+//    directly; otherwise each partition writes its (o, lse) and the last of them to
+//    finish (atomic ticket per (sequence, kv head); nobody waits) merges them.  For
+//    paged_decode_split it only writes the partials, merged by combine_kernel.
 // Every wait is bounded (about 2 s); on a timeout the kernel raises
 // PKV_DEVERR_TIMEOUT and unwinds instead of hanging.
 #include <cuda.h>  // CUtensorMap and its enums (header only; the entry point is fetched at run time)
@@ -36,6 +42,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
 
 #include "pkv_internal.h"
@@ -44,25 +51,19 @@ namespace pkv {
 
 constexpr int kChunk = 64;          // keys per pipeline stage
 constexpr int kConsumerWarps = 4;   // 16 keys each
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;
 constexpr int kMaxGroup = 8;        // query heads per kv head (one mma N tile)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 __device__ unsigned int g_decode_errors;
 
-struct DecodeArgs {
-  const uint16_t *q;           // [B][Hq][D] bf16
-  const int32_t *block_tables; // [B][max_blocks]
-  const int32_t *context_lens; // [B]
-  uint16_t *out;               // single pass: [B][Hq][D] bf16
-  float *o_part;               // split: [B][Hq][n_parts][D]
-  float *lse_part;             // split: [B][Hq][n_parts]
-  int64_t num_blocks;
-  int32_t max_blocks, max_context_len, num_q_heads, num_kv_heads, group;
-  int32_t block_size, log2_bs, box_rows, partition_tokens, n_parts, split;
-  float scale_log2;            // scale * log2(e)
-};
+__device__ __forceinline__ void raise_error(unsigned bit) { atomicOr(&g_decode_errors, bit); }
+
+__device__ __forceinline__ void consumer_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
 
 // Byte offset of 16-byte chunk `dch` (0 .. D/8-1) of key row `key` in a stage tile.
 // The tile is D/64 sub-tiles [64 keys][128 B], each filled by 128-byte-swizzled TMA
@@ -72,6 +73,7 @@ __device__ __forceinline__ uint32_t tile_off(int key, int dch) {
   return (uint32_t)((dch >> 3) * (kChunk * 128) + key * 128 + (((dch & 7) ^ (key & 7)) << 4));
 }
 
+// One TMA box (rb rows of one KV block, all head dims) of K and of V.
 template <int D>
 __device__ __forceinline__ void issue_box(uint32_t dst_k, uint32_t dst_v, const CUtensorMap *tmk,
                                           const CUtensorMap *tmv, int32_t row, uint32_t bar,
@@ -97,13 +99,250 @@ __device__ __forceinline__ void issue_box(uint32_t dst_k, uint32_t dst_v, const 
   }
 }
 
+// ---------------------------------------------------------------------------
+// Per-warp state and the per-stage work of a consumer warp.
+
+template <int D>
+struct WarpAcc {
+  float o[D / 16][4];  // O^T fragment: dims (16*mt + gid, +8) x heads (2*tig, 2*tig+1)
+  float m0, m1, l0, l1;  // running max (base 2) and partial sum for heads 2*tig, 2*tig+1
+};
+
+template <int D>
+__device__ __forceinline__ void acc_reset(WarpAcc<D> &a) {
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt) a.o[mt][0] = a.o[mt][1] = a.o[mt][2] = a.o[mt][3] = 0.f;
+  a.m0 = a.m1 = -INFINITY;
+  a.l0 = a.l1 = 0.f;
+}
+
+// QK, online softmax and PV for this warp's 16 keys (nvalid of them in range) of the
+// stage whose K tile is at kb and V tile at vb.
+template <int D>
+__device__ __forceinline__ void warp_tile(WarpAcc<D> &acc, const uint32_t (&qb)[D / 16][2],
+                                          uint32_t kb, uint32_t vb, int warp, int lane, int nvalid,
+                                          float scale_log2) {
+  constexpr int KS = D / 16;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int lj = lane >> 3, lr = lane & 7;  // ldmatrix: matrix index / row within it
+  // QK operand A = K rows: matrices (keys 0-7 | 8-15) x (dims lo | hi) of a k step.
+  const int qk_key = 16 * warp + lr + ((lj & 1) << 3), qk_dsel = lj >> 1;
+  // PV operand A = V^T: matrices (keys 0-7, dims lo), (keys 0-7, dims hi), (keys 8-15, ...).
+  const int pv_key = 16 * warp + lr + ((lj >> 1) << 3), pv_dsel = lj & 1;
+
+  // S^T (16 keys x 8 heads) = K_tile . Q^T
+  float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks) {
+    uint32_t ak[4];
+    dev::ldsm_x4(ak, kb + tile_off(qk_key, 2 * ks + qk_dsel));
+    dev::mma_bf16_16816(sc, ak, qb[ks][0], qb[ks][1]);
+  }
+  // scale to base 2, mask keys past the range
+  const bool v0 = gid < nvalid, v1 = gid + 8 < nvalid;
+  const float s0 = v0 ? sc[0] * scale_log2 : -INFINITY;
+  const float s1 = v0 ? sc[1] * scale_log2 : -INFINITY;
+  const float s2 = v1 ? sc[2] * scale_log2 : -INFINITY;
+  const float s3 = v1 ? sc[3] * scale_log2 : -INFINITY;
+  float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+  for (int x = 4; x < 32; x <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, x));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, x));
+  }
+  const float mn0 = fmaxf(acc.m0, mx0), mn1 = fmaxf(acc.m1, mx1);
+  const float al0 = dev::ex2(acc.m0 - mn0), al1 = dev::ex2(acc.m1 - mn1);
+  const float p0 = dev::ex2(s0 - mn0), p1 = dev::ex2(s1 - mn1);
+  const float p2 = dev::ex2(s2 - mn0), p3 = dev::ex2(s3 - mn1);
+  acc.l0 = acc.l0 * al0 + (p0 + p2);
+  acc.l1 = acc.l1 * al1 + (p1 + p3);
+  acc.m0 = mn0;
+  acc.m1 = mn1;
+#pragma unroll
+  for (int mt = 0; mt < KS; ++mt) {
+    acc.o[mt][0] *= al0;
+    acc.o[mt][1] *= al1;
+    acc.o[mt][2] *= al0;
+    acc.o[mt][3] *= al1;
+  }
+  // P^T as the B operand: bf16 hi part and the bf16 residual, transposed
+  const uint32_t h01 = dev::pack_bf16x2(p0, p1), h23 = dev::pack_bf16x2(p2, p3);
+  const uint32_t r01 = dev::pack_bf16x2(p0 - dev::bf16lo_to_f32(h01), p1 - dev::bf16hi_to_f32(h01));
+  const uint32_t r23 = dev::pack_bf16x2(p2 - dev::bf16lo_to_f32(h23), p3 - dev::bf16hi_to_f32(h23));
+  const uint32_t bh0 = dev::movmatrix_trans(h01), bh1 = dev::movmatrix_trans(h23);
+  const uint32_t bl0 = dev::movmatrix_trans(r01), bl1 = dev::movmatrix_trans(r23);
+  // O^T (D x 8 heads) += V^T . P^T; rows of V past the range are zeroed in registers
+  // (never multiply an unloaded row: 0 * NaN would poison O)
+  uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+  if (nvalid < 16) {
+    const int kk = 2 * tig;
+    mlo = (kk < nvalid ? 0x0000ffffu : 0u) | (kk + 1 < nvalid ? 0xffff0000u : 0u);
+    mhi = (kk + 8 < nvalid ? 0x0000ffffu : 0u) | (kk + 9 < nvalid ? 0xffff0000u : 0u);
+  }
+#pragma unroll
+  for (int mt = 0; mt < KS; ++mt) {
+    uint32_t av[4];
+    dev::ldsm_x4_trans(av, vb + tile_off(pv_key, 2 * mt + pv_dsel));
+    av[0] &= mlo;
+    av[1] &= mlo;
+    av[2] &= mhi;
+    av[3] &= mhi;
+    dev::mma_bf16_16816(acc.o[mt], av, bh0, bh1);
+    dev::mma_bf16_16816(acc.o[mt], av, bl0, bl1);
+  }
+}
+
+// Merge area of the four warps: red_o [warps][G][D], red_m / red_l [warps][8].
+struct MergeArea {
+  float *o, *m, *l;
+};
+
+// Reduces l over the warp and writes the warp's (m, l, O) for heads < G.
+template <int D>
+__device__ __forceinline__ void warp_stash(WarpAcc<D> &acc, const MergeArea &r, int G, int warp,
+                                           int lane) {
+  const int gid = lane >> 2, tig = lane & 3;
+  float l0 = acc.l0, l1 = acc.l1;
+#pragma unroll
+  for (int x = 4; x < 32; x <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, x);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, x);
+  }
+  const int h0 = 2 * tig, h1 = h0 + 1;
+  if (gid == 0) {
+    r.m[warp * kMaxGroup + h0] = acc.m0;
+    r.m[warp * kMaxGroup + h1] = acc.m1;
+    r.l[warp * kMaxGroup + h0] = l0;
+    r.l[warp * kMaxGroup + h1] = l1;
+  }
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt) {
+    const int d = 16 * mt + gid;
+    if (h0 < G) {
+      r.o[(warp * G + h0) * D + d] = acc.o[mt][0];
+      r.o[(warp * G + h0) * D + d + 8] = acc.o[mt][2];
+    }
+    if (h1 < G) {
+      r.o[(warp * G + h1) * D + d] = acc.o[mt][1];
+      r.o[(warp * G + h1) * D + d + 8] = acc.o[mt][3];
+    }
+  }
+}
+
+// The four warps' softmax states merged for head h, dim d: the normalised output;
+// *M2 gets the base-2 max and *den the sum, so lse2 = *M2 + log2(*den).  A warp that
+// saw no key has m = -inf and weighs nothing.
+template <int D>
+__device__ __forceinline__ float cta_merge(const MergeArea &r, int G, int h, int d, float *M2,
+                                           float *den) {
+  float M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, r.m[w * kMaxGroup + h]);
+  float num = 0.f, dn = 0.f;
+#pragma unroll
+  for (int w = 0; w < kConsumerWarps; ++w) {
+    const float wt = dev::ex2(r.m[w * kMaxGroup + h] - M);
+    num += wt * r.o[(w * G + h) * D + d];
+    dn += wt * r.l[w * kMaxGroup + h];
+  }
+  *M2 = M;
+  *den = dn;
+  return num / dn;
+}
+
+__device__ __forceinline__ uint16_t to_bf16(float x) {
+  return (uint16_t)(dev::pack_bf16x2(x, 0.f) & 0xffffu);
+}
+
+// Merges the n partition results of one query head -- row p: normalised output
+// o_rows[p*D .. p*D+D) and natural-log lse_rows[p] -- into bf16 dst[0 .. D).  One warp:
+// each lane owns D/32 dims; partitions are read 8 at a time with all loads in flight
+// and folded in with the online-softmax rule.  Loads bypass L1 (__ldcg): the rows were
+// written by other CTAs.
+template <int D>
+__device__ __forceinline__ void merge_rows(uint16_t *dst, const float *o_rows,
+                                           const float *lse_rows, int n, int lane) {
+  constexpr int VPL = D / 32;
+  float M = -INFINITY, den = 0.f, acc[VPL];
+#pragma unroll
+  for (int v = 0; v < VPL; ++v) acc[v] = 0.f;
+  for (int k0 = 0; k0 < n; k0 += 8) {
+    float lk[8], ov[8][VPL];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int k = k0 + u;
+      lk[u] = -INFINITY;
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) ov[u][v] = 0.f;
+      if (k < n) {
+        lk[u] = __ldcg(lse_rows + k) * kLog2e;
+        const float *src = o_rows + (int64_t)k * D + lane * VPL;
+        if constexpr (VPL == 2) {
+          const float2 t2 = __ldcg(reinterpret_cast<const float2 *>(src));
+          ov[u][0] = t2.x;
+          ov[u][1] = t2.y;
+        } else {
+          const float4 t4 = __ldcg(reinterpret_cast<const float4 *>(src));
+          ov[u][0] = t4.x;
+          ov[u][1] = t4.y;
+          ov[u][2] = t4.z;
+          ov[u][3] = t4.w;
+        }
+      }
+    }
+    float mb = lk[0];
+#pragma unroll
+    for (int u = 1; u < 8; ++u) mb = fmaxf(mb, lk[u]);
+    const float Mn = fmaxf(M, mb);
+    const float sc = dev::ex2(M - Mn);
+    den *= sc;
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) acc[v] *= sc;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float wt = dev::ex2(lk[u] - Mn);
+      den += wt;
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) acc[v] += wt * ov[u][v];
+    }
+    M = Mn;
+  }
+  const float inv = 1.f / den;
+  uint16_t *d = dst + lane * VPL;
+  if constexpr (VPL == 2) {
+    *reinterpret_cast<uint32_t *>(d) = dev::pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  } else {
+    *reinterpret_cast<uint2 *>(d) = make_uint2(dev::pack_bf16x2(acc[0] * inv, acc[1] * inv),
+                                              dev::pack_bf16x2(acc[2] * inv, acc[3] * inv));
+  }
+}
+
+// ===========================================================================
+// decode_kernel: one CTA per (sequence, kv head, partition of P tokens).
+// fused = 1 (paged_decode_attention): finished bf16 output, merging partitions itself.
+// fused = 0 (paged_decode_split): normalised fp32 partials + natural-log lse only.
+
+struct DecodeArgs {
+  const uint16_t *q;           // [B][Hq][D] bf16
+  const int32_t *block_tables; // [B][max_blocks]
+  const int32_t *context_lens; // [B]
+  float *o_part;               // [B][Hq][n_parts][D]
+  float *lse_part;             // [B][Hq][n_parts]
+  uint16_t *out;               // fused: [B][Hq][D] bf16
+  uint32_t *counters;          // fused: [B][Hkv] partitions finished; zero between calls
+  int64_t num_blocks;
+  int32_t max_blocks, max_context_len, num_q_heads, num_kv_heads, group;
+  int32_t block_size, log2_bs, box_rows, partition_tokens, n_parts, fused;
+  float scale_log2;            // scale * log2(e)
+};
+
 template <int D, int STAGES>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const DecodeArgs a) {
   constexpr int kTileBytes = kChunk * D * 2;  // K (or V) bytes of one stage
   constexpr int kStageBytes = 2 * kTileBytes;
-  constexpr int KS = D / 16;                  // 16-wide k steps / m tiles over the head dim
+  constexpr int KS = D / 16;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = dev::smem_addr(smem_raw);
@@ -111,20 +350,42 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint8_t *const base_ptr = smem_raw + (base - raw);
   const uint32_t bar_full = base + STAGES * kStageBytes;
   const uint32_t bar_empty = bar_full + STAGES * 8;
-  int *const s_flag = reinterpret_cast<int *>(base_ptr + STAGES * kStageBytes + STAGES * 16);
+  volatile int *const s_flag =
+      reinterpret_cast<volatile int *>(base_ptr + STAGES * kStageBytes + STAGES * 16);
+  volatile int *const s_last = s_flag + 1;
 
+  // grid: x = partition (fastest), y = kv head, z = sequence
   const int part = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int32_t *trow = a.block_tables + (int64_t)b * a.max_blocks;
+  // The first block-table window does not depend on the context length (entries past
+  // it are valid memory, just unused), so the producer loads it together with the length.
+  const int win0 = (part * a.partition_tokens) >> a.log2_bs;
+  int tb0 = 0;
+  if (warp == kConsumerWarps && win0 + lane < a.max_blocks) tb0 = __ldg(trow + win0 + lane);
+  // consumer warps: the group's query rows as mma B fragments, also loaded up front
+  uint32_t qb[KS][2];
+  if (warp < kConsumerWarps) {
+    const int gid = lane >> 2, tig = lane & 3;
+    const bool hv = gid < a.group;
+    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+        a.q + ((int64_t)b * a.num_q_heads + g * a.group + (hv ? gid : 0)) * D);
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      qb[ks][0] = hv ? __ldg(qrow + 8 * ks + tig) : 0u;
+      qb[ks][1] = hv ? __ldg(qrow + 8 * ks + 4 + tig) : 0u;
+    }
+  }
 
   int L = __ldg(a.context_lens + b);
   const int cap = (int)min((int64_t)a.max_blocks * a.block_size, (int64_t)a.max_context_len);
   if (L < 0 || L > cap) {
-    if (tid == 0 && part == 0) atomicOr(&g_decode_errors, (unsigned)PKV_DEVERR_CONTEXT_LEN);
+    if (tid == 0 && part == 0) raise_error(PKV_DEVERR_CONTEXT_LEN);
     L = L < 0 ? 0 : cap;
   }
   const int t_begin = part * a.partition_tokens;
-  if (t_begin >= L) {
-    if (!a.split && part == 0) {  // empty context: zero output
+  if (t_begin >= L) {  // empty range: nothing written (the merge skips it)
+    if (a.fused && part == 0) {  // empty context: zero output
       uint16_t *o = a.out + ((int64_t)b * a.num_q_heads + g * a.group) * D;
       for (int i = tid; i < a.group * D; i += kThreads) o[i] = 0;
     }
@@ -147,18 +408,21 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------- producer warp
     const uint64_t policy = dev::policy_evict_first();
-    const int32_t *trow = a.block_tables + (int64_t)b * a.max_blocks;
-    const int rb = a.box_rows;                    // keys per TMA box = min(BS, 64)
+    const int rb = a.box_rows;                       // keys per TMA box = min(BS, 64)
     const uint32_t box_bytes = (uint32_t)rb * 128u;  // per 64-dim half
     const int lb_last = (t_end - 1) >> a.log2_bs;
-    int win = t_begin >> a.log2_bs;               // lanes hold table entries [win, win + 32)
-    int tb = (win + lane <= lb_last) ? __ldg(trow + win + lane) : 0;
+    int win = win0;                                  // lanes hold table entries [win, win + 32)
+    int tb = tb0;
+    // Launched as a programmatic dependent of the slot-write kernel, everything above
+    // overlapped it; the cache is read only after that grid's writes are visible.
+    // (Without a programmatic launch this returns at once.)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int c = 0; c < n_chunks; ++c) {
       const int s = c % STAGES;
       if (c >= STAGES &&
           !__all_sync(0xffffffffu, dev::mbar_wait(bar_empty + 8 * s, ((c / STAGES) - 1) & 1))) {
         if (lane == 0) {
-          atomicOr(&g_decode_errors, (unsigned)PKV_DEVERR_TIMEOUT);
+          raise_error(PKV_DEVERR_TIMEOUT);
           *s_flag = 1;
         }
         break;
@@ -179,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (lane < nbox) {
         int64_t phys = phys_raw;
         if (phys < 0 || phys >= a.num_blocks) {
-          atomicOr(&g_decode_errors, (unsigned)PKV_DEVERR_BLOCK_ID);
+          raise_error(PKV_DEVERR_BLOCK_ID);
           phys = 0;
         }
         const int off = key & (a.block_size - 1);
@@ -191,34 +455,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   } else {
     // ----------------------------------------------------------- consumer warps
-    const int gid = lane >> 2, tig = lane & 3;  // mma group id / thread in group
-    uint32_t qb[KS][2];
-    {
-      const bool hv = gid < a.group;
-      const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-          a.q + ((int64_t)b * a.num_q_heads + g * a.group + (hv ? gid : 0)) * D);
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        qb[ks][0] = hv ? __ldg(qrow + 8 * ks + tig) : 0u;
-        qb[ks][1] = hv ? __ldg(qrow + 8 * ks + 4 + tig) : 0u;
-      }
-    }
-    float o[KS][4];
-#pragma unroll
-    for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads 2*tig, 2*tig+1
-
-    const int lj = lane >> 3, lr = lane & 7;  // ldmatrix: matrix index / row within it
-    // QK operand A = K rows: matrices (keys 0-7 | 8-15) x (dims lo | hi) of a k step.
-    const int qk_key = 16 * warp + lr + ((lj & 1) << 3), qk_dsel = lj >> 1;
-    // PV operand A = V^T: matrices (keys 0-7, dims lo), (keys 0-7, dims hi), (keys 8-15, ...).
-    const int pv_key = 16 * warp + lr + ((lj >> 1) << 3), pv_dsel = lj & 1;
-
+    WarpAcc<D> acc;
+    acc_reset(acc);
     for (int c = 0; c < n_chunks; ++c) {
       const int s = c % STAGES;
       if (!__all_sync(0xffffffffu, dev::mbar_wait(bar_full + 8 * s, (c / STAGES) & 1))) {
         if (lane == 0) {
-          atomicOr(&g_decode_errors, (unsigned)PKV_DEVERR_TIMEOUT);
+          raise_error(PKV_DEVERR_TIMEOUT);
           *s_flag = 1;
         }
         break;
@@ -227,118 +470,58 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int nvalid = min(16, t_end - key0);
       if (nvalid > 0) {
         const uint32_t kb = base + s * kStageBytes;
-        const uint32_t vb = kb + kTileBytes;
-        // S^T (16 keys x 8 heads) = K_tile . Q^T
-        float sc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          uint32_t ak[4];
-          dev::ldsm_x4(ak, kb + tile_off(qk_key, 2 * ks + qk_dsel));
-          dev::mma_bf16_16816(sc, ak, qb[ks][0], qb[ks][1]);
-        }
-        // scale to base 2, mask keys past the range
-        const bool v0 = gid < nvalid, v1 = gid + 8 < nvalid;
-        const float s0 = v0 ? sc[0] * a.scale_log2 : -INFINITY;
-        const float s1 = v0 ? sc[1] * a.scale_log2 : -INFINITY;
-        const float s2 = v1 ? sc[2] * a.scale_log2 : -INFINITY;
-        const float s3 = v1 ? sc[3] * a.scale_log2 : -INFINITY;
-        float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
-#pragma unroll
-        for (int x = 4; x < 32; x <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, x));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, x));
-        }
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float al0 = dev::ex2(m0 - mn0), al1 = dev::ex2(m1 - mn1);
-        const float p0 = dev::ex2(s0 - mn0), p1 = dev::ex2(s1 - mn1);
-        const float p2 = dev::ex2(s2 - mn0), p3 = dev::ex2(s3 - mn1);
-        l0 = l0 * al0 + (p0 + p2);
-        l1 = l1 * al1 + (p1 + p3);
-        m0 = mn0;
-        m1 = mn1;
-#pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-          o[mt][0] *= al0;
-          o[mt][1] *= al1;
-          o[mt][2] *= al0;
-          o[mt][3] *= al1;
-        }
-        // P^T as the B operand: bf16 hi part and the bf16 residual, transposed
-        const uint32_t h01 = dev::pack_bf16x2(p0, p1), h23 = dev::pack_bf16x2(p2, p3);
-        const uint32_t r01 = dev::pack_bf16x2(p0 - dev::bf16lo_to_f32(h01), p1 - dev::bf16hi_to_f32(h01));
-        const uint32_t r23 = dev::pack_bf16x2(p2 - dev::bf16lo_to_f32(h23), p3 - dev::bf16hi_to_f32(h23));
-        const uint32_t bh0 = dev::movmatrix_trans(h01), bh1 = dev::movmatrix_trans(h23);
-        const uint32_t bl0 = dev::movmatrix_trans(r01), bl1 = dev::movmatrix_trans(r23);
-        // O^T (D x 8 heads) += V^T . P^T; rows of V past the range are zeroed in
-        // registers (never multiply an unloaded row: 0 * NaN would poison O)
-        uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-        if (nvalid < 16) {
-          const int kk = 2 * tig;
-          mlo = (kk < nvalid ? 0x0000ffffu : 0u) | (kk + 1 < nvalid ? 0xffff0000u : 0u);
-          mhi = (kk + 8 < nvalid ? 0x0000ffffu : 0u) | (kk + 9 < nvalid ? 0xffff0000u : 0u);
-        }
-#pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-          uint32_t av[4];
-          dev::ldsm_x4_trans(av, vb + tile_off(pv_key, 2 * mt + pv_dsel));
-          av[0] &= mlo;
-          av[1] &= mlo;
-          av[2] &= mhi;
-          av[3] &= mhi;
-          dev::mma_bf16_16816(o[mt], av, bh0, bh1);
-          dev::mma_bf16_16816(o[mt], av, bl0, bl1);
-        }
+        warp_tile<D>(acc, qb, kb, kb + kTileBytes, warp, lane, nvalid, a.scale_log2);
       }
       __syncwarp();
       if (lane == 0) dev::mbar_arrive(bar_empty + 8 * s);
     }
-
-    // ---- merge the four warps' (m, l, O) through shared memory
-#pragma unroll
-    for (int x = 4; x < 32; x <<= 1) {
-      l0 += __shfl_xor_sync(0xffffffffu, l0, x);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, x);
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");  // stages are free now
-    float *const red_o = reinterpret_cast<float *>(base_ptr);  // [warps][8 heads][D]
-    float *const red_m = red_o + kConsumerWarps * kMaxGroup * D;  // [warps][8]
-    float *const red_l = red_m + kConsumerWarps * kMaxGroup;      // [warps][8]
-    if (gid == 0) {
-      red_m[warp * kMaxGroup + 2 * tig] = m0;
-      red_m[warp * kMaxGroup + 2 * tig + 1] = m1;
-      red_l[warp * kMaxGroup + 2 * tig] = l0;
-      red_l[warp * kMaxGroup + 2 * tig + 1] = l1;
-    }
-#pragma unroll
-    for (int mt = 0; mt < KS; ++mt) {
-      float *r0 = red_o + (warp * kMaxGroup + 2 * tig) * D + 16 * mt + gid;
-      float *r1 = r0 + D;
-      r0[0] = o[mt][0];
-      r1[0] = o[mt][1];
-      r0[8] = o[mt][2];
-      r1[8] = o[mt][3];
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+    // ---- merge the four warps through shared memory (the stages are free now)
+    consumer_bar();
+    MergeArea r;
+    r.o = reinterpret_cast<float *>(base_ptr);
+    r.m = r.o + kConsumerWarps * a.group * D;
+    r.l = r.m + kConsumerWarps * kMaxGroup;
+    warp_stash<D>(acc, r, a.group, warp, lane);
+    consumer_bar();
     const int64_t head0 = (int64_t)b * a.num_q_heads + g * a.group;
-    for (int i = tid; i < a.group * D; i += kConsumerWarps * 32) {
-      const int h = i / D, d = i - h * D;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red_m[w * kMaxGroup + h]);
-      float num = 0.f, den = 0.f;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float wt = dev::ex2(red_m[w * kMaxGroup + h] - M);
-        num += wt * red_o[(w * kMaxGroup + h) * D + d];
-        den += wt * red_l[w * kMaxGroup + h];
+    const int nparts_b = (L + a.partition_tokens - 1) / a.partition_tokens;  // non-empty ones
+    if (a.fused && nparts_b == 1) {  // the whole sequence is here: finished output
+      for (int i = tid; i < a.group * D; i += kConsumers) {
+        const int h = i / D, d = i - h * D;
+        float M2, den;
+        a.out[head0 * D + i] = to_bf16(cta_merge<D>(r, a.group, h, d, &M2, &den));
       }
-      const float val = num / den;
-      if (a.split) {
+    } else {
+      for (int i = tid; i < a.group * D; i += kConsumers) {
+        const int h = i / D, d = i - h * D;
+        float M2, den;
+        const float val = cta_merge<D>(r, a.group, h, d, &M2, &den);
         const int64_t row = (head0 + h) * a.n_parts + part;
         a.o_part[row * D + d] = val;
-        if (d == 0) a.lse_part[row] = (M + log2f(den)) * kLn2;
-      } else {
-        a.out[(head0 + h) * D + d] = (uint16_t)(dev::pack_bf16x2(val, 0.f) & 0xffffu);
+        if (d == 0) a.lse_part[row] = (M2 + log2f(den)) * kLn2;
+      }
+      if (a.fused) {
+        // ticket: the last partition of (b, g) to finish merges all of them.  The barrier
+        // orders every thread's partial stores before thread 0's fence, and the fence is
+        // cumulative, so one fence publishes them all before the ticket is taken.
+        consumer_bar();
+        if (tid == 0) {
+          int last = 0;
+          if (!*s_flag) {
+            __threadfence();
+            const unsigned old = atomicAdd(a.counters + (int64_t)b * a.num_kv_heads + g, 1u);
+            last = (old + 1 == (unsigned)nparts_b);
+            if (last) __threadfence();  // acquire side: the other partitions' stores
+          }
+          *s_last = last;
+        }
+        consumer_bar();
+        if (*s_last) {
+          for (int h = warp; h < a.group; h += kConsumerWarps)
+            merge_rows<D>(a.out + (head0 + h) * D, a.o_part + (head0 + h) * a.n_parts * D,
+                          a.lse_part + (head0 + h) * a.n_parts, nparts_b, lane);
+          if (tid == 0) a.counters[(int64_t)b * a.num_kv_heads + g] = 0u;  // ready for the next call
+        }
       }
     }
   }
@@ -354,9 +537,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 // ---------------------------------------------------------------------------
-// Log-sum-exp merge: one CTA per (sequence, query head).  Thread groups of D/4
-// threads each read one partition row with float4 loads; groups take partitions
-// round robin and are summed through shared memory.
+// Log-sum-exp merge of fixed partitions: one CTA per (sequence, query head).  Thread
+// groups of D/4 threads each read one partition row with float4 loads; groups take
+// partitions round robin and are summed through shared memory.
 template <int D>
 __global__ void __launch_bounds__(128)
     combine_kernel(uint16_t *__restrict__ out, const float *__restrict__ o_part,
@@ -373,7 +556,7 @@ __global__ void __launch_bounds__(128)
   const int tid = threadIdx.x, grp = tid / TPR, col = tid % TPR;
   int L = __ldg(context_lens + b);
   if (L < 0 || L > max_context_len) {
-    if (tid == 0) atomicOr(&g_decode_errors, (unsigned)PKV_DEVERR_CONTEXT_LEN);
+    if (tid == 0) raise_error(PKV_DEVERR_CONTEXT_LEN);
     L = L < 0 ? 0 : max_context_len;
   }
   const int n = (L + partition_tokens - 1) / partition_tokens;
@@ -446,8 +629,8 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-int g_sms[kMaxDevices];            // SM count per device (0 = not queried)
-bool g_attr_set[kMaxDevices][2];   // dynamic smem attribute set, per head_dim variant
+int g_sms[kMaxDevices];              // SM count per device (0 = not queried)
+bool g_split_attr[kMaxDevices][2];   // dynamic smem attribute of decode_kernel set
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -463,14 +646,20 @@ int get_encoder() {
   return PKV_OK;
 }
 
+int current_device(int *dev) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
+  if (*dev < 0 || *dev >= kMaxDevices) return set_error(PKV_ERR_CUDA, "device index %d", *dev);
+  return PKV_OK;
+}
+
 int device_sms(int *sms) {
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
-  if (dev < 0 || dev >= kMaxDevices) return set_error(PKV_ERR_CUDA, "device index %d", dev);
+  int rc = current_device(&dev);
+  if (rc) return rc;
   if (!g_sms[dev]) {
     int n = 0;
-    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cudaError_t e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_error(e, "cudaDeviceGetAttribute");
     g_sms[dev] = n;
   }
@@ -526,9 +715,33 @@ int tensor_map(const void *cache_ptr, const pkv_cache_desc &c, CUtensorMap *out)
   return PKV_OK;
 }
 
-constexpr int stages_for(int d) { return d == 64 ? 4 : 3; }
-constexpr size_t smem_for(int d) {
-  return 1024 + (size_t)stages_for(d) * 2 * kChunk * d * 2 + stages_for(d) * 16 + 16;
+constexpr int split_stages(int d) { return d == 64 ? 4 : 3; }
+constexpr size_t split_smem(int d) {
+  return 1024 + (size_t)split_stages(d) * 2 * kChunk * d * 2 + split_stages(d) * 16 + 16;
+}
+
+// CTAs of decode_kernel one SM holds (shared memory limited: 66 KB at D=64, 99 KB at D=128).
+constexpr int split_occupancy(int d) { return d == 64 ? 3 : 2; }
+
+// Partition size for paged_decode_attention.  Few (sequence, kv head) units: cut each
+// into as many partitions as make about one wave of CTAs, so every CTA streams a long
+// range; many units: 1024-token partitions (short contexts stay whole).  Never below
+// min(context, 512) tokens, so short contexts are not cut into tiny pieces.
+int32_t plan_partition(int32_t num_seqs, int32_t hkv, int32_t d, int32_t max_len, int sms) {
+  const int64_t units = (int64_t)num_seqs * hkv;
+  const int64_t slots = (int64_t)sms * split_occupancy(d);
+  const int64_t lr = ((int64_t)max_len + kChunk - 1) / kChunk * kChunk;
+  int64_t P;
+  if (units >= slots) {
+    P = lr < 1024 ? lr : 1024;
+  } else {
+    const int64_t parts = slots / units;
+    P = ((max_len + parts - 1) / parts + kChunk - 1) / kChunk * kChunk;
+  }
+  const int64_t floor_p = lr < 512 ? lr : 512;
+  if (P < floor_p) P = floor_p;
+  if (P < kChunk) P = kChunk;
+  return (int32_t)P;
 }
 
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
@@ -536,6 +749,25 @@ int ilog2(int x) {
   int r = 0;
   while ((1 << r) < x) ++r;
   return r;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Workspace of paged_decode_attention: merge counters [B*Hkv] u32, then
+// paged_decode_split's partials for the planned partition size.
+struct FusedLayout {
+  size_t counters, o_part, lse_part, total;
+};
+
+FusedLayout fused_layout(int32_t num_seqs, int32_t hq, int32_t hkv, int32_t d, int32_t mlen,
+                         int32_t P) {
+  FusedLayout f;
+  const size_t rows = (size_t)num_seqs * hq * (size_t)((mlen + P - 1) / P);
+  f.counters = 0;
+  f.o_part = align256((size_t)num_seqs * hkv * 4);
+  f.lse_part = f.o_part + align256(rows * d * sizeof(float));
+  f.total = f.lse_part + align256(rows * sizeof(float));
+  return f;
 }
 
 // Checks shared by the split, single-pass and combined entry points.
@@ -569,38 +801,47 @@ int check_decode(const void *q, const void *k_cache, const void *v_cache, const 
   return PKV_OK;
 }
 
-size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+int maps_for(const pkv_bf16 *k_cache, const pkv_bf16 *v_cache, const pkv_cache_desc &c,
+             CUtensorMap *tmk, CUtensorMap *tmv) {
+  int rc = tensor_map(k_cache, c, tmk);
+  if (!rc) rc = tensor_map(v_cache, c, tmv);
+  return rc;
+}
 
 template <int D>
-int launch_decode(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
-                  const int32_t *bt, int32_t max_blocks, const int32_t *lens, int32_t max_len,
-                  int32_t num_seqs, int32_t hq, const pkv_cache_desc &c, float scale,
-                  int32_t P, int split, pkv_bf16 *out, float *o_part, float *lse_part,
-                  cudaStream_t stream) {
+int launch_split(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                 const int32_t *bt, int32_t max_blocks, const int32_t *lens, int32_t max_len,
+                 int32_t num_seqs, int32_t hq, const pkv_cache_desc &c, float scale, int32_t P,
+                 float *o_part, float *lse_part, pkv_bf16 *out, uint32_t *counters,
+                 cudaStream_t stream, bool programmatic = false) {
   CUtensorMap tmk, tmv;
-  int rc;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    if ((rc = tensor_map(k_cache, c, &tmk))) return rc;
-    if ((rc = tensor_map(v_cache, c, &tmv))) return rc;
+    int rc = maps_for(k_cache, v_cache, c, &tmk, &tmv);
+    if (rc) return rc;
     int dev = 0;
-    cudaGetDevice(&dev);
+    if ((rc = current_device(&dev))) return rc;
     const int vi = D == 64 ? 0 : 1;
-    if (dev >= 0 && dev < kMaxDevices && !g_attr_set[dev][vi]) {
-      cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, stages_for(D)>,
+    if (!g_split_attr[dev][vi]) {
+      cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, split_stages(D)>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)smem_for(D));
+                                           (int)split_smem(D));
       if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute");
-      g_attr_set[dev][vi] = true;
+      e = cudaFuncSetAttribute(decode_kernel<D, split_stages(D)>,
+                               cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+      if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(carveout)");
+      g_split_attr[dev][vi] = true;
     }
   }
   DecodeArgs a;
   a.q = q;
   a.block_tables = bt;
   a.context_lens = lens;
-  a.out = out;
   a.o_part = o_part;
   a.lse_part = lse_part;
+  a.out = out;
+  a.counters = counters;
+  a.fused = out != nullptr;
   a.num_blocks = c.num_blocks;
   a.max_blocks = max_blocks;
   a.max_context_len = max_len;
@@ -612,11 +853,25 @@ int launch_decode(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_
   a.box_rows = c.block_size < kChunk ? c.block_size : kChunk;
   a.partition_tokens = P;
   a.n_parts = (max_len + P - 1) / P;
-  a.split = split;
   a.scale_log2 = scale * kLog2e;
   dim3 grid((unsigned)a.n_parts, (unsigned)c.num_kv_heads, (unsigned)num_seqs);
-  decode_kernel<D, stages_for(D)><<<grid, kThreads, smem_for(D), stream>>>(tmk, tmv, a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e;
+  if (!programmatic) {
+    decode_kernel<D, split_stages(D)><<<grid, kThreads, split_smem(D), stream>>>(tmk, tmv, a);
+    e = cudaGetLastError();
+  } else {  // may start while the previous kernel on the stream (the slot write) still runs
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = split_smem(D);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, decode_kernel<D, split_stages(D)>, tmk, tmv, a);
+  }
   if (e != cudaSuccess) return cuda_error(e, "decode_kernel launch");
   return PKV_OK;
 }
@@ -635,14 +890,12 @@ int launch_combine(pkv_bf16 *out, const float *o_part, const float *lse_part, co
   return PKV_OK;
 }
 
-int32_t plan(int32_t num_seqs, int32_t hkv, int32_t max_len, int32_t sms) {
-  if (num_seqs <= 0 || hkv <= 0 || max_len <= 256) return 0;
-  const int64_t units = (int64_t)num_seqs * hkv;
-  const int64_t target = 4LL * sms;  // CTAs wanted: a few per SM
-  int32_t P = 512;
-  while (P > 128 && units * ((max_len + P - 1) / P) < target) P /= 2;
-  if ((max_len + P - 1) / P <= 1) return 0;
-  return P;
+int sms_or_default(int32_t num_sms) {
+  if (num_sms > 0) return num_sms;
+  std::lock_guard<std::mutex> lk(g_mu);
+  int n = 0;
+  if (device_sms(&n) != PKV_OK || n <= 0) n = 148;
+  return n;
 }
 
 }  // namespace
@@ -650,13 +903,13 @@ int32_t plan(int32_t num_seqs, int32_t hkv, int32_t max_len, int32_t sms) {
 
 using namespace pkv;
 
-PKV_API int32_t paged_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t max_context_len,
-                                  int32_t num_sms) {
-  if (num_sms <= 0) {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (device_sms(&num_sms) != PKV_OK || num_sms <= 0) num_sms = 148;
-  }
-  return plan(num_seqs, num_kv_heads, max_context_len, num_sms);
+PKV_API int32_t paged_decode_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t max_context_len, int32_t num_sms) {
+  if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads ||
+      num_q_heads / num_kv_heads > kMaxGroup || (head_dim != 64 && head_dim != 128) ||
+      max_context_len <= 0)
+    return 0;
+  return plan_partition(num_seqs, num_kv_heads, head_dim, max_context_len, sms_or_default(num_sms));
 }
 
 PKV_API size_t paged_decode_split_workspace_size(int32_t num_seqs, int32_t num_q_heads,
@@ -673,9 +926,10 @@ PKV_API size_t paged_decode_split_workspace_size(int32_t num_seqs, int32_t num_q
 PKV_API size_t paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
                                            int32_t num_kv_heads, int32_t head_dim,
                                            int32_t max_context_len) {
-  const int32_t P = paged_decode_plan(num_seqs, num_kv_heads, max_context_len, 0);
-  if (P == 0) return 0;
-  return paged_decode_split_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len, P);
+  const int32_t mlen = max_context_len > 0 ? max_context_len : 1;
+  const int32_t P = paged_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, mlen, 0);
+  if (P <= 0) return 0;
+  return fused_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, mlen, P).total;
 }
 
 PKV_API int paged_decode_split(float *o_part, float *lse_part, const pkv_bf16 *q,
@@ -697,12 +951,12 @@ PKV_API int paged_decode_split(float *o_part, float *lse_part, const pkv_bf16 *q
   if (!o_part || !lse_part) return set_error(PKV_ERR_NULL, "paged_decode_split: NULL o_part/lse_part");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   rc = cache->head_dim == 64
-           ? launch_decode<64>(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+           ? launch_split<64>(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                              max_context_len, num_seqs, num_q_heads, *cache, scale,
+                              partition_tokens, o_part, lse_part, nullptr, nullptr, s)
+           : launch_split<128>(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                                max_context_len, num_seqs, num_q_heads, *cache, scale,
-                               partition_tokens, 1, nullptr, o_part, lse_part, s)
-           : launch_decode<128>(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-                                max_context_len, num_seqs, num_q_heads, *cache, scale,
-                                partition_tokens, 1, nullptr, o_part, lse_part, s);
+                               partition_tokens, o_part, lse_part, nullptr, nullptr, s);
   if (!rc) clear_error();
   return rc;
 }
@@ -728,11 +982,53 @@ PKV_API int paged_decode_combine(pkv_bf16 *out, const float *o_part, const float
   if ((reinterpret_cast<uintptr_t>(out) & 7u) || (o_part && !aligned16(o_part)))
     return set_error(PKV_ERR_ALIGN, "paged_decode_combine: out must be 8-byte and o_part 16-byte aligned");
   int rc = launch_combine(out, o_part, lse_part, context_lens, max_context_len, num_seqs,
-                          num_q_heads, head_dim, partition_tokens > 0 ? partition_tokens : 1,
-                          static_cast<cudaStream_t>(stream));
+                          num_q_heads, head_dim, partition_tokens, static_cast<cudaStream_t>(stream));
   if (!rc) clear_error();
   return rc;
 }
+
+namespace pkv {
+namespace {
+
+// Checks and launches the fused decode; `programmatic` only when the previous kernel on
+// the stream is this library's slot write (which writes nothing but cache rows).
+int decode_fused(pkv_bf16 *out, const pkv_bf16 *q, const pkv_bf16 *k_cache,
+                 const pkv_bf16 *v_cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                 const int32_t *context_lens, int32_t max_context_len, int32_t num_seqs,
+                 int32_t num_q_heads, const pkv_cache_desc *cache, float scale, void *workspace,
+                 size_t workspace_bytes, cudaStream_t s, bool programmatic, bool launch,
+                 const char *fn) {
+  int rc = check_decode(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                        max_context_len, num_seqs, num_q_heads, cache, fn);
+  if (rc) return rc;
+  if (num_seqs == 0) return PKV_OK;
+  if (!out) return set_error(PKV_ERR_NULL, "%s: out is NULL", fn);
+  if (reinterpret_cast<uintptr_t>(out) & 7u)
+    return set_error(PKV_ERR_ALIGN, "%s: out must be 8-byte aligned", fn);
+  const int D = cache->head_dim;
+  const int32_t mlen = max_context_len > 0 ? max_context_len : 1;  // all-empty: zero outputs
+  const int32_t P = paged_decode_plan(num_seqs, num_q_heads, cache->num_kv_heads, D, mlen, 0);
+  const FusedLayout f = fused_layout(num_seqs, num_q_heads, cache->num_kv_heads, D, mlen, P);
+  if (!workspace || workspace_bytes < f.total)
+    return set_error(PKV_ERR_WORKSPACE, "%s: workspace %zu bytes < %zu needed", fn,
+                     workspace_bytes, f.total);
+  if (!aligned16(workspace))
+    return set_error(PKV_ERR_ALIGN, "%s: workspace must be 16-byte aligned", fn);
+  if (!launch) return PKV_OK;
+  char *ws = static_cast<char *>(workspace);
+  uint32_t *counters = reinterpret_cast<uint32_t *>(ws + f.counters);
+  float *o_part = reinterpret_cast<float *>(ws + f.o_part);
+  float *lse_part = reinterpret_cast<float *>(ws + f.lse_part);
+  return D == 64 ? launch_split<64>(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                    context_lens, mlen, num_seqs, num_q_heads, *cache, scale, P,
+                                    o_part, lse_part, out, counters, s, programmatic)
+                 : launch_split<128>(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                     context_lens, mlen, num_seqs, num_q_heads, *cache, scale, P,
+                                     o_part, lse_part, out, counters, s, programmatic);
+}
+
+}  // namespace
+}  // namespace pkv
 
 PKV_API int paged_decode_attention(pkv_bf16 *out, const pkv_bf16 *q, const pkv_bf16 *k_cache,
                                    const pkv_bf16 *v_cache, const int32_t *block_tables,
@@ -740,51 +1036,34 @@ PKV_API int paged_decode_attention(pkv_bf16 *out, const pkv_bf16 *q, const pkv_b
                                    int32_t max_context_len, int32_t num_seqs, int32_t num_q_heads,
                                    const pkv_cache_desc *cache, float scale, void *workspace,
                                    size_t workspace_bytes, void *stream) {
-  int rc = check_decode(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-                        max_context_len, num_seqs, num_q_heads, cache, "paged_decode_attention");
-  if (rc) return rc;
-  if (num_seqs == 0) {
-    clear_error();
-    return PKV_OK;
-  }
-  if (!out) return set_error(PKV_ERR_NULL, "paged_decode_attention: out is NULL");
-  if (reinterpret_cast<uintptr_t>(out) & 7u)
-    return set_error(PKV_ERR_ALIGN, "paged_decode_attention: out must be 8-byte aligned");
+  const int rc = decode_fused(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                              context_lens, max_context_len, num_seqs, num_q_heads, cache, scale,
+                              workspace, workspace_bytes, static_cast<cudaStream_t>(stream), false,
+                              true, "paged_decode_attention");
+  if (!rc) clear_error();
+  return rc;
+}
+
+PKV_API int paged_decode_step(pkv_bf16 *out, const pkv_bf16 *q, const pkv_bf16 *k,
+                              const pkv_bf16 *v, const int64_t *slot_mapping, int64_t num_tokens,
+                              pkv_bf16 *k_cache, pkv_bf16 *v_cache, const int32_t *block_tables,
+                              int32_t max_blocks_per_seq, const int32_t *context_lens,
+                              int32_t max_context_len, int32_t num_seqs, int32_t num_q_heads,
+                              const pkv_cache_desc *cache, float scale, void *workspace,
+                              size_t workspace_bytes, void *stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int32_t P = paged_decode_plan(num_seqs, cache->num_kv_heads, max_context_len, 0);
-  const int D = cache->head_dim;
-  if (P == 0) {
-    const int32_t Pone = max_context_len > 0 ? ((max_context_len + kChunk - 1) / kChunk) * kChunk : kChunk;
-    const int32_t mlen = max_context_len > 0 ? max_context_len : 1;
-    rc = D == 64 ? launch_decode<64>(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
-                                     context_lens, mlen, num_seqs, num_q_heads, *cache, scale,
-                                     Pone, 0, out, nullptr, nullptr, s)
-                 : launch_decode<128>(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
-                                      context_lens, mlen, num_seqs, num_q_heads, *cache, scale,
-                                      Pone, 0, out, nullptr, nullptr, s);
-    if (!rc) clear_error();
-    return rc;
-  }
-  const size_t need = paged_decode_split_workspace_size(num_seqs, num_q_heads, D, max_context_len, P);
-  if (!workspace || workspace_bytes < need)
-    return set_error(PKV_ERR_WORKSPACE, "paged_decode_attention: workspace %zu bytes < %zu needed",
-                     workspace_bytes, need);
-  if (!aligned16(workspace))
-    return set_error(PKV_ERR_ALIGN, "paged_decode_attention: workspace must be 16-byte aligned");
-  const int n_parts = (max_context_len + P - 1) / P;
-  const size_t rows = (size_t)num_seqs * num_q_heads * n_parts;
-  float *o_part = static_cast<float *>(workspace);
-  float *lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                              align256(rows * D * sizeof(float)));
-  rc = D == 64 ? launch_decode<64>(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
-                                   context_lens, max_context_len, num_seqs, num_q_heads, *cache,
-                                   scale, P, 1, nullptr, o_part, lse_part, s)
-               : launch_decode<128>(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
-                                    context_lens, max_context_len, num_seqs, num_q_heads, *cache,
-                                    scale, P, 1, nullptr, o_part, lse_part, s);
+  // check both halves before enqueuing either
+  int rc = check_write(k, v, slot_mapping, num_tokens, k_cache, v_cache, cache);
+  if (!rc)
+    rc = decode_fused(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                      max_context_len, num_seqs, num_q_heads, cache, scale, workspace,
+                      workspace_bytes, s, false, false, "paged_decode_step");
   if (rc) return rc;
-  rc = launch_combine(out, o_part, lse_part, context_lens, max_context_len, num_seqs, num_q_heads,
-                      D, P, s);
+  rc = launch_write(k, v, slot_mapping, num_tokens, k_cache, v_cache, *cache, s);
+  if (!rc)
+    rc = decode_fused(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                      max_context_len, num_seqs, num_q_heads, cache, scale, workspace,
+                      workspace_bytes, s, num_tokens > 0, true, "paged_decode_step");
   if (!rc) clear_error();
   return rc;
 }

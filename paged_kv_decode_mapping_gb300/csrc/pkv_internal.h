@@ -20,6 +20,13 @@ int cuda_error(cudaError_t e, const char *what);
 // Device error word of the write kernel's translation unit (read + optional clear).
 cudaError_t read_write_errors(uint32_t *flags, int clear);
 
+// The slot-mapping write, split into its host checks and its launch.
+int check_write(const void *k, const void *v, const int64_t *slot_mapping, int64_t num_tokens,
+                const void *k_cache, const void *v_cache, const pkv_cache_desc *cache);
+int launch_write(const pkv_bf16 *k, const pkv_bf16 *v, const int64_t *slot_mapping,
+                 int64_t num_tokens, pkv_bf16 *k_cache, pkv_bf16 *v_cache,
+                 const pkv_cache_desc &c, cudaStream_t stream);
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace pkv

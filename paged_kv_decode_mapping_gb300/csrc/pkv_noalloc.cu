@@ -77,7 +77,15 @@ PKV_API int paged_decode_attention_noalloc(pkv_bf16 *out, const pkv_bf16 *q,
   void *scratch = nullptr;
   int rc = scratch_address(&scratch);
   if (rc) return rc;
+  // The decode keeps one completion counter per (sequence, kv head) at the start of
+  // its workspace; they must be zero when the kernel starts.  A completed call leaves
+  // them zero, but clear them anyway so a call never depends on the previous one.
+  if (num_seqs > 0) {
+    const cudaError_t e = cudaMemsetAsync(scratch, 0, (size_t)num_seqs * cache->num_kv_heads * 4,
+                                          static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_error(e, "paged_decode_attention_noalloc: clear counters");
+  }
   return paged_decode_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                 context_lens, max_context_len, num_seqs, num_q_heads, cache,
-                                scale, scratch, need > 0 ? kNoAllocScratchBytes : 0, stream);
+                                scale, scratch, kNoAllocScratchBytes, stream);
 }

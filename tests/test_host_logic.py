@@ -19,18 +19,24 @@ def B():
     return binding
 
 
-def test_plan_picks_splits_from_context_length(B):
+def test_plan_picks_partitions_from_context_length(B):
+    """Few (sequence, kv head) units: about one wave of long partitions (3 CTAs/SM at
+    head_dim 64, 2 at 128); many units: 1024 tokens; never below min(context, 512)."""
     sms = 152
-    assert B.paged_decode_plan(1, 8, 128, sms) == 0            # short context: one pass
-    assert B.paged_decode_plan(1, 8, 256, sms) == 0
-    assert B.paged_decode_plan(4, 8, 32768, sms) == 512         # long context: 512-token partitions
-    assert B.paged_decode_plan(16, 8, 2048, sms) == 256         # 128 units: finer split to fill the SMs
-    assert B.paged_decode_plan(64, 8, 4096, sms) == 512
-    assert B.paged_decode_plan(256, 4, 8192, sms) == 512
-    assert B.paged_decode_plan(0, 8, 4096, sms) == 0
-    for b, h, L in [(1, 1, 100_000), (2, 8, 300), (1000, 8, 600), (3, 2, 5000)]:
-        P = B.paged_decode_plan(b, h, L, sms)
-        assert P == 0 or (P % 64 == 0 and 128 <= P <= 512 and math.ceil(L / P) >= 2)
+    assert B.paged_decode_plan(1, 32, 8, 64, 128, sms) == 128          # short: one partition
+    assert B.paged_decode_plan(16, 32, 8, 64, 2048, sms) == 704        # 128 units x 3 = 384 CTAs
+    assert B.paged_decode_plan(4, 24, 8, 128, 32768, sms) == 3648      # 32 units x 9 = 288 CTAs
+    assert B.paged_decode_plan(64, 24, 8, 128, 4096, sms) == 1024      # 512 units >= 304 slots
+    assert B.paged_decode_plan(256, 32, 4, 64, 8192, sms) == 1024
+    assert B.paged_decode_plan(256, 32, 4, 64, 300, sms) == 320        # short contexts stay whole
+    assert B.paged_decode_plan(1, 8, 8, 64, 1, sms) == 64
+    assert B.paged_decode_plan(0, 8, 8, 64, 4096, sms) == 0
+    assert B.paged_decode_plan(2, 8, 8, 96, 4096, sms) == 0            # unsupported head_dim
+    assert B.paged_decode_plan(2, 8, 1, 64, 4096, sms) == 512          # group 8: the largest built
+    assert B.paged_decode_plan(2, 16, 1, 64, 4096, sms) == 0           # group 16: not built
+    for b, hq, h, d, L in [(1, 1, 1, 64, 100_000), (3, 12, 4, 128, 5000), (1000, 8, 8, 64, 600)]:
+        P = B.paged_decode_plan(b, hq, h, d, L, sms)
+        assert P % 64 == 0 and P >= min(512, -(-L // 64) * 64)
 
 
 def test_workspace_sizes(B):
@@ -41,6 +47,11 @@ def test_workspace_sizes(B):
     assert B.paged_decode_split_workspace_size(4, 24, 128, 32768, 512) == expect
     assert B.paged_decode_split_workspace_size(4, 24, 128, 0, 512) == 0
     assert B.paged_decode_split_workspace_size(4, 24, 128, 100, 0) == 0
+    # paged_decode_attention: counters [B*Hkv] u32, then the split layout for the planned P
+    P = B.paged_decode_plan(4, 24, 8, 128, 32768)
+    up = lambda x: -(-x // 256) * 256
+    assert B.paged_decode_workspace_size(4, 24, 8, 128, 32768) == (
+        up(4 * 8 * 4) + B.paged_decode_split_workspace_size(4, 24, 128, 32768, P))
 
 
 @pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])

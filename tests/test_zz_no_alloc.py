@@ -52,7 +52,7 @@ def _with_workspace(B, g):
     out = torch.empty_like(g["q"])
     Bn, Hq, D = g["q"].shape
     need = B.paged_decode_workspace_size(Bn, Hq, g["k_cache"].shape[1], D, g["max_context_len"])
-    ws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(max(need, 16), dtype=torch.uint8, device="cuda")
     B.paged_decode_attention(out, g["q"], g["k_cache"], g["v_cache"], g["block_tables"],
                              g["context_lens"], g["max_context_len"], g["scale"], workspace=ws)
     return out, need
@@ -69,7 +69,7 @@ def test_noalloc_matches_workspace_entry_point_twice(B):
         inp = W.make_inputs(w, poison=True)
         g = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
         ref, need = _with_workspace(B, g)
-        assert 0 < need <= B.NOALLOC_SCRATCH_BYTES  # the split plan really uses the scratch
+        assert 0 < need <= B.NOALLOC_SCRATCH_BYTES  # the decode really uses the scratch
         out = torch.full_like(g["q"], float("nan"))
         rc = _noalloc(B, out, g)
         assert rc == 0, B.pkv_last_error()
@@ -83,11 +83,12 @@ def test_noalloc_matches_workspace_entry_point_twice(B):
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(B):
     # a plan whose partition workspace exceeds the fixed array is refused up front
-    Bn, Hq, Hkv, D, L = 4096, 64, 8, 128, 32768
+    # (one completion counter per (sequence, kv head): 65535 x 256 of them is 64 MiB)
+    Bn, Hq, Hkv, D, L, BS = 65535, 256, 256, 64, 64, 64
     need = B.paged_decode_workspace_size(Bn, Hq, Hkv, D, L)
     assert need > B.NOALLOC_SCRATCH_BYTES
-    d = B.pkv_cache_desc(1 << 20, 16, Hkv, D)
+    d = B.pkv_cache_desc(16, BS, Hkv, D)
     fake = ctypes.c_void_p(1 << 20)
-    rc = B.lib().paged_decode_attention_noalloc(fake, fake, fake, fake, fake, L // 16, fake, L, Bn,
+    rc = B.lib().paged_decode_attention_noalloc(fake, fake, fake, fake, fake, L // BS, fake, L, Bn,
                                                 Hq, ctypes.byref(d), 0.1, None)
     assert rc == -4 and "scratch" in B.pkv_last_error()
