@@ -61,7 +61,8 @@ enum {
   PKV_ERR_WORKSPACE = -4,   /* workspace missing or smaller than required */
   PKV_ERR_ALIGN = -5,       /* a pointer is not 16-byte aligned */
   PKV_ERR_CUDA = -6,        /* a CUDA runtime call or launch failed */
-  PKV_ERR_DEVICE = -7       /* pkv_device_errors() found a device-side error bit */
+  PKV_ERR_DEVICE = -7,      /* pkv_device_errors() found a device-side error bit */
+  PKV_ERR_NOSPACE = -8      /* the block pool has too few free blocks (block manager) */
 };
 
 /* Device error bits reported by pkv_device_errors(). */
@@ -233,6 +234,41 @@ int paged_decode_attention_noalloc(pkv_bf16 *out, const pkv_bf16 *q, const pkv_b
                                    int32_t max_blocks_per_seq, const int32_t *context_lens,
                                    int32_t max_context_len, int32_t num_seqs, int32_t num_q_heads,
                                    const pkv_cache_desc *cache, float scale, void *stream);
+
+/*
+ * Block manager -- the host-side allocator that produces block tables and slot
+ * mappings ("mini-vLLM" README, architecture diagram and M4 row: a Block Manager
+ * allocates physical blocks and keeps per-sequence block tables, with LIFO preemption
+ * under memory pressure; "vLLM-Style Llama Inference Engine", How it works: the
+ * scheduler allocates blocks and finished requests release them).  HOST memory and
+ * host code only; thread-safe.  Blocks are handed out from a LIFO free list (block 0
+ * first on a fresh pool); a sequence of L tokens owns ceil(L / block_size) blocks.
+ * Functions return PKV_OK or a negative PKV_ERR_* code (PKV_ERR_NOSPACE when the pool
+ * cannot satisfy a request; nothing changes then).
+ */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* A pool of num_blocks blocks of block_size slots; NULL on bad sizes (see pkv_last_error). */
+pkv_block_manager *pkv_bm_create(int64_t num_blocks, int32_t block_size);
+void pkv_bm_destroy(pkv_block_manager *m);
+/* Free blocks now (>= 0), or a negative error code. */
+int64_t pkv_bm_num_free_blocks(pkv_block_manager *m);
+/* Admit sequence seq_id holding num_tokens tokens (e.g. a prompt): allocates its blocks. */
+int pkv_bm_add_sequence(pkv_block_manager *m, int64_t seq_id, int64_t num_tokens);
+/* Append one token to each listed sequence (a sequence may appear several times): writes
+ * the token's slot (block * block_size + offset) to slot_mapping[i], allocating a block
+ * when a sequence's last block is full.  All or nothing. */
+int pkv_bm_append_slots(pkv_block_manager *m, const int64_t *seq_ids, int32_t n,
+                        int64_t *slot_mapping);
+/* A finished sequence releases its blocks. */
+int pkv_bm_free_sequence(pkv_block_manager *m, int64_t seq_id);
+/* Preempt the most recently admitted sequence (LIFO): release its blocks, report its id. */
+int pkv_bm_preempt_lifo(pkv_block_manager *m, int64_t *seq_id);
+/* Block tables [n][max_blocks_per_seq] (unused entries -1) and context lengths [n] of the
+ * listed sequences, ready to copy to the device for paged_decode_attention. */
+int pkv_bm_block_tables(pkv_block_manager *m, const int64_t *seq_ids, int32_t n,
+                        int32_t max_blocks_per_seq, int32_t *block_tables,
+                        int32_t *context_lens);
 
 /*
  * pkv_device_errors -- synchronises the current device, then ORs the device error

@@ -26,7 +26,8 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 PKV_OK = 0
 ERRORS = {-1: "PKV_ERR_NULL", -2: "PKV_ERR_SHAPE", -3: "PKV_ERR_UNSUPPORTED",
-          -4: "PKV_ERR_WORKSPACE", -5: "PKV_ERR_ALIGN", -6: "PKV_ERR_CUDA", -7: "PKV_ERR_DEVICE"}
+          -4: "PKV_ERR_WORKSPACE", -5: "PKV_ERR_ALIGN", -6: "PKV_ERR_CUDA", -7: "PKV_ERR_DEVICE",
+          -8: "PKV_ERR_NOSPACE"}
 DEVERR = {1: "BLOCK_ID", 2: "SLOT", 4: "CONTEXT_LEN", 8: "TIMEOUT"}
 
 
@@ -69,6 +70,22 @@ _lib.paged_decode_attention_noalloc.argtypes = [_P, _P, _P, _P, _P, _i32, _P, _i
                                                 _D, _f32, _P]
 _lib.paged_decode_attention_noalloc.restype = ctypes.c_int
 NOALLOC_SCRATCH_BYTES = 32 << 20  # PKV_NOALLOC_SCRATCH_BYTES in include/paged_kv.h
+_lib.pkv_bm_create.argtypes = [_i64, _i32]
+_lib.pkv_bm_create.restype = _P
+_lib.pkv_bm_destroy.argtypes = [_P]
+_lib.pkv_bm_destroy.restype = None
+_lib.pkv_bm_num_free_blocks.argtypes = [_P]
+_lib.pkv_bm_num_free_blocks.restype = _i64
+_lib.pkv_bm_add_sequence.argtypes = [_P, _i64, _i64]
+_lib.pkv_bm_add_sequence.restype = ctypes.c_int
+_lib.pkv_bm_append_slots.argtypes = [_P, _P, _i32, _P]
+_lib.pkv_bm_append_slots.restype = ctypes.c_int
+_lib.pkv_bm_free_sequence.argtypes = [_P, _i64]
+_lib.pkv_bm_free_sequence.restype = ctypes.c_int
+_lib.pkv_bm_preempt_lifo.argtypes = [_P, ctypes.POINTER(ctypes.c_int64)]
+_lib.pkv_bm_preempt_lifo.restype = ctypes.c_int
+_lib.pkv_bm_block_tables.argtypes = [_P, _P, _i32, _i32, _P, _P]
+_lib.pkv_bm_block_tables.restype = ctypes.c_int
 _lib.pkv_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
 _lib.pkv_device_errors.restype = ctypes.c_int
 _lib.pkv_last_error.argtypes = []
@@ -270,3 +287,51 @@ def pkv_device_errors(clear: bool = True) -> int:
 
 def pkv_last_error() -> str:
     return _lib.pkv_last_error().decode(errors="replace")
+
+
+class BlockManager:
+    """The library's host block allocator (pkv_bm_*): block tables and slot mappings."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        self._h = _lib.pkv_bm_create(int(num_blocks), int(block_size))
+        if not self._h:
+            raise PkvError(-2, "pkv_bm_create")
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+
+    def __del__(self):
+        h, self._h = getattr(self, "_h", None), None
+        if h:
+            _lib.pkv_bm_destroy(h)
+
+    @property
+    def num_free_blocks(self) -> int:
+        n = int(_lib.pkv_bm_num_free_blocks(self._h))
+        if n < 0:
+            raise PkvError(n, "pkv_bm_num_free_blocks")
+        return n
+
+    def add_sequence(self, seq_id: int, num_tokens: int) -> None:
+        _check(_lib.pkv_bm_add_sequence(self._h, int(seq_id), int(num_tokens)), "pkv_bm_add_sequence")
+
+    def append_slots(self, seq_ids) -> torch.Tensor:
+        ids = torch.as_tensor(list(seq_ids), dtype=torch.int64).contiguous()
+        out = torch.empty(len(ids), dtype=torch.int64)
+        _check(_lib.pkv_bm_append_slots(self._h, ids.data_ptr(), len(ids), out.data_ptr()),
+               "pkv_bm_append_slots")
+        return out
+
+    def free_sequence(self, seq_id: int) -> None:
+        _check(_lib.pkv_bm_free_sequence(self._h, int(seq_id)), "pkv_bm_free_sequence")
+
+    def preempt_lifo(self) -> int:
+        v = ctypes.c_int64(0)
+        _check(_lib.pkv_bm_preempt_lifo(self._h, ctypes.byref(v)), "pkv_bm_preempt_lifo")
+        return int(v.value)
+
+    def block_tables(self, seq_ids, max_blocks_per_seq: int):
+        ids = torch.as_tensor(list(seq_ids), dtype=torch.int64).contiguous()
+        tables = torch.empty(len(ids), int(max_blocks_per_seq), dtype=torch.int32)
+        lens = torch.empty(len(ids), dtype=torch.int32)
+        _check(_lib.pkv_bm_block_tables(self._h, ids.data_ptr(), len(ids), int(max_blocks_per_seq),
+                                        tables.data_ptr(), lens.data_ptr()), "pkv_bm_block_tables")
+        return tables, lens

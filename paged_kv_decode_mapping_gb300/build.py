@@ -34,7 +34,7 @@ def _cuda_lib_dir(nvcc: str) -> str:
 
 
 def sources() -> list[str]:
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _inputs() -> list[str]:
@@ -60,7 +60,7 @@ def build(force: bool = False, verbose: bool = False, extra: tuple = ()) -> str:
     nvcc = _nvcc()
     os.makedirs(OBJDIR, exist_ok=True)
     srcs = sources()
-    objs = [os.path.join(OBJDIR, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    objs = [os.path.join(OBJDIR, os.path.splitext(os.path.basename(s))[0] + ".o") for s in srcs]
 
     def cc(pair):
         src, obj = pair

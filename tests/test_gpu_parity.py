@@ -351,3 +351,53 @@ def test_device_error_bits(B):
                              90, inp["scale"])
     assert B.pkv_device_errors(clear=True) & 4
     assert B.pkv_device_errors(clear=True) == 0
+
+
+# ------------------------------------------------------- block-manager driven steps
+def test_block_manager_driven_decode_steps(B, oracle):
+    """Decode steps whose block tables and slot mappings come from the host block
+    manager: prompts written through its slots, one appended token per step, a finished
+    sequence freed and a new one admitted into the reused blocks, a LIFO preemption.
+    Caches and outputs match the oracle at every step."""
+    BS, Hkv, D, Hq, NB = 16, 2, 64, 8, 48
+    gen = torch.Generator().manual_seed(21)
+    rnd = lambda *s: torch.randn(*s, generator=gen).to(torch.bfloat16)
+    kc, vc = rnd(NB, Hkv, BS, D), rnd(NB, Hkv, BS, D)
+    kg, vg = kc.cuda(), vc.cuda()
+    bm = B.BlockManager(NB, BS)
+
+    def write(ids):
+        nonlocal kc, vc
+        slots = bm.append_slots(ids)
+        kn, vn = rnd(len(ids), Hkv, D), rnd(len(ids), Hkv, D)
+        kc, vc = oracle.kv_write(kn, vn, slots, kc, vc)
+        return kn, vn, slots
+
+    def admit(s, n):
+        bm.add_sequence(s, 0)
+        kn, vn, slots = write([s] * n)
+        B.paged_kv_write(kn.cuda(), vn.cuda(), slots.cuda(), kg, vg)
+
+    for s, n in ((1, 37), (2, 100), (3, 5)):
+        admit(s, n)
+    active = [1, 2, 3]
+    for step in range(6):
+        if step == 2:
+            bm.free_sequence(2)
+            active.remove(2)
+            admit(4, 60)
+            active.append(4)
+        if step == 4:
+            assert bm.preempt_lifo() == 4
+            active.remove(4)
+        kn, vn, slots = write(active)
+        tables, lens = bm.block_tables(active, NB)
+        q = rnd(len(active), Hq, D)
+        out = torch.empty(len(active), Hq, D, dtype=torch.bfloat16, device="cuda")
+        B.paged_decode_step(out, q.cuda(), kn.cuda(), vn.cuda(), slots.cuda(), kg, vg,
+                            tables.cuda(), lens.cuda(), int(lens.max()), 0.125)
+        ref = oracle.decode(q, kc, vc, tables, lens, 0.125)
+        check_attention(out, ref, f"manager step {step}")
+        assert torch.equal(kg.cpu().view(torch.int16), kc.view(torch.int16))
+        assert torch.equal(vg.cpu().view(torch.int16), vc.view(torch.int16))
+    assert_no_device_errors(B)
