@@ -27,7 +27,8 @@ _lock = threading.Lock()
 
 def build(src: str = _SRC, out: str = _LIB, extra_flags: tuple = ()) -> str:
     """Compile ``oracle.c`` with gcc into a shared library (OpenMP over rows)."""
-    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", *extra_flags, src, "-o",
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-fopenmp",
+           *extra_flags, src, "-o",
            out + ".tmp", "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(out + ".tmp", out)
@@ -63,6 +64,9 @@ class Oracle:
         L.oracle_decode_partitions.restype = ctypes.c_int
         L.oracle_lse_combine.argtypes = [P, P, P, i32, i32]
         L.oracle_lse_combine.restype = ctypes.c_int
+        L.oracle_kv_write_rope.argtypes = [P, P, P, i32, P, P, i64, P, i64, i32, i32, P, P, i64,
+                                           i32, i32, i32]
+        L.oracle_kv_write_rope.restype = ctypes.c_int
         self._L = L
 
     # -- helpers -------------------------------------------------------------
@@ -106,6 +110,29 @@ class Oracle:
         self._check(rc, "kv_write")
         to_t = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).reshape(NB, Hkv, BS, D)
         return to_t(kc), to_t(vc)
+
+    def kv_write_rope(self, k, v, slot_mapping, positions, cos_sin, k_cache, v_cache, q=None,
+                      rotary_dim=None, neox_style=True):
+        """Rotary embedding of k (and q) at `positions` (fp32 table cos_sin [max_pos, r]),
+        then the slot write.  Returns (k_cache, v_cache, q) as new bf16 tensors."""
+        NB, Hkv, BS, D = k_cache.shape
+        r = D if rotary_dim is None else int(rotary_dim)
+        kc, vc = self._u16(k_cache).copy(), self._u16(v_cache).copy()
+        ka, va = self._u16(k), self._u16(v)
+        qa = self._u16(q).copy() if q is not None else None
+        Hq = q.shape[1] if q is not None else 0
+        sl = self._arr(slot_mapping, np.int64)
+        po = self._arr(positions, np.int64)
+        cs = self._arr(cos_sin, np.float32)
+        rc = self._L.oracle_kv_write_rope(self._p(ka), self._p(va),
+                                          self._p(qa) if qa is not None else None, Hq,
+                                          self._p(sl), self._p(po), len(sl), self._p(cs),
+                                          cs.shape[0], r, 1 if neox_style else 0, self._p(kc),
+                                          self._p(vc), NB, Hkv, BS, D)
+        self._check(rc, "kv_write_rope")
+        to_t = lambda a, shape: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).reshape(shape)
+        qo = to_t(qa, tuple(q.shape)) if q is not None else None
+        return to_t(kc, (NB, Hkv, BS, D)), to_t(vc, (NB, Hkv, BS, D)), qo
 
     # -- decode attention -----------------------------------------------------
     def decode(self, q, k_cache, v_cache, block_tables, context_lens, scale: float,

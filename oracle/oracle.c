@@ -328,3 +328,76 @@ int oracle_lse_combine(double *out, const double *o_part, const double *lse_part
   for (int32_t d = 0; d < head_dim; ++d) out[d] /= den;
   return ORACLE_OK;
 }
+
+/* ---- rotary position embedding, fused into the write ---------------------------
+ * "Building ... with tiny-vLLM", CUDA kernel engineering: RoPE rotates pairs of
+ * coordinates by position-dependent angles (sine/cosine); "llm-stack", Serving engine:
+ * RoPE is applied at absolute positions before keys enter the cache, and the Model
+ * section names the two pairings (its "RoPE pairing permutation").
+ * Pairs: neox_style != 0 ("rotate half"): (i, i + r/2) for i < r/2; else interleaved
+ * (2i, 2i + 1).  Angle table: cos_sin[pos][0 .. r/2) = cos, [r/2 .. r) = sin of pair i
+ * (fp32, given by the caller).  Coordinates at or past rotary_dim are copied.
+ * The rotated bf16 value is decided by floating point, so it is computed in the
+ * precision the kernel uses: fp32 products and sums, each rounded once (no fused
+ * multiply-add), then rounded to bf16 (nearest even):
+ *   x1' = x1*c - x2*s,   x2' = x2*c + x1*s.                                        */
+static void rope_row(uint16_t *dst, const uint16_t *src, const float *cs, int32_t head_dim,
+                     int32_t rotary_dim, int neox) {
+  const int32_t half = rotary_dim / 2;
+  for (int32_t d = 0; d < head_dim; ++d) dst[d] = src[d];
+  for (int32_t i = 0; i < half; ++i) {
+    const int32_t a = neox ? i : 2 * i, b = neox ? i + half : 2 * i + 1;
+    const float x1 = (float)oracle_bf16_to_double(src[a]);
+    const float x2 = (float)oracle_bf16_to_double(src[b]);
+    const float c = cs[i], s = cs[half + i];
+    volatile float p1 = x1 * c, p2 = x2 * s, p3 = x2 * c, p4 = x1 * s;
+    const float r1 = p1 - p2, r2 = p3 + p4;
+    dst[a] = oracle_double_to_bf16((double)r1);
+    dst[b] = oracle_double_to_bf16((double)r2);
+  }
+}
+
+/* Rotate k (and q, in place, when q != NULL) at positions[i], then write k and v at
+ * slot_mapping[i] like oracle_kv_write.  q is [num_tokens][num_q_heads][head_dim]. */
+int oracle_kv_write_rope(const uint16_t *k, const uint16_t *v, uint16_t *q, int32_t num_q_heads,
+                         const int64_t *slot_mapping, const int64_t *positions,
+                         int64_t num_tokens, const float *cos_sin, int64_t max_position,
+                         int32_t rotary_dim, int32_t neox_style, uint16_t *k_cache,
+                         uint16_t *v_cache, int64_t num_blocks, int32_t num_kv_heads,
+                         int32_t block_size, int32_t head_dim) {
+  if (num_tokens < 0 || rotary_dim <= 0 || rotary_dim > head_dim || rotary_dim % 2 != 0)
+    return ORACLE_ERR_ARG;
+  uint16_t *krot = (uint16_t *)malloc(sizeof(uint16_t) * ((size_t)num_tokens * num_kv_heads * head_dim + 1));
+  uint16_t *row = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)head_dim);
+  if (!krot || !row) {
+    free(krot);
+    free(row);
+    return ORACLE_ERR_NOMEM;
+  }
+  int rc = ORACLE_OK;
+  for (int64_t i = 0; i < num_tokens && rc == ORACLE_OK; ++i) {
+    const int64_t pos = positions[i];
+    if (pos < 0 || pos >= max_position) {
+      rc = ORACLE_ERR_ARG;
+      break;
+    }
+    const float *cs = cos_sin + pos * rotary_dim;
+    for (int32_t h = 0; h < num_kv_heads; ++h) {
+      const int64_t o = (i * num_kv_heads + h) * (int64_t)head_dim;
+      rope_row(krot + o, k + o, cs, head_dim, rotary_dim, neox_style);
+    }
+    if (q) {
+      for (int32_t h = 0; h < num_q_heads; ++h) {
+        uint16_t *qr = q + (i * num_q_heads + h) * (int64_t)head_dim;
+        rope_row(row, qr, cs, head_dim, rotary_dim, neox_style);
+        for (int32_t d = 0; d < head_dim; ++d) qr[d] = row[d];
+      }
+    }
+  }
+  if (rc == ORACLE_OK)
+    rc = oracle_kv_write(krot, v, slot_mapping, num_tokens, k_cache, v_cache, num_blocks,
+                         num_kv_heads, block_size, head_dim);
+  free(krot);
+  free(row);
+  return rc;
+}

@@ -280,8 +280,103 @@ def pin_cached_equals_recompute(o):
     assert torch.allclose(got, ref, atol=1e-12)
 
 
+# ------------------------------------------------------------------ RoPE write
+def rope_table(max_pos, rotary_dim, base=10000.0, dtype=torch.float64):
+    """cos/sin table [max_pos, r]: angle(pos, i) = pos * base^(-2i/r), cos first then sin."""
+    half = rotary_dim // 2
+    inv = base ** (-torch.arange(half, dtype=torch.float64) * 2.0 / rotary_dim)
+    ang = torch.arange(max_pos, dtype=torch.float64)[:, None] * inv[None, :]
+    return torch.cat([ang.cos(), ang.sin()], dim=1).to(dtype)
+
+
+def _rope_case(T=5, Hkv=2, Hq=4, D=16, seed=2):
+    g = torch.Generator().manual_seed(seed)
+    k = torch.randn(T, Hkv, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(T, Hkv, D, generator=g).to(torch.bfloat16)
+    q = torch.randn(T, Hq, D, generator=g).to(torch.bfloat16)
+    kc = torch.zeros(4, Hkv, 4, D, dtype=torch.bfloat16)
+    return k, v, q, kc
+
+
+def pin_rope_zero_angle_is_identity(o):
+    """Rotation by angle 0 (cos 1, sin 0) leaves k and q bit-identical."""
+    k, v, q, kc = _rope_case()
+    cs = torch.cat([torch.ones(1, 8), torch.zeros(1, 8)], dim=1).float()
+    slots = torch.arange(5, dtype=torch.int64)
+    kr, vr, qr = o.kv_write_rope(k, v, slots, torch.zeros(5, dtype=torch.int64), cs, kc, kc, q=q)
+    ek, ev = o.kv_write(k, v, slots, kc, kc)
+    assert torch.equal(kr.view(torch.int16), ek.view(torch.int16))
+    assert torch.equal(vr.view(torch.int16), ev.view(torch.int16))
+    assert torch.equal(qr.view(torch.int16), q.view(torch.int16))
+
+
+def pin_rope_is_complex_rotation(o):
+    """Each pair (x1, x2) becomes (x1 + i x2) * e^{i angle}, computed independently in
+    complex128; the oracle's fp32-then-bf16 result is within bf16 rounding of it."""
+    k, v, q, kc = _rope_case(T=6, D=32)
+    cs = rope_table(50, 32).float()
+    pos = torch.tensor([0, 1, 7, 13, 31, 49], dtype=torch.int64)
+    kr, _, qr = o.kv_write_rope(k, v, torch.full((6,), -1, dtype=torch.int64), pos, cs, kc, kc, q=q)
+    for x, y in ((q, qr),):
+        xd = x.double()
+        z = torch.complex(xd[..., :16], xd[..., 16:])
+        c = cs.double()[pos][:, None, :16]
+        s = cs.double()[pos][:, None, 16:]
+        zr = z * torch.complex(c, s)
+        exact = torch.cat([zr.real, zr.imag], dim=-1)
+        err = (y.double() - exact).abs()
+        assert bool((err <= 2.0 ** -8 * exact.abs() + 1e-6 * (1 + xd.abs())).all()), err.max()
+
+
+def pin_rope_pairing_permutation(o):
+    """Interleaved pairs (2i, 2i+1) are the rotate-half pairs (i, i + r/2) of the vector
+    with its even coordinates first and odd ones after (the pairing permutation)."""
+    k, v, q, kc = _rope_case(T=4, D=16)
+    cs = rope_table(20, 16).float()
+    pos = torch.tensor([3, 5, 11, 19], dtype=torch.int64)
+    perm = torch.cat([torch.arange(0, 16, 2), torch.arange(1, 16, 2)])
+    inv = torch.argsort(perm)
+    none = torch.full((4,), -1, dtype=torch.int64)
+    _, _, qi = o.kv_write_rope(k, v, none, pos, cs, kc, kc, q=q, neox_style=False)
+    _, _, qn = o.kv_write_rope(k, v, none, pos, cs, kc, kc, q=q[..., perm].contiguous(), neox_style=True)
+    assert torch.equal(qi.view(torch.int16), qn[..., inv].contiguous().view(torch.int16))
+
+
+def pin_rope_relative_position(o):
+    """<R(m) q, R(n) k> depends only on m - n (up to bf16 rounding of the rotated vectors)."""
+    k, v, q, kc = _rope_case(T=1, Hkv=1, Hq=1, D=64, seed=4)
+    cs = rope_table(200, 64).float()
+    none = torch.full((1,), -1, dtype=torch.int64)
+
+    def rot(x, p):
+        _, _, y = o.kv_write_rope(k, v, none, torch.tensor([p]), cs, kc[:, :1], kc[:, :1], q=x)
+        return y.double().flatten()
+
+    base = float(rot(q, 40) @ rot(k.reshape(1, 1, 64), 25))
+    for d in (0, 17, 100, 150):
+        other = float(rot(q, 40 + d) @ rot(k.reshape(1, 1, 64), 25 + d))
+        assert abs(other - base) < 0.05 * (1 + abs(base)), (d, other, base)
+
+
+def pin_rope_partial_rotary(o):
+    """Coordinates at or past rotary_dim are copied unchanged; the rest match a full
+    rotation of the first rotary_dim coordinates."""
+    k, v, q, kc = _rope_case(T=3, D=32)
+    cs = rope_table(10, 16).float()
+    pos = torch.tensor([1, 4, 9], dtype=torch.int64)
+    none = torch.full((3,), -1, dtype=torch.int64)
+    _, _, qp = o.kv_write_rope(k, v, none, pos, cs, kc, kc, q=q, rotary_dim=16)
+    assert torch.equal(qp[..., 16:].contiguous().view(torch.int16), q[..., 16:].contiguous().view(torch.int16))
+    kc16 = torch.zeros(4, 2, 4, 16, dtype=torch.bfloat16)
+    _, _, qf = o.kv_write_rope(k[..., :16].contiguous(), v[..., :16].contiguous(), none, pos, cs,
+                               kc16, kc16, q=q[..., :16].contiguous())
+    assert torch.equal(qp[..., :16].contiguous().view(torch.int16), qf.view(torch.int16))
+
+
 ALL_PINS = [
     pin_bf16_widening, pin_bf16_rounding, pin_write, pin_sdpa, pin_paged_equals_dense,
     pin_pool_permutations, pin_length_one, pin_identical_keys_and_zero_scale, pin_two_tokens,
     pin_context_zero, pin_nan_poison, pin_partitions, pin_cached_equals_recompute,
+    pin_rope_zero_angle_is_identity, pin_rope_is_complex_rotation, pin_rope_pairing_permutation,
+    pin_rope_relative_position, pin_rope_partial_rotary,
 ]

@@ -36,6 +36,12 @@ MUTATIONS = {
     "rounding_ties_away": ("(frac == 0.5 && fmod(n, 2.0) != 0.0)", "(frac == 0.5)"),
     "widening_drops_low_bits": ("uint32_t u = ((uint32_t)bits) << 16;",
                                 "uint32_t u = ((uint32_t)(bits & 0xFF80)) << 16;"),
+    "rope_sine_sign": ("const float r1 = p1 - p2, r2 = p3 + p4;",
+                       "const float r1 = p1 + p2, r2 = p3 - p4;"),
+    "rope_wrong_partner": ("const int32_t a = neox ? i : 2 * i, b = neox ? i + half : 2 * i + 1;",
+                           "const int32_t a = neox ? i : 2 * i, b = neox ? (i + 1) % half : 2 * i + 1;"),
+    "rope_cos_sin_swapped": ("const float c = cs[i], s = cs[half + i];",
+                             "const float c = cs[half + i], s = cs[i];"),
     "q_row_of_wrong_head": (
         "qd[d] = oracle_bf16_to_double(q[((int64_t)b * num_q_heads + h) * head_dim + d]);",
         "qd[d] = oracle_bf16_to_double(q[((int64_t)b * num_q_heads + (h ^ 1)) * head_dim + d]);"),
