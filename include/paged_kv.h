@@ -70,7 +70,8 @@ enum {
   PKV_DEVERR_BLOCK_ID = 1,     /* a block table entry outside [0, num_blocks): read as block 0 */
   PKV_DEVERR_SLOT = 2,         /* a slot >= num_blocks * block_size: that token was skipped */
   PKV_DEVERR_CONTEXT_LEN = 4,  /* context_len < 0 or over the table/max_context_len: clamped */
-  PKV_DEVERR_TIMEOUT = 8       /* a pipeline wait gave up (should never happen): output invalid */
+  PKV_DEVERR_TIMEOUT = 8,      /* a pipeline wait gave up (should never happen): output invalid */
+  PKV_DEVERR_POSITION = 16     /* a RoPE position outside [0, max_position): that row skipped */
 };
 
 /*
@@ -88,6 +89,32 @@ enum {
 int paged_kv_write(const pkv_bf16 *k, const pkv_bf16 *v, const int64_t *slot_mapping,
                    int64_t num_tokens, pkv_bf16 *k_cache, pkv_bf16 *v_cache,
                    const pkv_cache_desc *cache, void *stream);
+
+/*
+ * paged_kv_write_rope -- the slot-mapping write with rotary position embedding fused
+ * in ("llm-stack", Serving engine: RoPE is applied at absolute positions before keys
+ * enter the cache; "Building ... with tiny-vLLM", CUDA kernel engineering: RoPE
+ * rotates coordinate pairs by sine/cosine of position-dependent angles).
+ *
+ * For token i at position p = positions[i] (0 <= p < max_position), each head row x
+ * of k[i] (and of q[i] when q != NULL, in place) is rotated pairwise:
+ *   neox_style != 0: pairs (e, e + r/2), e < r/2 ("rotate half");
+ *   neox_style == 0: pairs (2e, 2e + 1)   (interleaved);
+ *   x1' = x1 * cos_sin[p][e] - x2 * cos_sin[p][r/2 + e],
+ *   x2' = x2 * cos_sin[p][e] + x1 * cos_sin[p][r/2 + e],
+ * in fp32 with every product and sum rounded once (no fused multiply-add), then
+ * rounded to bf16 (nearest even); coordinates at or past r = rotary_dim are copied.
+ * Then k' and v are written like paged_kv_write.  cos_sin is DEVICE fp32
+ * [max_position][rotary_dim] (cosines first, then sines), made by the caller (e.g.
+ * angle(p, e) = p * base^(-2e/r)).  q is [num_tokens][num_q_heads][head_dim].
+ * rotary_dim: a positive multiple of 16, <= head_dim.  A position out of range
+ * skips that token's rows and raises PKV_DEVERR_POSITION.
+ */
+int paged_kv_write_rope(const pkv_bf16 *k, const pkv_bf16 *v, pkv_bf16 *q, int32_t num_q_heads,
+                        const int64_t *slot_mapping, const int64_t *positions,
+                        int64_t num_tokens, const float *cos_sin, int64_t max_position,
+                        int32_t rotary_dim, int32_t neox_style, pkv_bf16 *k_cache,
+                        pkv_bf16 *v_cache, const pkv_cache_desc *cache, void *stream);
 
 /*
  * paged_decode_plan -- the launcher's split choice ("vLLM-Style Llama Inference

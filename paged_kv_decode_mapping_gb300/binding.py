@@ -28,7 +28,7 @@ PKV_OK = 0
 ERRORS = {-1: "PKV_ERR_NULL", -2: "PKV_ERR_SHAPE", -3: "PKV_ERR_UNSUPPORTED",
           -4: "PKV_ERR_WORKSPACE", -5: "PKV_ERR_ALIGN", -6: "PKV_ERR_CUDA", -7: "PKV_ERR_DEVICE",
           -8: "PKV_ERR_NOSPACE"}
-DEVERR = {1: "BLOCK_ID", 2: "SLOT", 4: "CONTEXT_LEN", 8: "TIMEOUT"}
+DEVERR = {1: "BLOCK_ID", 2: "SLOT", 4: "CONTEXT_LEN", 8: "TIMEOUT", 16: "POSITION"}
 
 
 class PkvError(RuntimeError):
@@ -49,6 +49,9 @@ _D = ctypes.POINTER(pkv_cache_desc)
 
 _lib.paged_kv_write.argtypes = [_P, _P, _P, _i64, _P, _P, _D, _P]
 _lib.paged_kv_write.restype = ctypes.c_int
+_lib.paged_kv_write_rope.argtypes = [_P, _P, _P, _i32, _P, _P, _i64, _P, _i64, _i32, _i32, _P, _P,
+                                     _D, _P]
+_lib.paged_kv_write_rope.restype = ctypes.c_int
 _lib.paged_decode_plan.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
 _lib.paged_decode_plan.restype = _i32
 _lib.paged_decode_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32]
@@ -141,6 +144,36 @@ def paged_kv_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
     d = cache_desc(k_cache)
     _check(_lib.paged_kv_write(_ptr(k), _ptr(v), _ptr(slot_mapping), k.shape[0], _ptr(k_cache),
                                _ptr(v_cache), ctypes.byref(d), _stream(stream)), "paged_kv_write")
+
+
+def paged_kv_write_rope(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                        positions: torch.Tensor, cos_sin: torch.Tensor, k_cache: torch.Tensor,
+                        v_cache: torch.Tensor, q: Optional[torch.Tensor] = None,
+                        rotary_dim: Optional[int] = None, neox_style: bool = True,
+                        stream=None) -> None:
+    """RoPE of k (and q, in place) at `positions`, then the slot write of k and v."""
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1)
+    _need(positions, "positions", torch.int64, 1)
+    _need(cos_sin, "cos_sin", torch.float32, 2)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    if q is not None:
+        _need(q, "q", torch.bfloat16, 3)
+        if q.shape[0] != k.shape[0] or q.shape[2] != k.shape[2]:
+            raise ValueError("q must be [T, Hq, D] with k's T and D")
+    r = k.shape[2] if rotary_dim is None else int(rotary_dim)
+    if cos_sin.shape[1] != r:
+        raise ValueError("cos_sin must be [max_position, rotary_dim]")
+    if not (k.shape[0] == slot_mapping.shape[0] == positions.shape[0]):
+        raise ValueError("k, slot_mapping and positions must have the same number of tokens")
+    d = cache_desc(k_cache)
+    _check(_lib.paged_kv_write_rope(_ptr(k), _ptr(v), _ptr(q), 0 if q is None else q.shape[1],
+                                    _ptr(slot_mapping), _ptr(positions), k.shape[0], _ptr(cos_sin),
+                                    cos_sin.shape[0], r, 1 if neox_style else 0, _ptr(k_cache),
+                                    _ptr(v_cache), ctypes.byref(d), _stream(stream)),
+           "paged_kv_write_rope")
 
 
 def paged_decode_plan(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,

@@ -401,3 +401,60 @@ def test_block_manager_driven_decode_steps(B, oracle):
         assert torch.equal(kg.cpu().view(torch.int16), kc.view(torch.int16))
         assert torch.equal(vg.cpu().view(torch.int16), vc.view(torch.int16))
     assert_no_device_errors(B)
+
+
+# ---------------------------------------------------------------- fused RoPE write
+from pins import rope_table  # noqa: E402
+
+
+@pytest.mark.parametrize("D,r,neox,Hq,Hkv", [(64, 64, True, 8, 2), (128, 128, True, 24, 8),
+                                             (128, 128, False, 12, 4), (64, 32, True, 4, 4),
+                                             (128, 64, False, 16, 2), (64, 16, True, 8, 1)])
+def test_rope_write_bit_exact(B, oracle, D, r, neox, Hq, Hkv):
+    T, BS, NB, maxpos = 37, 16, 20, 5000
+    gen = torch.Generator().manual_seed(D + r + Hq)
+    rnd = lambda *s: torch.randn(*s, generator=gen).to(torch.bfloat16)
+    k, v, q = rnd(T, Hkv, D), rnd(T, Hkv, D), rnd(T, Hq, D)
+    kc, vc = rnd(NB, Hkv, BS, D), rnd(NB, Hkv, BS, D)
+    slots = torch.randperm(NB * BS, generator=gen)[:T].to(torch.int64)
+    slots[3] = -1
+    pos = torch.randint(0, maxpos, (T,), generator=gen, dtype=torch.int64)
+    cs = rope_table(maxpos, r, base=500000.0).float()
+    ek, ev, eq = oracle.kv_write_rope(k, v, slots, pos, cs, kc, vc, q=q, rotary_dim=r, neox_style=neox)
+    kg, vg, qg = kc.cuda(), vc.cuda(), q.cuda()
+    B.paged_kv_write_rope(k.cuda(), v.cuda(), slots.cuda(), pos.cuda(), cs.cuda(), kg, vg, q=qg,
+                          rotary_dim=r, neox_style=neox)
+    torch.cuda.synchronize()
+    assert torch.equal(kg.cpu().view(torch.int16), ek.view(torch.int16))
+    assert torch.equal(vg.cpu().view(torch.int16), ev.view(torch.int16))
+    assert torch.equal(qg.cpu().view(torch.int16), eq.view(torch.int16))
+    assert_no_device_errors(B)
+
+
+def test_rope_write_then_decode(B, oracle):
+    """One decode step with RoPE: rotate the step's q and new k at position L-1, write, attend."""
+    w = W.small_workload(B=4, Hq=32, Hkv=8, D=128, BS=16, lens=(1, 200, 513, 1300), seed=33)
+    inp = W.make_inputs(w, poison=True)
+    pos = (inp["context_lens"].long() - 1).clamp(min=0)
+    cs = rope_table(2048, 128).float()
+    kc, vc, qr = oracle.kv_write_rope(inp["k_new"], inp["v_new"], inp["slot_mapping"], pos, cs,
+                                      inp["k_cache"], inp["v_cache"], q=inp["q"])
+    ref = oracle.decode(qr, kc, vc, inp["block_tables"], inp["context_lens"], inp["scale"])
+    g = dev(inp)
+    B.paged_kv_write_rope(g["k_new"], g["v_new"], g["slot_mapping"], pos.cuda(), cs.cuda(),
+                          g["k_cache"], g["v_cache"], q=g["q"])
+    out = torch.empty_like(g["q"])
+    B.paged_decode_attention(out, g["q"], g["k_cache"], g["v_cache"], g["block_tables"],
+                             g["context_lens"], g["max_context_len"], g["scale"])
+    check_attention(out, ref, "rope + decode")
+    assert torch.equal(g["q"].cpu().view(torch.int16), qr.view(torch.int16))
+
+
+def test_rope_position_out_of_range_is_flagged(B):
+    k = torch.zeros(2, 1, 64, dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros(4, 1, 16, 64, dtype=torch.bfloat16, device="cuda")
+    cs = rope_table(8, 64).float().cuda()
+    B.pkv_device_errors(clear=True)
+    B.paged_kv_write_rope(k, k, torch.tensor([0, 1], device="cuda"), torch.tensor([3, 8], device="cuda"),
+                          cs, kc, kc.clone())
+    assert B.pkv_device_errors(clear=True) == 16
