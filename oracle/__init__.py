@@ -67,6 +67,9 @@ class Oracle:
         L.oracle_kv_write_rope.argtypes = [P, P, P, i32, P, P, i64, P, i64, i32, i32, P, P, i64,
                                            i32, i32, i32]
         L.oracle_kv_write_rope.restype = ctypes.c_int
+        L.oracle_prefill_attention.argtypes = [P, P, P, P, P, i32, P, P, i32, i32, i32, i64, i32,
+                                               i32, dbl]
+        L.oracle_prefill_attention.restype = ctypes.c_int
         self._L = L
 
     # -- helpers -------------------------------------------------------------
@@ -158,6 +161,22 @@ class Oracle:
                                             self._p(cl), B, Hq, Hkv, NB, BS, D, float(scale),
                                             num_threads)
         self._check(rc, "decode")
+        return torch.from_numpy(out)
+
+    def prefill(self, q, k_cache, v_cache, block_tables, context_lens, query_start,
+                scale: float) -> torch.Tensor:
+        """fp64 causal attention of each sequence's last n_b tokens (packed q [Nq, Hq, D])."""
+        Nq, Hq, D = q.shape
+        NB, Hkv, BS, _ = k_cache.shape
+        qa, ka, va = self._u16(q), self._u16(k_cache), self._u16(v_cache)
+        bt = self._arr(block_tables, np.int32)
+        cl = self._arr(context_lens, np.int32)
+        qs = self._arr(query_start, np.int32)
+        out = np.zeros((Nq, Hq, D), dtype=np.float64)
+        rc = self._L.oracle_prefill_attention(self._p(out), self._p(qa), self._p(ka), self._p(va),
+                                              self._p(bt), bt.shape[1], self._p(cl), self._p(qs),
+                                              len(cl), Hq, Hkv, NB, BS, D, float(scale))
+        self._check(rc, "prefill")
         return torch.from_numpy(out)
 
     def decode_partitions(self, b: int, h: int, num_parts: int, partition_tokens: int, q,

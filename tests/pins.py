@@ -373,10 +373,53 @@ def pin_rope_partial_rotary(o):
     assert torch.equal(qp[..., :16].contiguous().view(torch.int16), qf.view(torch.int16))
 
 
+# ---------------------------------------------------------------- paged prefill
+def _prefill_case(lens=(9, 23, 4), chunks=(9, 5, 1), Hq=8, Hkv=2, D=16, BS=4, seed=3):
+    inp = _case(B=len(lens), Hq=Hq, Hkv=Hkv, D=D, BS=BS, lens=lens, seed=seed, write="none")
+    g = torch.Generator().manual_seed(seed + 1)
+    qs = torch.tensor([0] + list(itertools.accumulate(chunks)), dtype=torch.int32)
+    q = torch.randn(int(qs[-1]), Hq, D, generator=g).to(torch.bfloat16)
+    return inp, q, qs
+
+
+def pin_prefill_matches_sdpa_with_causal_mask(o):
+    """Chunked prefill == torch fp64 SDPA over the gathered keys with the mask t <= p
+    (is_causal=True when the chunk is the whole context)."""
+    for lens, chunks in (((9, 23, 4), (9, 5, 1)), ((16, 7), (16, 7))):
+        inp, q, qs = _prefill_case(lens, chunks)
+        got = o.prefill(q, inp["k_cache"], inp["v_cache"], inp["block_tables"], inp["context_lens"],
+                        qs, inp["scale"])
+        Hq, Hkv = q.shape[1], inp["k_cache"].shape[1]
+        for b, (L, n) in enumerate(zip(lens, chunks)):
+            K = torch.stack([_gather(inp["k_cache"], inp["block_tables"][b], L, g) for g in range(Hkv)])
+            V = torch.stack([_gather(inp["v_cache"], inp["block_tables"][b], L, g) for g in range(Hkv)])
+            K, V = K.repeat_interleave(Hq // Hkv, 0)[None], V.repeat_interleave(Hq // Hkv, 0)[None]
+            qq = q[int(qs[b]):int(qs[b + 1])].double().permute(1, 0, 2)[None]  # [1, Hq, n, D]
+            if n == L:
+                ref = F.scaled_dot_product_attention(qq, K, V, is_causal=True, scale=inp["scale"])
+            else:
+                pos = torch.arange(L - n, L)[:, None]
+                mask = torch.arange(L)[None, :] <= pos
+                ref = F.scaled_dot_product_attention(qq, K, V, attn_mask=mask, scale=inp["scale"])
+            assert torch.allclose(got[int(qs[b]):int(qs[b + 1])], ref[0].permute(1, 0, 2), atol=1e-12)
+
+
+def pin_prefill_last_token_is_decode(o):
+    """The last query of each chunk sees every cached key: it equals decode attention."""
+    inp, q, qs = _prefill_case()
+    got = o.prefill(q, inp["k_cache"], inp["v_cache"], inp["block_tables"], inp["context_lens"],
+                    qs, inp["scale"])
+    last = q[(qs[1:] - 1).long()]
+    dec = o.decode(last, inp["k_cache"], inp["v_cache"], inp["block_tables"], inp["context_lens"],
+                   inp["scale"])
+    assert torch.equal(got[(qs[1:] - 1).long()], dec)
+
+
 ALL_PINS = [
     pin_bf16_widening, pin_bf16_rounding, pin_write, pin_sdpa, pin_paged_equals_dense,
     pin_pool_permutations, pin_length_one, pin_identical_keys_and_zero_scale, pin_two_tokens,
     pin_context_zero, pin_nan_poison, pin_partitions, pin_cached_equals_recompute,
     pin_rope_zero_angle_is_identity, pin_rope_is_complex_rotation, pin_rope_pairing_permutation,
     pin_rope_relative_position, pin_rope_partial_rotary,
+    pin_prefill_matches_sdpa_with_causal_mask, pin_prefill_last_token_is_decode,
 ]

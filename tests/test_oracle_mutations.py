@@ -42,6 +42,10 @@ MUTATIONS = {
                            "const int32_t a = neox ? i : 2 * i, b = neox ? (i + 1) % half : 2 * i + 1;"),
     "rope_cos_sin_swapped": ("const float c = cs[i], s = cs[half + i];",
                              "const float c = cs[half + i], s = cs[i];"),
+    "prefill_causal_off_by_one": ("attend_range(out + row, &lse, qd, Kd, Vd, 0, pos + 1, head_dim, scale, s);",
+                                  "attend_range(out + row, &lse, qd, Kd, Vd, 0, pos, head_dim, scale, s);"),
+    "prefill_position_from_chunk_start": ("const int32_t pos = len - n + i;",
+                                          "const int32_t pos = i;"),
     "q_row_of_wrong_head": (
         "qd[d] = oracle_bf16_to_double(q[((int64_t)b * num_q_heads + h) * head_dim + d]);",
         "qd[d] = oracle_bf16_to_double(q[((int64_t)b * num_q_heads + (h ^ 1)) * head_dim + d]);"),
