@@ -198,6 +198,29 @@ int paged_decode_step(pkv_bf16 *out, const pkv_bf16 *q, const pkv_bf16 *k, const
                       void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * paged_prefill_attention -- causal attention of each sequence's newest tokens over
+ * the paged cache: prefill, chunked prefill, or recomputation after preemption
+ * ("vLLM-Style Llama Inference Engine", How it works: prefill and recomputation use
+ * causal attention).
+ *
+ * Sequence b holds L_b = context_lens[b] tokens in the cache (their K/V already
+ * written, e.g. by paged_kv_write); its last n_b = query_start[b+1] - query_start[b]
+ * tokens are the queries, packed in q [num_queries][num_q_heads][head_dim] at rows
+ * query_start[b] .. query_start[b+1]-1 (query_start is DEVICE int32 [num_seqs + 1],
+ * nondecreasing).  Query i of sequence b sits at position p = L_b - n_b + i and
+ *   out[row][h] = bf16( sum_{t <= p} softmax_t(scale * <q[row][h], K_t>) V_t )
+ * with K_t, V_t read through block_tables as in paged_decode_attention (same head
+ * mapping, sizes and alignment rules; out is 4-byte aligned).  max_query_len >= every
+ * n_b sizes the grid.  Every out row of a query is written; nothing else.
+ */
+int paged_prefill_attention(pkv_bf16 *out, const pkv_bf16 *q, const pkv_bf16 *k_cache,
+                            const pkv_bf16 *v_cache, const int32_t *block_tables,
+                            int32_t max_blocks_per_seq, const int32_t *context_lens,
+                            int32_t max_context_len, const int32_t *query_start,
+                            int32_t max_query_len, int32_t num_seqs, int32_t num_q_heads,
+                            const pkv_cache_desc *cache, float scale, void *stream);
+
+/*
  * paged_decode_split -- flash-decoding partition kernel (split-K over the keys;
  * the FlashAttention-2 online-softmax algebra that the first page references).
  *

@@ -64,6 +64,9 @@ _lib.paged_decode_attention.restype = ctypes.c_int
 _lib.paged_decode_step.argtypes = [_P, _P, _P, _P, _P, _i64, _P, _P, _P, _i32, _P, _i32, _i32,
                                    _i32, _D, _f32, _P, _sz, _P]
 _lib.paged_decode_step.restype = ctypes.c_int
+_lib.paged_prefill_attention.argtypes = [_P, _P, _P, _P, _P, _i32, _P, _i32, _P, _i32, _i32, _i32,
+                                         _D, _f32, _P]
+_lib.paged_prefill_attention.restype = ctypes.c_int
 _lib.paged_decode_split.argtypes = [_P, _P, _P, _P, _P, _P, _i32, _P, _i32, _i32, _i32, _D, _f32,
                                     _i32, _P]
 _lib.paged_decode_split.restype = ctypes.c_int
@@ -258,6 +261,31 @@ def paged_decode_step(out: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: to
                                   block_tables.shape[1], _ptr(context_lens), int(max_context_len),
                                   B, Hq, ctypes.byref(d), float(scale), _ptr(workspace), ws_bytes,
                                   _stream(stream)), "paged_decode_step")
+
+
+def paged_prefill_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                            v_cache: torch.Tensor, block_tables: torch.Tensor,
+                            context_lens: torch.Tensor, max_context_len: int,
+                            query_start: torch.Tensor, max_query_len: int, scale: float,
+                            stream=None) -> None:
+    """Causal attention of each sequence's last n_b cached tokens (packed q [Nq, Hq, D])."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(out, "out", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    _need(query_start, "query_start", torch.int32, 1)
+    B = context_lens.shape[0]
+    if out.shape != q.shape or query_start.shape[0] != B + 1 or block_tables.shape[0] != B:
+        raise ValueError("out/q, query_start [B+1] or block_tables [B, M] disagree")
+    d = cache_desc(k_cache)
+    _check(_lib.paged_prefill_attention(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                        _ptr(block_tables), block_tables.shape[1],
+                                        _ptr(context_lens), int(max_context_len),
+                                        _ptr(query_start), int(max_query_len), B, q.shape[1],
+                                        ctypes.byref(d), float(scale), _stream(stream)),
+           "paged_prefill_attention")
 
 
 def paged_decode_attention_noalloc(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,

@@ -458,3 +458,53 @@ def test_rope_position_out_of_range_is_flagged(B):
     B.paged_kv_write_rope(k, k, torch.tensor([0, 1], device="cuda"), torch.tensor([3, 8], device="cuda"),
                           cs, kc, kc.clone())
     assert B.pkv_device_errors(clear=True) == 16
+
+
+# ------------------------------------------------------------------ paged prefill
+PREFILL = [
+    # D, BS, Hq, Hkv, lens, chunks
+    (64, 16, 8, 2, (37, 100, 1, 300), (37, 20, 1, 300)),
+    (128, 16, 24, 8, (513, 64, 1000), (513, 64, 7)),
+    (128, 32, 12, 4, (65, 130), (1, 130)),
+    (64, 8, 4, 4, (200, 31, 17), (50, 31, 16)),
+    (64, 128, 16, 2, (700, 2), (120, 2)),
+    (128, 16, 8, 1, (90, 90), (90, 45)),
+]
+
+
+@pytest.mark.parametrize("D,BS,Hq,Hkv,lens,chunks", PREFILL)
+def test_prefill_matches_oracle(B, oracle, D, BS, Hq, Hkv, lens, chunks):
+    import itertools
+    w = W.small_workload(B=len(lens), Hq=Hq, Hkv=Hkv, D=D, BS=BS, lens=lens, seed=D + BS + Hq,
+                         write="none")
+    inp = W.make_inputs(w, poison=True)
+    gen = torch.Generator().manual_seed(len(lens))
+    qs = torch.tensor([0] + list(itertools.accumulate(chunks)), dtype=torch.int32)
+    q = torch.randn(int(qs[-1]), Hq, D, generator=gen).to(torch.bfloat16)
+    ref = oracle.prefill(q, inp["k_cache"], inp["v_cache"], inp["block_tables"], inp["context_lens"],
+                         qs, inp["scale"])
+    g = dev(inp)
+    out = torch.full((int(qs[-1]), Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    B.paged_prefill_attention(out, q.cuda(), g["k_cache"], g["v_cache"], g["block_tables"],
+                              g["context_lens"], inp["max_context_len"], qs.cuda(), max(chunks),
+                              inp["scale"])
+    check_attention(out, ref, f"prefill D={D} BS={BS} G={Hq // Hkv}")
+    assert_no_device_errors(B)
+
+
+def test_prefill_single_token_chunks_equal_decode(B, oracle):
+    """A chunk of one token per sequence is a decode step."""
+    w = W.small_workload(B=3, Hq=32, Hkv=8, D=64, BS=16, lens=(5, 900, 2048), seed=51, write="none")
+    inp = W.make_inputs(w, poison=True)
+    g = dev(inp)
+    qs = torch.arange(4, dtype=torch.int32).cuda()
+    out = torch.empty_like(g["q"])
+    B.paged_prefill_attention(out, g["q"], g["k_cache"], g["v_cache"], g["block_tables"],
+                              g["context_lens"], inp["max_context_len"], qs, 1, inp["scale"])
+    dec = torch.empty_like(g["q"])
+    B.paged_decode_attention(dec, g["q"], g["k_cache"], g["v_cache"], g["block_tables"],
+                             g["context_lens"], inp["max_context_len"], inp["scale"])
+    ref = oracle.decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_tables"],
+                        inp["context_lens"], inp["scale"])
+    check_attention(out, ref, "prefill n=1")
+    check_attention(dec, ref, "decode")
