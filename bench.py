@@ -21,9 +21,11 @@ max over ranks is reported.  `value` is algorithmic HBM bytes per step / time,
 in GB/s (whole job: all ranks' bytes / the slowest rank's time).
 
 `roofline` covers the dominant kernel (the decode kernel), timed alone by
-the same method; `e2e` runs the same step eagerly through the public API with the
-step's inputs copied from pinned host memory and the output read back each step;
+the same method; `e2e` runs the same step through the public API with the step's
+inputs copied from pinned host memory and the output read back each step;
 `cpu_baseline` is the CPU oracle (fp64, all host cores) on the same workload.
+`e2e` replays the whole step -- copies in, paged_decode_step, copy out -- as one CUDA
+graph per step (the eager time is reported beside it).
 
 `--impl reference` times that oracle as the reference arm (rank 0 only).
 """
@@ -347,35 +349,63 @@ def run_ours(args, w) -> None:
     dec_s = t_dec / args.steps
     achieved = nb["decode_kernel"] / dec_s / 1e9
 
-    # end to end through the public API: pinned host inputs in, output back, every step
-    host = {k: inp[k].pin_memory() for k in ("q", "k_new", "v_new", "slot_mapping",
-                                               "block_tables", "context_lens")}
+    # end to end through the public API: pinned host inputs in, output back, every step.
+    # The step -- the host-to-device copy of its inputs, paged_decode_step, the
+    # device-to-host copy of out -- is captured once as a CUDA graph and replayed, then
+    # synchronised, each step; the same step run eagerly is reported beside it.
+    # one pinned staging buffer holds all of the step's inputs (256-byte aligned pieces),
+    # so they cross in a single host-to-device copy
+    names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")
+    offs, total = [], 0
+    for k in names:
+        offs.append(total)
+        total += -(-inp[k].numel() * inp[k].element_size() // 256) * 256
+    stage_h = torch.empty(total, dtype=torch.uint8).pin_memory()
+    stage_d = torch.empty(total, dtype=torch.uint8, device=device)
+
+    def view(buf, k, o):
+        t = inp[k]
+        n = t.numel() * t.element_size()
+        return buf[o:o + n].view(t.dtype).view(t.shape)
+
+    for k, o in zip(names, offs):
+        view(stage_h, k, o).copy_(inp[k])
+    dq, dkn, dvn, dsm, dbt, dcl = (view(stage_d, k, o) for k, o in zip(names, offs))
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = sum(inp[k].numel() * inp[k].element_size() for k in names)
     d2h = out_h.numel() * out_h.element_size()
-    dq, dkn, dvn, dsm, dbt, dcl = (torch.empty_like(t, device=device) for t in host.values())
     e2e_steps = max(20, min(args.steps, 2000))
 
-    def e2e_step(r):
-        for dst, src in zip((dq, dkn, dvn, dsm, dbt, dcl), host.values()):
-            dst.copy_(src, non_blocking=True)
+    def e2e_body(r):
+        stage_d.copy_(stage_h, non_blocking=True)
         B.paged_decode_step(out, dq, dkn, dvn, dsm, kcs[r], vcs[r], dbt, dcl, max_len, scale,
                             workspace=ws)
         out_h.copy_(out, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
 
-    with torch.cuda.stream(stream):
-        for i in range(3):
-            e2e_step(i % R)
-        barrier(world)
+    def time_e2e(run) -> float:
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                run(i % R)
+                stream.synchronize()
+            barrier(world)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(e2e_steps):
+                run(i % R)
+                stream.synchronize()  # the host reads the step's output
+            e1.record(stream)
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(e2e_steps):
-            e2e_step(i % R)
-        e1.record(stream)
-    torch.cuda.synchronize()
-    t_e2e = reduce_max(e0.elapsed_time(e1) / 1e3 / e2e_steps, world, device)
+        return reduce_max(e0.elapsed_time(e1) / 1e3 / e2e_steps, world, device)
+
+    e2e_graphs = []
+    for r in range(R):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            e2e_body(r)
+        e2e_graphs.append(gr)
+    t_e2e = time_e2e(lambda r: e2e_graphs[r].replay())
+    t_e2e_eager = time_e2e(e2e_body)
     e2e_value = reduce_sum(nb["step"], world, device) / t_e2e / 1e9
 
     peaks = measured_peaks()
@@ -406,7 +436,10 @@ def run_ours(args, w) -> None:
                      "traffic": traffic},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "us_per_step": t_e2e * 1e6},
+                "d2h_bytes_per_step": d2h, "us_per_step": t_e2e * 1e6,
+                "how": "one pinned H2D copy of the step's inputs + paged_decode_step + D2H of "
+                       "out, one CUDA graph replayed and synchronised per step",
+                "eager_us_per_step": t_e2e_eager * 1e6},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
@@ -415,6 +448,99 @@ def run_ours(args, w) -> None:
         import torch.distributed as dist
 
         dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- other kernels
+def run_kernel(args, w) -> None:
+    """Times one of the other kernels on the workload's shapes (graph replays, rotating
+    pool copies, CUDA events) and prints one JSON line for it."""
+    import itertools
+
+    from paged_kv_decode_mapping_gb300 import binding as B
+
+    device = torch.device("cuda", 0)
+    inp = W.make_inputs(w)
+    Bn, Hq, D = inp["q"].shape
+    NB, Hkv, BS, _ = inp["k_cache"].shape
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    R = max(2, math.ceil(3 * l2 / (2 * inp["k_cache"].numel() * 2)))
+    kcs = [inp["k_cache"].to(device) for _ in range(R)]
+    vcs = [inp["v_cache"].to(device) for _ in range(R)]
+    bt, cl = inp["block_tables"].to(device), inp["context_lens"].to(device)
+    gen = torch.Generator().manual_seed(w.seed + 1)
+    peaks = measured_peaks()
+    line = {"n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "data": "synthetic",
+            "dtype": "bf16", "vs_baseline": None, "scaling": "weak",
+            "config": config_dict(w, inp, args, 1)}
+    if args.kernel == "prefill":
+        lens = inp["context_lens"].long()
+        chunks = torch.clamp(lens, max=args.chunk)
+        qs = torch.tensor([0] + list(itertools.accumulate(chunks.tolist())), dtype=torch.int32)
+        nq = int(qs[-1])
+        q = torch.randn(nq, Hq, D, generator=gen).to(torch.bfloat16).to(device)
+        out = torch.empty_like(q)
+        qsd = qs.to(device)
+        # useful flops: each query at position p does (p+1) keys x (QK + PV) x 2 flops x D
+        keys = sum(int(L * n - n * (n - 1) // 2) for L, n in zip(lens.tolist(), chunks.tolist()))
+        flops = keys * Hq * D * 4
+
+        def fn(r):
+            B.paged_prefill_attention(out, q, kcs[r], vcs[r], bt, cl, inp["max_context_len"], qsd,
+                                      int(chunks.max()), inp["scale"])
+        unit, per = "TFLOP/s", flops / 1e12
+        bound, peak = "tensor", peaks.get("bf16_tflops") or 1900.0
+        metric = f"paged prefill attention (last min(L, {args.chunk}) tokens of each sequence) TFLOP/s"
+    else:  # rope_write
+        T = Bn
+        kn = torch.randn(T, Hkv, D, generator=gen).to(torch.bfloat16).to(device)
+        vn = torch.randn(T, Hkv, D, generator=gen).to(torch.bfloat16).to(device)
+        q = inp["q"].to(device)
+        sm = inp["slot_mapping"][:T].to(device) if inp["slot_mapping"].numel() >= T else \
+            torch.arange(T, dtype=torch.int64, device=device)
+        pos = (inp["context_lens"].long() - 1).clamp(min=0).to(device)
+        maxpos = int(inp["max_context_len"]) + 1
+        half = D // 2
+        inv = 10000.0 ** (-torch.arange(half, dtype=torch.float64) * 2.0 / D)
+        ang = torch.arange(maxpos, dtype=torch.float64)[:, None] * inv[None, :]
+        cs = torch.cat([ang.cos(), ang.sin()], 1).float().to(device)
+        nbytes = T * (Hkv * D * 2 * 4 + Hq * D * 2 * 2 + 16 + D * 4 * 2)
+
+        def fn(r):
+            B.paged_kv_write_rope(kn, vn, sm, pos, cs, kcs[r], vcs[r], q=q)
+        unit, per = "GB/s", nbytes / 1e9
+        bound, peak = "hbm", peaks.get("hbm_gbs") or 6800.0
+        metric = "fused RoPE + slot write GB/s"
+    stream = torch.cuda.Stream(device)
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            fn(i % R)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for r in range(R):
+            fn(r)
+    reps = max(1, args.steps // R)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(0)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    t = e0.elapsed_time(e1) / 1e3 / (reps * R)
+    value = per / t
+    assert B.pkv_device_errors() == 0
+    line.update({"metric": metric, "value": value, "unit": unit, "ms_per_step": t * 1e3,
+                 "steps": reps * R, "higher_is_better": True,
+                 "roofline": {"bound": bound, "achieved": value, "peak": peak, "unit": unit,
+                              "frac": value / peak, "traffic": None},
+                 "gpu_launches": reps * R, "clocks": clk})
+    print(json.dumps(line), flush=True)
 
 
 def main():
@@ -426,9 +552,14 @@ def main():
     ap.add_argument("--workload", type=int, default=2, choices=sorted(W.WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for the cpu_baseline object (0: skip)")
+    ap.add_argument("--kernel", choices=["step", "prefill", "rope_write"], default="step",
+                    help="step: the decode step (the benchmark line); others time one kernel")
+    ap.add_argument("--chunk", type=int, default=512, help="prefill: query tokens per sequence")
     args = ap.parse_args()
     w = W.WORKLOADS[args.workload]
-    if args.impl == "reference":
+    if args.kernel != "step":
+        run_kernel(args, w)
+    elif args.impl == "reference":
         run_reference(args, w)
     else:
         run_ours(args, w)
