@@ -403,6 +403,78 @@ def test_block_manager_driven_decode_steps(B, oracle):
     assert_no_device_errors(B)
 
 
+
+def test_whole_step_graph_replay(B, oracle):
+    """The whole decode step -- one host-to-device copy of the step's inputs from pinned
+    memory, paged_decode_step, the device-to-host copy of the output -- captured once
+    as a CUDA graph and replayed for several steps, the host buffers refilled between
+    replays (one new token per sequence per step).  Every replay's output matches the
+    oracle, the caches match bit for bit, and the merge counters stay consistent across
+    replays (the lengths need several partitions)."""
+    Bn, Hq, Hkv, D, BS, steps = 3, 8, 2, 64, 16, 5
+    w = W.small_workload(B=Bn, Hq=Hq, Hkv=Hkv, D=D, BS=BS, lens=(1300, 700, 1517), seed=23,
+                         write="none")
+    inp = W.make_inputs(w)
+    final = inp["context_lens"].clone()
+    max_len = int(final.max())
+    assert B.paged_decode_plan(Bn, Hq, Hkv, D, max_len) < max_len  # several partitions
+    kg, vg = inp["k_cache"].cuda(), inp["v_cache"].cuda()
+    names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")
+    shapes = {"q": ((Bn, Hq, D), torch.bfloat16), "k_new": ((Bn, Hkv, D), torch.bfloat16),
+              "v_new": ((Bn, Hkv, D), torch.bfloat16), "slot_mapping": ((Bn,), torch.int64),
+              "block_tables": (tuple(inp["block_tables"].shape), torch.int32),
+              "context_lens": ((Bn,), torch.int32)}
+    host = {k: torch.zeros(*shp, dtype=dt).pin_memory() for k, (shp, dt) in shapes.items()}
+    devb = {k: torch.zeros(*shp, dtype=dt, device="cuda") for k, (shp, dt) in shapes.items()}
+    out = torch.empty(Bn, Hq, D, dtype=torch.bfloat16, device="cuda")
+    out_h = torch.empty(Bn, Hq, D, dtype=torch.bfloat16).pin_memory()
+    ws = torch.zeros(B.paged_decode_workspace_size(Bn, Hq, Hkv, D, max_len), dtype=torch.uint8,
+                     device="cuda")
+
+    def body():
+        for k in names:
+            devb[k].copy_(host[k], non_blocking=True)
+        B.paged_decode_step(out, devb["q"], devb["k_new"], devb["v_new"], devb["slot_mapping"],
+                            kg, vg, devb["block_tables"], devb["context_lens"], max_len,
+                            inp["scale"], workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+
+    gen = torch.Generator().manual_seed(5)
+    rnd = lambda *s: torch.randn(*s, generator=gen).to(torch.bfloat16)
+    kc, vc = inp["k_cache"], inp["v_cache"]
+    lens = final - steps
+    stream = torch.cuda.Stream()
+    graph = None
+    for s in range(steps + 1):
+        lens = lens + 1 if s > 0 else lens
+        slots = torch.tensor([int(inp["block_tables"][b, (int(lens[b]) - 1) // BS]) * BS
+                              + (int(lens[b]) - 1) % BS for b in range(Bn)], dtype=torch.int64)
+        fill = {"q": rnd(Bn, Hq, D), "k_new": rnd(Bn, Hkv, D), "v_new": rnd(Bn, Hkv, D),
+                "slot_mapping": slots, "block_tables": inp["block_tables"],
+                "context_lens": lens.to(torch.int32)}
+        for k in names:
+            host[k].copy_(fill[k])
+        kc, vc = oracle.kv_write(fill["k_new"], fill["v_new"], slots, kc, vc)
+        if s == 0:   # the first step runs eagerly (warm-up), then the graph is captured
+            with torch.cuda.stream(stream):
+                body()
+            stream.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                body()
+        else:
+            with torch.cuda.stream(stream):
+                graph.replay()
+            stream.synchronize()
+        ref = oracle.decode(fill["q"], kc, vc, inp["block_tables"], lens.to(torch.int32),
+                            inp["scale"])
+        check_attention(out_h.clone(), ref, f"graph step {s}")
+    assert torch.equal(kg.cpu().view(torch.int16), kc.view(torch.int16))
+    assert torch.equal(vg.cpu().view(torch.int16), vc.view(torch.int16))
+    assert int(ws[:Bn * Hkv * 4].view(torch.int32).abs().sum()) == 0  # counters back at zero
+    assert_no_device_errors(B)
+
+
 # ---------------------------------------------------------------- fused RoPE write
 from pins import rope_table  # noqa: E402
 
