@@ -124,18 +124,28 @@ def measured_peaks() -> dict:
         return {}
 
 
-def recorded_traffic(kernel_source: str) -> float | None:
+DECODE_SOURCES = ("pkv_decode.cu", "attn_device.cuh", "pkv_internal.h")
+
+
+def decode_source_sha() -> str:
+    """sha256 over the decode kernel's device source files, in a fixed order."""
+    h = hashlib.sha256()
+    for name in DECODE_SOURCES:
+        h.update(open(os.path.join(ROOT, "paged_kv_decode_mapping_gb300", "csrc", name), "rb").read())
+    return h.hexdigest()
+
+
+def recorded_traffic() -> float | None:
     """Per-launch DRAM bytes of the decode kernel from the committed ncu summary, if it
-    was taken on the current kernel source (same sha256); else None."""
+    was taken on the current kernel source (same sha256 over DECODE_SOURCES); else None."""
     path = os.path.join(ROOT, "profiles", "ncu_decode_kernel_workload2.md")
     try:
         text = open(path).read()
     except OSError:
         return None
-    sha = hashlib.sha256(open(kernel_source, "rb").read()).hexdigest()
     m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
     m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m_sha or not m_tr or m_sha.group(1) != sha:
+    if not m_sha or not m_tr or m_sha.group(1) != decode_source_sha():
         return None
     return float(m_tr.group(1))
 
@@ -412,7 +422,7 @@ def run_ours(args, w) -> None:
     peak = peaks.get("hbm_gbs")
     peak_src = "measured" if peak else "fallback"
     peak = peak or 6800.0
-    traffic = recorded_traffic(os.path.join(ROOT, "paged_kv_decode_mapping_gb300", "csrc", "pkv_decode.cu"))
+    traffic = recorded_traffic()
     launches_per_step = 2  # kv_write_kernel + decode_kernel (merge fused)
 
     if rank != 0:

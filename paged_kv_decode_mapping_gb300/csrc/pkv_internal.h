@@ -1,8 +1,11 @@
 // pkv_internal.h -- helpers shared by the library's translation units (not installed).
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (header only)
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <mutex>
 
 #include "paged_kv.h"
 
@@ -28,6 +31,44 @@ int launch_write(const pkv_bf16 *k, const pkv_bf16 *v, const int64_t *slot_mappi
                  const pkv_cache_desc &c, cudaStream_t stream);
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---- shared by the attention kernels (decode and prefill) ----------------------
+constexpr int kChunk = 64;          // keys per pipeline stage
+constexpr int kConsumerWarps = 4;   // 16 keys each
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;
+constexpr int kMaxGroup = 8;        // query heads per kv head (one mma N tile)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kMaxDevices = 64;
+
+// Stages of the TMA ring and the dynamic shared memory of one attention CTA.
+constexpr int split_stages(int d) { return d == 64 ? 4 : 3; }
+constexpr size_t split_smem(int d) {
+  return 1024 + (size_t)split_stages(d) * 2 * kChunk * d * 2 + split_stages(d) * 16 + 16;
+}
+// CTAs of decode_kernel one SM holds (shared memory limited: 66 KB at D=64, 99 KB at D=128).
+constexpr int split_occupancy(int d) { return d == 64 ? 3 : 2; }
+
+// Guards the tensor-map cache, the SM-count cache and the per-device kernel attributes.
+std::mutex &attn_mutex();
+// The current device (0 .. kMaxDevices-1), or a PKV_ERR_CUDA code.
+int current_device(int *dev);
+// SM count of the current device (cached); the caller holds attn_mutex().
+int device_sms(int *sms);
+// Encoded TMA maps of the two pools (cached by pointer and shape); the caller holds
+// attn_mutex().
+int maps_for(const pkv_bf16 *k_cache, const pkv_bf16 *v_cache, const pkv_cache_desc &c,
+             CUtensorMap *tmk, CUtensorMap *tmv);
+// Argument checks shared by the decode and prefill entry points.
+int check_decode(const void *q, const void *k_cache, const void *v_cache, const int32_t *bt,
+                 int32_t max_blocks, const int32_t *lens, int32_t max_len, int32_t num_seqs,
+                 int32_t hq, const pkv_cache_desc *c, const char *fn);
+int ilog2(int x);  // smallest r with 2^r >= x
+
+// Device error words of the attention translation units (read + optional clear).
+cudaError_t read_decode_errors(uint32_t *flags, int clear);
+cudaError_t read_prefill_errors(uint32_t *flags, int clear);
 
 }  // namespace pkv
 
