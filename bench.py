@@ -135,10 +135,11 @@ def decode_source_sha() -> str:
     return h.hexdigest()
 
 
-def recorded_traffic() -> float | None:
-    """Per-launch DRAM bytes of the decode kernel from the committed ncu summary, if it
-    was taken on the current kernel source (same sha256 over DECODE_SOURCES); else None."""
-    path = os.path.join(ROOT, "profiles", "ncu_decode_kernel_workload2.md")
+def recorded_traffic(workload: int) -> float | None:
+    """Per-launch DRAM bytes of the decode kernel on this workload from the committed ncu
+    summary, if it was taken on the current kernel source (same sha256 over
+    DECODE_SOURCES); else None."""
+    path = os.path.join(ROOT, "profiles", f"ncu_decode_kernel_workload{workload}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -283,6 +284,7 @@ def run_ours(args, w) -> None:
     max_len = inp["max_context_len"]
     scale = inp["scale"]
     P = B.paged_decode_plan(Bn, Hq, Hkv, D, max_len)
+    path = B.paged_decode_path(Bn, Hq, Hkv, D, max_len)
 
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     pool_bytes = 2 * inp["k_cache"].numel() * 2
@@ -422,8 +424,11 @@ def run_ours(args, w) -> None:
     peak = peaks.get("hbm_gbs")
     peak_src = "measured" if peak else "fallback"
     peak = peak or 6800.0
-    traffic = recorded_traffic()
-    launches_per_step = 2  # kv_write_kernel + decode_kernel (merge fused)
+    traffic = recorded_traffic(args.workload)
+    launches_per_step = 2  # kv_write_kernel + the fused decode (one launch, merge included)
+    decode_name = {B.PATH_PARTITIONS: "decode_kernel (one CTA per partition, merge by the last)",
+                   B.PATH_CLUSTER: "decode_kernel (partitions of a unit in one cluster, DSMEM merge)",
+                   B.PATH_PERSISTENT: "decode_persistent_kernel (work items, longest first)"}[path]
 
     if rank != 0:
         if world > 1:
@@ -438,8 +443,9 @@ def run_ours(args, w) -> None:
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": config_dict(w, inp, args, world),
         "hbm_frac_of_peak": value / peak,
-        "plan": {"partition_tokens": P, "n_parts": math.ceil(max_len / P), "pool_copies": R},
-        "roofline": {"bound": "hbm", "kernel": "decode_kernel (partitions + fused merge)",
+        "plan": {"partition_tokens": P, "n_parts": math.ceil(max_len / P), "path": path,
+                 "pool_copies": R},
+        "roofline": {"bound": "hbm", "kernel": decode_name,
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_src} hbm_gbs (copy, burst)",
                      "bytes_per_launch": nb["decode_kernel"], "us_per_launch": dec_s * 1e6,

@@ -121,14 +121,33 @@ int paged_kv_write_rope(const pkv_bf16 *k, const pkv_bf16 *v, pkv_bf16 *q, int32
  * Engine", Features and scope, where split-K decode is the named next step).
  *
  * Returns the partition size P in tokens (a multiple of 64) that
- * paged_decode_attention cuts each (sequence, kv head) into; one CTA streams one
- * partition.  With few (sequence, kv head) units, P is chosen so that the
- * partitions make about one wave of CTAs on this GPU; with many, P = 1024.  P is
- * never below min(max_context_len, 512) rounded up to 64, so short contexts stay
- * whole.  0 for empty or unsupported sizes.  num_sms <= 0 queries the current
- * device.  Pure host function.
+ * paged_decode_attention cuts each (sequence, kv head) into.  With few (sequence,
+ * kv head) units, one CTA streams one partition and P is chosen so that the
+ * partitions make about one wave of CTAs on this GPU.  With many units (at least
+ * a wave of CTAs), a persistent wave of CTAs streams the partitions as work items,
+ * longest first, and P = 1536 (1024 for batches over 1024 sequences, which take one
+ * CTA per partition).  P is never below min(max_context_len, 512) rounded up to 64,
+ * so short contexts stay whole.  0 for empty or unsupported sizes.  num_sms <= 0
+ * queries the current device.  Pure host function.
  */
 int32_t paged_decode_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                          int32_t head_dim, int32_t max_context_len, int32_t num_sms);
+
+/*
+ * paged_decode_path -- which kernel arrangement paged_decode_attention (and
+ * paged_decode_step) launches for these sizes on the current device:
+ *   PKV_PATH_PARTITIONS: one CTA per partition; a sequence cut into several
+ *     partitions is merged by the last of them to finish (through global memory);
+ *   PKV_PATH_CLUSTER: few units with 2..8 partitions each: the partitions of one
+ *     (sequence, kv head) form a thread-block cluster and merge through distributed
+ *     shared memory;
+ *   PKV_PATH_PERSISTENT: many units (at least a wave of CTAs): a persistent wave of
+ *     CTAs streams the partitions as work items, longest first.
+ * 0 for empty or unsupported sizes.  num_sms <= 0 queries the current device.  Pure
+ * host function.
+ */
+enum { PKV_PATH_PARTITIONS = 1, PKV_PATH_CLUSTER = 2, PKV_PATH_PERSISTENT = 3 };
+int32_t paged_decode_path(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                           int32_t head_dim, int32_t max_context_len, int32_t num_sms);
 
 /*

@@ -54,6 +54,8 @@ _lib.paged_kv_write_rope.argtypes = [_P, _P, _P, _i32, _P, _P, _i64, _P, _i64, _
 _lib.paged_kv_write_rope.restype = ctypes.c_int
 _lib.paged_decode_plan.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
 _lib.paged_decode_plan.restype = _i32
+_lib.paged_decode_path.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
+_lib.paged_decode_path.restype = _i32
 _lib.paged_decode_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32]
 _lib.paged_decode_workspace_size.restype = _sz
 _lib.paged_decode_split_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32]
@@ -177,6 +179,16 @@ def paged_kv_write_rope(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Te
                                     cos_sin.shape[0], r, 1 if neox_style else 0, _ptr(k_cache),
                                     _ptr(v_cache), ctypes.byref(d), _stream(stream)),
            "paged_kv_write_rope")
+
+
+PATH_PARTITIONS, PATH_CLUSTER, PATH_PERSISTENT = 1, 2, 3
+
+
+def paged_decode_path(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                      max_context_len: int, num_sms: int = 0) -> int:
+    """Kernel arrangement paged_decode_attention launches for these sizes (PATH_*; 0 if none)."""
+    return int(_lib.paged_decode_path(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                      max_context_len, num_sms))
 
 
 def paged_decode_plan(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,

@@ -137,6 +137,17 @@ __device__ __forceinline__ void warp_tile(WarpAcc<D> &acc, const uint32_t (&qb)[
   }
 }
 
+// Partitions one cluster merges (portable cluster size).
+constexpr int kMaxClusterParts = 8;
+// Where a CTA publishes its per-head results for the cluster merge: after the merge
+// area of its four warps, inside the (then free) stage ring.
+template <int D>
+constexpr uint32_t kPubOffset =
+    ((kConsumerWarps * kMaxGroup * D + 2 * kConsumerWarps * kMaxGroup) * 4 + 1023) & ~1023u;
+static_assert(kPubOffset<64> + (kMaxGroup * 64 + kMaxGroup) * 4 <= 4 * 2 * kChunk * 64 * 2 &&
+                  kPubOffset<128> + (kMaxGroup * 128 + kMaxGroup) * 4 <= 3 * 2 * kChunk * 128 * 2,
+              "the published results must fit in the stage ring");
+
 // Merge area of the four warps: red_o [warps][G][D], red_m / red_l [warps][8].
 struct MergeArea {
   float *o, *m, *l;
@@ -262,6 +273,62 @@ __device__ __forceinline__ void merge_rows(uint16_t *dst, const float *o_rows,
   }
 }
 
+// Cluster merge: every CTA of the cluster (one per partition of a (sequence, kv head))
+// published, in its own shared memory at `pub`, the normalised output [kMaxGroup][D]
+// and then the base-2 lse [kMaxGroup] of each head (-inf for a partition without
+// keys).  One warp merges head h over the n CTAs, reading them through distributed
+// shared memory; each lane owns D/32 dims.  All -inf (empty context): zeros.
+template <int D>
+__device__ __forceinline__ void cluster_merge_head(uint16_t *dst, uint32_t pub, int h, int n,
+                                                   int lane) {
+  constexpr int VPL = D / 32;
+  float lk[kMaxClusterParts], ov[kMaxClusterParts][VPL];
+  float M = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < kMaxClusterParts; ++u) {
+    lk[u] = -INFINITY;
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) ov[u][v] = 0.f;
+    if (u < n) {
+      const uint32_t peer = dev::mapa(pub, (uint32_t)u);
+      lk[u] = dev::ld_dsmem(peer + (uint32_t)(kMaxGroup * D + h) * 4u);
+      const uint32_t src = peer + (uint32_t)(h * D + lane * VPL) * 4u;
+      if constexpr (VPL == 2) {
+        const float2 t2 = dev::ld_dsmem_v2(src);
+        ov[u][0] = t2.x;
+        ov[u][1] = t2.y;
+      } else {
+        const float4 t4 = dev::ld_dsmem_v4(src);
+        ov[u][0] = t4.x;
+        ov[u][1] = t4.y;
+        ov[u][2] = t4.z;
+        ov[u][3] = t4.w;
+      }
+    }
+    M = fmaxf(M, lk[u]);
+  }
+  float den = 0.f, acc[VPL];
+#pragma unroll
+  for (int v = 0; v < VPL; ++v) acc[v] = 0.f;
+  if (M != -INFINITY) {
+#pragma unroll
+    for (int u = 0; u < kMaxClusterParts; ++u) {
+      const float wt = dev::ex2(lk[u] - M);  // 0 for an empty partition
+      den += wt;
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) acc[v] += wt * ov[u][v];
+    }
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  uint16_t *d = dst + lane * VPL;
+  if constexpr (VPL == 2) {
+    *reinterpret_cast<uint32_t *>(d) = dev::pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  } else {
+    *reinterpret_cast<uint2 *>(d) = make_uint2(dev::pack_bf16x2(acc[0] * inv, acc[1] * inv),
+                                              dev::pack_bf16x2(acc[2] * inv, acc[3] * inv));
+  }
+}
+
 // ===========================================================================
 // decode_kernel: one CTA per (sequence, kv head, partition of P tokens).
 // fused = 1 (paged_decode_attention): finished bf16 output, merging partitions itself.
@@ -274,12 +341,64 @@ struct DecodeArgs {
   float *o_part;               // [B][Hq][n_parts][D]
   float *lse_part;             // [B][Hq][n_parts]
   uint16_t *out;               // fused: [B][Hq][D] bf16
-  uint32_t *counters;          // fused: [B][Hkv] partitions finished; zero between calls
+  uint32_t *counters;          // fused == 1: [B][Hkv] partitions finished; zero between calls
   int64_t num_blocks;
   int32_t max_blocks, max_context_len, num_q_heads, num_kv_heads, group;
-  int32_t block_size, log2_bs, box_rows, partition_tokens, n_parts, fused;
+  int32_t block_size, log2_bs, box_rows, partition_tokens, n_parts;
+  int32_t fused;               // 0: partials only; 1: ticket merge; 2: cluster merge
   float scale_log2;            // scale * log2(e)
+  uint32_t *sched;             // persistent: [0] next dynamic item, [1] CTAs finished
+  int32_t num_seqs;            // persistent: sequences in the batch
 };
+
+// The end of one partition (any mode but the cluster merge), on the consumer warps
+// after warp_stash: a sequence held whole writes its bf16 output; otherwise the
+// partition writes its (normalised o, natural-log lse) row and, fused, takes a ticket
+// on the (sequence, kv head) counter -- the last partition to arrive merges them all
+// (nobody waits).  The barrier orders every thread's partial stores before thread 0's
+// ticket, an acquire-release atomic at GPU scope: its release publishes them (it is
+// cumulative over what the barrier ordered before it), and for the last partition its
+// acquire, passed on by the next barrier, makes the other partitions' rows visible.
+template <int D>
+__device__ __forceinline__ void finish_partition(const DecodeArgs &a, const MergeArea &r, int b,
+                                                 int g, int part, int nparts_b, int tid, int warp,
+                                                 int lane, volatile int *s_flag,
+                                                 volatile int *s_last) {
+  const int64_t head0 = (int64_t)b * a.num_q_heads + g * a.group;
+  if (a.fused && nparts_b == 1) {  // the whole sequence is here: finished output
+    for (int i = tid; i < a.group * D; i += kConsumers) {
+      const int h = i / D, d = i - h * D;
+      float M2, den;
+      a.out[head0 * D + i] = to_bf16(cta_merge<D>(r, a.group, h, d, &M2, &den));
+    }
+    return;
+  }
+  for (int i = tid; i < a.group * D; i += kConsumers) {
+    const int h = i / D, d = i - h * D;
+    float M2, den;
+    const float val = cta_merge<D>(r, a.group, h, d, &M2, &den);
+    const int64_t row = (head0 + h) * a.n_parts + part;
+    a.o_part[row * D + d] = val;
+    if (d == 0) a.lse_part[row] = (M2 + log2f(den)) * kLn2;
+  }
+  if (!a.fused) return;
+  consumer_bar();
+  if (tid == 0) {
+    int last = 0;
+    if (!*s_flag) {
+      const unsigned old = dev::atomic_add_acq_rel(a.counters + (int64_t)b * a.num_kv_heads + g, 1u);
+      last = (old + 1 == (unsigned)nparts_b);
+    }
+    *s_last = last;
+  }
+  consumer_bar();
+  if (*s_last) {
+    for (int h = warp; h < a.group; h += kConsumerWarps)
+      merge_rows<D>(a.out + (head0 + h) * D, a.o_part + (head0 + h) * a.n_parts * D,
+                    a.lse_part + (head0 + h) * a.n_parts, nparts_b, lane);
+    if (tid == 0) a.counters[(int64_t)b * a.num_kv_heads + g] = 0u;  // ready for the next call
+  }
+}
 
 template <int D, int STAGES>
 __global__ void __launch_bounds__(kThreads, 2)
@@ -329,15 +448,18 @@ __global__ void __launch_bounds__(kThreads, 2)
     L = L < 0 ? 0 : cap;
   }
   const int t_begin = part * a.partition_tokens;
-  if (t_begin >= L) {  // empty range: nothing written (the merge skips it)
+  const bool cluster = a.fused == 2;  // uniform over the grid
+  if (t_begin >= L && !cluster) {  // empty range: nothing written (the merge skips it)
     if (a.fused && part == 0) {  // empty context: zero output
       uint16_t *o = a.out + ((int64_t)b * a.num_q_heads + g * a.group) * D;
       for (int i = tid; i < a.group * D; i += kThreads) o[i] = 0;
     }
     return;
   }
+  // In a cluster every CTA takes part in the merge, so an empty range streams nothing
+  // and publishes lse = -inf.
   const int t_end = min(t_begin + a.partition_tokens, L);
-  const int n_chunks = (t_end - t_begin + kChunk - 1) / kChunk;
+  const int n_chunks = t_end > t_begin ? (t_end - t_begin + kChunk - 1) / kChunk : 0;
 
   if (tid == 0) {
 #pragma unroll
@@ -428,47 +550,42 @@ __global__ void __launch_bounds__(kThreads, 2)
     r.l = r.m + kConsumerWarps * kMaxGroup;
     warp_stash<D>(acc, r, a.group, warp, lane);
     consumer_bar();
-    const int64_t head0 = (int64_t)b * a.num_q_heads + g * a.group;
     const int nparts_b = (L + a.partition_tokens - 1) / a.partition_tokens;  // non-empty ones
-    if (a.fused && nparts_b == 1) {  // the whole sequence is here: finished output
-      for (int i = tid; i < a.group * D; i += kConsumers) {
-        const int h = i / D, d = i - h * D;
-        float M2, den;
-        a.out[head0 * D + i] = to_bf16(cta_merge<D>(r, a.group, h, d, &M2, &den));
-      }
-    } else {
+    if (cluster) {  // publish (normalised o, base-2 lse) per head for the cluster merge
+      float *pub_o = reinterpret_cast<float *>(base_ptr + kPubOffset<D>);
+      float *pub_l = pub_o + kMaxGroup * D;
       for (int i = tid; i < a.group * D; i += kConsumers) {
         const int h = i / D, d = i - h * D;
         float M2, den;
         const float val = cta_merge<D>(r, a.group, h, d, &M2, &den);
-        const int64_t row = (head0 + h) * a.n_parts + part;
-        a.o_part[row * D + d] = val;
-        if (d == 0) a.lse_part[row] = (M2 + log2f(den)) * kLn2;
+        const bool live = den > 0.f;  // false (or NaN) when this range had no keys
+        pub_o[h * D + d] = live ? val : 0.f;
+        if (d == 0) pub_l[h] = live ? M2 + log2f(den) : -INFINITY;
       }
-      if (a.fused) {
-        // ticket: the last partition of (b, g) to finish merges all of them.  The barrier
-        // orders every thread's partial stores before thread 0's fence, and the fence is
-        // cumulative, so one fence publishes them all before the ticket is taken.
-        consumer_bar();
-        if (tid == 0) {
-          int last = 0;
-          if (!*s_flag) {
-            __threadfence();
-            const unsigned old = atomicAdd(a.counters + (int64_t)b * a.num_kv_heads + g, 1u);
-            last = (old + 1 == (unsigned)nparts_b);
-            if (last) __threadfence();  // acquire side: the other partitions' stores
-          }
-          *s_last = last;
-        }
-        consumer_bar();
-        if (*s_last) {
-          for (int h = warp; h < a.group; h += kConsumerWarps)
-            merge_rows<D>(a.out + (head0 + h) * D, a.o_part + (head0 + h) * a.n_parts * D,
-                          a.lse_part + (head0 + h) * a.n_parts, nparts_b, lane);
-          if (tid == 0) a.counters[(int64_t)b * a.num_kv_heads + g] = 0u;  // ready for the next call
-        }
+    } else {
+      finish_partition<D>(a, r, b, g, part, nparts_b, tid, warp, lane, s_flag, s_last);
+    }
+  }
+
+  // ---- cluster merge.  Every thread of every CTA reaches both barriers exactly once:
+  // no path above returns in cluster mode and every wait above is bounded.  The first
+  // barrier publishes each CTA's results to the cluster; after it, CTA `rank` merges
+  // heads rank, rank + n, ... (one warp each); the second keeps every CTA's shared
+  // memory alive until its peers have read it.
+  if (cluster) {
+    dev::cluster_sync();
+    const int n = (int)dev::cluster_nctarank();
+    const int rank = (int)dev::cluster_ctarank();
+    if (warp < kConsumerWarps) {
+      if (n == a.n_parts && n <= kMaxClusterParts) {
+        const int64_t head0 = (int64_t)b * a.num_q_heads + g * a.group;
+        for (int h = rank + n * warp; h < a.group; h += n * kConsumerWarps)
+          cluster_merge_head<D>(a.out + (head0 + h) * D, base + kPubOffset<D>, h, n, lane);
+      } else if (tid == 0 && rank == 0) {
+        raise_error(PKV_DEVERR_TIMEOUT);  // launched with the wrong cluster shape
       }
     }
+    dev::cluster_sync();
   }
 
   // ---- a timed-out wait leaves copies possibly in flight: wait for them (bounded)
@@ -481,6 +598,376 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
+
+// ===========================================================================
+// decode_persistent_kernel: the fused decode for many (sequence, kv head) units.
+//
+// A grid of about one wave of CTAs (warp roles, TMA ring, per-stage work and epilogue
+// as in decode_kernel) takes work items -- one non-empty partition of P tokens of one
+// (sequence, kv head) -- and streams them back to back through its ring.  The producer
+// runs ahead across item boundaries: the next item's table window, query rows and
+// first boxes are in flight while the consumers finish the current item, so a CTA pays
+// its launch, set-up and first-copy latency once, not once per partition.
+//
+// Order: longest first.  All full partitions come first (by partition index,
+// descending), then every sequence's last partition by its number of 64-key chunks,
+// descending; within a category, by sequence, then kv head.  Each CTA derives the same
+// order from the context lengths (histograms in shared memory), takes item blockIdx.x
+// first and then items gridDim.x + (a global counter).  No CTA waits for another; the
+// last CTA to finish resets the counter for the next call.
+
+constexpr int kMaxPersistSeqs = 1024;  // sequences per batch (a warp scans 32 x 32 of them)
+constexpr int kMaxCategories = 64;     // full-partition levels + last-partition chunk counts
+
+// What the producer tells the consumers about the chunk in a stage.
+struct ItemDesc {
+  int32_t b, g;               // sequence, kv head
+  int32_t t_begin, t_end;     // the item's token range
+  int32_t key0;               // first key of this chunk
+  int32_t flags;              // kFirst | kLast | kStop
+  int32_t np;                 // partitions of the sequence
+  int32_t pad;
+};
+constexpr int32_t kFirst = 1, kLast = 2, kStop = 4;
+
+// Shared-memory layout after the 1024-byte aligned base.
+template <int D, int STAGES>
+struct PersistSmem {
+  static constexpr uint32_t kStageBytes = 2 * kChunk * D * 2;
+  static constexpr uint32_t kQSlot = kMaxGroup * D * 2;
+  static constexpr uint32_t q = STAGES * kStageBytes;
+  static constexpr uint32_t desc = q + STAGES * kQSlot;
+  static constexpr uint32_t bars = desc + STAGES * sizeof(ItemDesc);  // full[STAGES], empty[STAGES]
+  static constexpr uint32_t flags = bars + STAGES * 16;               // flag, last, issued
+  static constexpr uint32_t hist_nf = flags + 16;
+  static constexpr uint32_t hist_lc = hist_nf + kMaxCategories * 4;
+  static constexpr uint32_t off = hist_lc + kMaxCategories * 4;       // [kMaxCategories + 1]
+  static constexpr uint32_t lt = off + (kMaxCategories + 4) * 4;      // u16 [kMaxPersistSeqs]
+  static constexpr uint32_t nf = lt + kMaxPersistSeqs * 2;            // u8 [kMaxPersistSeqs]
+  static constexpr uint32_t total = nf + kMaxPersistSeqs;
+};
+static_assert(PersistSmem<64, 4>::lt % 16 == 0 && PersistSmem<128, 3>::lt % 16 == 0 &&
+                  PersistSmem<64, 4>::nf % 16 == 0 && PersistSmem<128, 3>::nf % 16 == 0,
+              "per-sequence arrays are read as 16-byte vectors");
+
+struct Item {
+  int b, g, t_begin, t_end, np;
+};
+
+// Item k of the order above (false when k >= the number of items).  All 32 lanes of the
+// producer warp take part; the result is the same on every lane.
+//   s_off: exclusive prefix of the categories' item counts, s_off[ncat] = total;
+//   category c < R-1: full partition r = R-2-c of sequences with nf > r;
+//   category c >= R-1: last partition of sequences with ceil(lt / 64) = q = Q-(c-(R-1)).
+__device__ __forceinline__ bool find_item(int k, const int *s_off, int ncat, int R, int P, int Hkv,
+                                          int num_seqs, const uint16_t *s_lt, const uint8_t *s_nf,
+                                          int lane, Item &it) {
+  if (k >= s_off[ncat]) return false;
+  // category: the last c with s_off[c] <= k (s_off is nondecreasing; that one is non-empty)
+  const unsigned m0 = __ballot_sync(0xffffffffu, lane < ncat && s_off[lane] <= k);
+  const unsigned m1 = __ballot_sync(0xffffffffu, lane + 32 < ncat && s_off[lane + 32] <= k);
+  const int cat = __popc(m0) + __popc(m1) - 1;
+  const int j = k - s_off[cat];
+  const int m = j / Hkv;
+  it.g = j - m * Hkv;
+  const bool full = cat < R - 1;
+  const int r = R - 2 - cat;                    // full: partition index
+  const int q = (P / kChunk) - (cat - (R - 1));  // last partition: its chunk count
+  // select the m-th sequence (ascending) of the category; lane w holds sequences [32w, 32w+32)
+  unsigned bits = 0;
+  if (32 * lane >= num_seqs) {
+    // no sequences in this lane's word (the arrays are written up to num_seqs rounded to 32)
+  } else if (full) {
+    const uint4 *v = reinterpret_cast<const uint4 *>(s_nf + 32 * lane);
+    const uint4 w0 = v[0], w1 = v[1];
+    const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+    for (int t = 0; t < 32; ++t) bits |= (int)((wd[t >> 2] >> (8 * (t & 3))) & 0xffu) > r ? 1u << t : 0u;
+  } else {
+    const uint4 *v = reinterpret_cast<const uint4 *>(s_lt + 32 * lane);
+    uint32_t wd[16];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint4 x = v[u];
+      wd[4 * u] = x.x;
+      wd[4 * u + 1] = x.y;
+      wd[4 * u + 2] = x.z;
+      wd[4 * u + 3] = x.w;
+    }
+#pragma unroll
+    for (int t = 0; t < 32; ++t) {
+      const int lt = (int)((wd[t >> 1] >> (16 * (t & 1))) & 0xffffu);
+      bits |= (lt > 0 && (lt + kChunk - 1) / kChunk == q) ? 1u << t : 0u;
+    }
+  }
+  const int pc = __popc(bits);
+  int incl = pc;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const unsigned sel = __ballot_sync(0xffffffffu, incl > m);
+  if (sel == 0u) {  // cannot happen (the counts come from the same arrays): stop cleanly
+    if (lane == 0) raise_error(PKV_DEVERR_CONTEXT_LEN);
+    return false;
+  }
+  const int w = __ffs(sel) - 1;
+  const int before = __shfl_sync(0xffffffffu, incl - pc, w);
+  unsigned wb = __shfl_sync(0xffffffffu, bits, w);
+  for (int i = 0; i < m - before; ++i) wb &= wb - 1;
+  it.b = 32 * w + __ffs(wb) - 1;
+  const int nf = s_nf[it.b], lt = s_lt[it.b];
+  it.np = nf + (lt > 0 ? 1 : 0);
+  if (full) {
+    it.t_begin = r * P;
+    it.t_end = it.t_begin + P;
+  } else {
+    it.t_begin = nf * P;
+    it.t_end = it.t_begin + lt;
+  }
+  return true;
+}
+
+template <int D, int STAGES>
+__global__ void __launch_bounds__(kThreads, 2)
+    decode_persistent_kernel(const __grid_constant__ CUtensorMap tmk,
+                             const __grid_constant__ CUtensorMap tmv, const DecodeArgs a) {
+  using SL = PersistSmem<D, STAGES>;
+  constexpr int kTileBytes = kChunk * D * 2;
+  constexpr int KS = D / 16;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = dev::smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t *const base_ptr = smem_raw + (base - raw);
+  const uint32_t bar_full = base + SL::bars;
+  const uint32_t bar_empty = bar_full + STAGES * 8;
+  volatile int *const s_flag = reinterpret_cast<volatile int *>(base_ptr + SL::flags);
+  volatile int *const s_last = s_flag + 1;
+  volatile int *const s_issued = s_flag + 2;
+  ItemDesc *const s_desc = reinterpret_cast<ItemDesc *>(base_ptr + SL::desc);
+  int *const s_hist_nf = reinterpret_cast<int *>(base_ptr + SL::hist_nf);
+  int *const s_hist_lc = reinterpret_cast<int *>(base_ptr + SL::hist_lc);
+  int *const s_off = reinterpret_cast<int *>(base_ptr + SL::off);
+  uint16_t *const s_lt = reinterpret_cast<uint16_t *>(base_ptr + SL::lt);
+  uint8_t *const s_nf = base_ptr + SL::nf;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int P = a.partition_tokens, R = a.n_parts, Q = P / kChunk;
+  const int ncat = R - 1 + Q;
+  const int Hkv = a.num_kv_heads;
+  const int cap = (int)min((int64_t)a.max_blocks * a.block_size, (int64_t)a.max_context_len);
+  const int bpad = (a.num_seqs + 31) & ~31;
+
+  // ---- set-up: barriers, and the order's histograms from the context lengths
+  if (tid == 0) {
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) {
+      dev::mbar_init(bar_full + 8 * s, 1);
+      dev::mbar_init(bar_empty + 8 * s, kConsumerWarps);
+    }
+    *s_flag = 0;
+    *s_issued = 0;
+    dev::fence_mbar_init();
+  }
+  for (int i = tid; i < 2 * kMaxCategories; i += kThreads) s_hist_nf[i] = 0;  // both histograms
+  __syncthreads();
+  for (int bb = tid; bb < bpad; bb += kThreads) {
+    int nf = 0, lt = 0;
+    if (bb < a.num_seqs) {
+      int L = __ldg(a.context_lens + bb);
+      if (L < 0 || L > cap) {
+        if (blockIdx.x == 0) raise_error(PKV_DEVERR_CONTEXT_LEN);
+        L = L < 0 ? 0 : cap;
+      }
+      if (L > 0) {
+        nf = (L - 1) / P;
+        lt = L - nf * P;
+        if (nf > 0) atomicAdd(s_hist_nf + nf, 1);
+        atomicAdd(s_hist_lc + (lt + kChunk - 1) / kChunk, 1);
+      } else if (bb % (int)gridDim.x == (int)blockIdx.x) {  // empty context: zero output
+        uint2 *o = reinterpret_cast<uint2 *>(a.out + (int64_t)bb * a.num_q_heads * D);
+        for (int i = 0; i < a.num_q_heads * D / 4; ++i) o[i] = make_uint2(0u, 0u);
+      }
+    }
+    s_nf[bb] = (uint8_t)nf;
+    s_lt[bb] = (uint16_t)lt;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int off = 0, suffix = 0, c = 0;
+    for (int r = R - 2; r >= 0; --r, ++c) {  // full partitions r: sequences with nf > r
+      suffix += s_hist_nf[r + 1];
+      s_off[c] = off;
+      off += suffix * Hkv;
+    }
+    for (int q = Q; q >= 1; --q, ++c) {  // last partitions of q chunks
+      s_off[c] = off;
+      off += s_hist_lc[q] * Hkv;
+    }
+    s_off[ncat] = off;
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------- producer warp
+    const uint64_t policy = dev::policy_evict_first();
+    const int rb = a.box_rows;
+    const uint32_t box_bytes = (uint32_t)rb * 128u;
+    const uint32_t q_bytes = (uint32_t)a.group * D * 2u;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // see decode_kernel
+    int c = 0;  // chunks issued, over all items
+    bool ok = true;
+    Item it;
+    int k_next = 0;
+    bool have = find_item((int)blockIdx.x, s_off, ncat, R, P, Hkv, a.num_seqs, s_lt, s_nf, lane, it);
+    if (have && lane == 0) k_next = (int)gridDim.x + (int)atomicAdd(a.sched, 1u);
+    while (have) {
+      const int32_t *trow = a.block_tables + (int64_t)it.b * a.max_blocks;
+      const int lb_last = (it.t_end - 1) >> a.log2_bs;
+      int win = it.t_begin >> a.log2_bs;
+      int tb = (win + lane <= lb_last) ? __ldg(trow + win + lane) : 0;
+      const int n_chunks = (it.t_end - it.t_begin + kChunk - 1) / kChunk;
+      for (int i = 0; i < n_chunks; ++i, ++c) {
+        const int s = c % STAGES;
+        if (c >= STAGES &&
+            !__all_sync(0xffffffffu, dev::mbar_wait(bar_empty + 8 * s, ((c / STAGES) - 1) & 1))) {
+          if (lane == 0) {
+            raise_error(PKV_DEVERR_TIMEOUT);
+            *s_flag = 1;
+          }
+          ok = false;
+          break;
+        }
+        const int k0 = it.t_begin + i * kChunk;
+        const int nk = min(kChunk, it.t_end - k0);
+        const int nbox = (nk + rb - 1) / rb;
+        const int lb_hi = (k0 + (nbox - 1) * rb) >> a.log2_bs;
+        if (lb_hi >= win + 32) {  // slide the table window
+          win = k0 >> a.log2_bs;
+          tb = (win + lane <= lb_last) ? __ldg(trow + win + lane) : 0;
+        }
+        const int key = k0 + lane * rb;
+        const int src = min(max((key >> a.log2_bs) - win, 0), 31);
+        const int64_t phys_raw = __shfl_sync(0xffffffffu, tb, src);
+        if (lane == 0) {
+          ItemDesc dsc;
+          dsc.b = it.b;
+          dsc.g = it.g;
+          dsc.t_begin = it.t_begin;
+          dsc.t_end = it.t_end;
+          dsc.key0 = k0;
+          dsc.flags = (i == 0 ? kFirst : 0) | (i == n_chunks - 1 ? kLast : 0);
+          dsc.np = it.np;
+          dsc.pad = 0;
+          s_desc[s] = dsc;
+          dev::mbar_arrive_expect_tx(bar_full + 8 * s,
+                                     2u * nbox * box_bytes * (D / 64) + (i == 0 ? q_bytes : 0u));
+          if (i == 0)  // the group's query rows, contiguous in q
+            dev::bulk_load(base + SL::q + s * SL::kQSlot,
+                           a.q + ((int64_t)it.b * a.num_q_heads + it.g * a.group) * D, q_bytes,
+                           bar_full + 8 * s);
+        }
+        __syncwarp();
+        if (lane < nbox) {
+          int64_t phys = phys_raw;
+          if (phys < 0 || phys >= a.num_blocks) {
+            raise_error(PKV_DEVERR_BLOCK_ID);
+            phys = 0;
+          }
+          const int off = key & (a.block_size - 1);
+          const int32_t row = (int32_t)((phys * a.num_kv_heads + it.g) * a.block_size + off);
+          const uint32_t dk = base + s * SL::kStageBytes + lane * box_bytes;
+          issue_box<D>(dk, dk + kTileBytes, &tmk, &tmv, row, bar_full + 8 * s, policy);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      const int k = __shfl_sync(0xffffffffu, k_next, 0);
+      have = find_item(k, s_off, ncat, R, P, Hkv, a.num_seqs, s_lt, s_nf, lane, it);
+      if (have && lane == 0) k_next = (int)gridDim.x + (int)atomicAdd(a.sched, 1u);
+    }
+    if (ok) {  // no item follows: a stop marker in the next stage
+      const int s = c % STAGES;
+      if (c >= STAGES &&
+          !__all_sync(0xffffffffu, dev::mbar_wait(bar_empty + 8 * s, ((c / STAGES) - 1) & 1))) {
+        if (lane == 0) {
+          raise_error(PKV_DEVERR_TIMEOUT);
+          *s_flag = 1;
+        }
+      } else if (lane == 0) {
+        s_desc[s].flags = kStop;
+        dev::mbar_arrive(bar_full + 8 * s);
+      }
+    }
+    if (lane == 0) *s_issued = c;
+  } else {
+    // ----------------------------------------------------------- consumer warps
+    WarpAcc<D> acc;
+    acc_reset(acc);
+    uint32_t qb[KS][2];
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) qb[ks][0] = qb[ks][1] = 0u;
+    const int gid = lane >> 2, tig = lane & 3;
+    for (int c = 0;; ++c) {
+      const int s = c % STAGES;
+      if (!__all_sync(0xffffffffu, dev::mbar_wait(bar_full + 8 * s, (c / STAGES) & 1))) {
+        if (lane == 0) {
+          raise_error(PKV_DEVERR_TIMEOUT);
+          *s_flag = 1;
+        }
+        break;
+      }
+      const ItemDesc d = s_desc[s];
+      if (d.flags & kStop) break;
+      if (d.flags & kFirst) {  // a new item: its query rows and a fresh softmax state
+        const uint32_t *qs = reinterpret_cast<const uint32_t *>(base_ptr + SL::q + s * SL::kQSlot);
+        const bool hv = gid < a.group;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          qb[ks][0] = hv ? qs[gid * (D / 2) + 8 * ks + tig] : 0u;
+          qb[ks][1] = hv ? qs[gid * (D / 2) + 8 * ks + 4 + tig] : 0u;
+        }
+        acc_reset(acc);
+      }
+      const int key0 = d.key0 + 16 * warp;
+      const int nvalid = min(16, d.t_end - key0);
+      const uint32_t kb = base + s * SL::kStageBytes;
+      if (nvalid > 0) warp_tile<D>(acc, qb, kb, kb + kTileBytes, warp, lane, nvalid, a.scale_log2);
+      if (d.flags & kLast) {
+        consumer_bar();  // every warp is done with this stage's tiles: reuse it to merge
+        MergeArea r;
+        r.o = reinterpret_cast<float *>(base_ptr + s * SL::kStageBytes);
+        r.m = r.o + kConsumerWarps * a.group * D;
+        r.l = r.m + kConsumerWarps * kMaxGroup;
+        warp_stash<D>(acc, r, a.group, warp, lane);
+        consumer_bar();
+        finish_partition<D>(a, r, d.b, d.g, d.t_begin / P, d.np, tid, warp, lane, s_flag, s_last);
+      }
+      __syncwarp();
+      if (lane == 0) dev::mbar_arrive(bar_empty + 8 * s);
+    }
+  }
+
+  // ---- a timed-out wait leaves copies possibly in flight: wait for them (bounded)
+  __syncthreads();
+  if (tid == 0 && *s_flag) {
+    const int issued = *s_issued;
+    for (int s = 0; s < STAGES; ++s) {
+      const int c_last = s + ((issued - 1 - s) / STAGES) * STAGES;  // last chunk on stage s
+      if (c_last >= 0 && c_last < issued) (void)dev::mbar_wait(bar_full + 8 * s, (c_last / STAGES) & 1);
+    }
+  }
+  // ---- the last CTA to finish resets the item counter for the next call
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(a.sched + 1, 1u) == gridDim.x - 1) {
+      a.sched[0] = 0u;
+      a.sched[1] = 0u;
+    }
+  }
+}
 
 // ---------------------------------------------------------------------------
 // Log-sum-exp merge of fixed partitions: one CTA per (sequence, query head).  Thread
@@ -556,19 +1043,22 @@ cudaError_t read_decode_errors(uint32_t *flags, int clear) { return read_tu_erro
 
 namespace {
 
-bool g_split_attr[kMaxDevices][2];  // dynamic smem attribute of decode_kernel set
+bool g_split_attr[kMaxDevices][2];    // dynamic smem attribute of decode_kernel set
+bool g_persist_attr[kMaxDevices][2];  // ... of decode_persistent_kernel
 
 // Partition size for paged_decode_attention.  Few (sequence, kv head) units: cut each
 // into as many partitions as make about one wave of CTAs, so every CTA streams a long
-// range; many units: 1024-token partitions (short contexts stay whole).  Never below
-// min(context, 512) tokens, so short contexts are not cut into tiny pieces.
+// range.  Many units: 1536-token work items of the persistent kernel (batches of at
+// most kMaxPersistSeqs sequences), 1024-token CTAs of decode_kernel beyond that.
+// Never below min(context, 512) tokens, so short contexts are not cut into tiny pieces.
 int32_t plan_partition(int32_t num_seqs, int32_t hkv, int32_t d, int32_t max_len, int sms) {
   const int64_t units = (int64_t)num_seqs * hkv;
   const int64_t slots = (int64_t)sms * split_occupancy(d);
   const int64_t lr = ((int64_t)max_len + kChunk - 1) / kChunk * kChunk;
   int64_t P;
   if (units >= slots) {
-    P = lr < 1024 ? lr : 1024;
+    const int64_t pm = num_seqs <= kMaxPersistSeqs ? 1536 : 1024;
+    P = lr < pm ? lr : pm;
   } else {
     const int64_t parts = slots / units;
     P = ((max_len + parts - 1) / parts + kChunk - 1) / kChunk * kChunk;
@@ -578,12 +1068,25 @@ int32_t plan_partition(int32_t num_seqs, int32_t hkv, int32_t d, int32_t max_len
   if (P < kChunk) P = kChunk;
   return (int32_t)P;
 }
+// Cluster size of the fused decode: when every partition of the grid is resident at
+// once (few (sequence, kv head) units) and a unit has 2..8 partitions, the partitions
+// of a unit form one cluster and merge through distributed shared memory; otherwise 0
+// (the last partition to finish merges through global memory).
+int cluster_parts(int32_t num_seqs, int32_t hkv, int32_t d, int32_t max_len, int32_t P, int sms) {
+  const int64_t units = (int64_t)num_seqs * hkv;
+  const int64_t n_parts = ((int64_t)max_len + P - 1) / P;
+  const int64_t slots = (int64_t)sms * split_occupancy(d);
+  if (n_parts < 2 || n_parts > kMaxClusterParts || units * n_parts > slots) return 0;
+  return (int)n_parts;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Workspace of paged_decode_attention: merge counters [B*Hkv] u32, then
-// paged_decode_split's partials for the planned partition size.
+// Workspace of paged_decode_attention: merge counters [B*Hkv] u32 and the persistent
+// kernel's two scheduling words, then paged_decode_split's partials for the planned
+// partition size.
 struct FusedLayout {
-  size_t counters, o_part, lse_part, total;
+  size_t counters, sched, o_part, lse_part, total;
 };
 
 FusedLayout fused_layout(int32_t num_seqs, int32_t hq, int32_t hkv, int32_t d, int32_t mlen,
@@ -591,7 +1094,8 @@ FusedLayout fused_layout(int32_t num_seqs, int32_t hq, int32_t hkv, int32_t d, i
   FusedLayout f;
   const size_t rows = (size_t)num_seqs * hq * (size_t)((mlen + P - 1) / P);
   f.counters = 0;
-  f.o_part = align256((size_t)num_seqs * hkv * 4);
+  f.sched = (size_t)num_seqs * hkv * 4;
+  f.o_part = align256(f.sched + 8);
   f.lse_part = f.o_part + align256(rows * d * sizeof(float));
   f.total = f.lse_part + align256(rows * sizeof(float));
   return f;
@@ -601,7 +1105,7 @@ int launch_split(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_c
                  const int32_t *bt, int32_t max_blocks, const int32_t *lens, int32_t max_len,
                  int32_t num_seqs, int32_t hq, const pkv_cache_desc &c, float scale, int32_t P,
                  float *o_part, float *lse_part, pkv_bf16 *out, uint32_t *counters,
-                 cudaStream_t stream, bool programmatic = false) {
+                 cudaStream_t stream, bool programmatic = false, int cluster = 0) {
   CUtensorMap tmk, tmv;
   {
     std::lock_guard<std::mutex> lk(attn_mutex());
@@ -629,7 +1133,7 @@ int launch_split(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_c
   a.lse_part = lse_part;
   a.out = out;
   a.counters = counters;
-  a.fused = out != nullptr;
+  a.fused = out == nullptr ? 0 : (cluster > 1 ? 2 : 1);
   a.num_blocks = c.num_blocks;
   a.max_blocks = max_blocks;
   a.max_context_len = max_len;
@@ -642,26 +1146,138 @@ int launch_split(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_c
   a.partition_tokens = P;
   a.n_parts = (max_len + P - 1) / P;
   a.scale_log2 = scale * kLog2e;
+  a.sched = nullptr;
+  a.num_seqs = num_seqs;
   dim3 grid((unsigned)a.n_parts, (unsigned)c.num_kv_heads, (unsigned)num_seqs);
   cudaError_t e;
-  if (!programmatic) {
+  if (!programmatic && cluster <= 1) {
     decode_kernel<D, split_stages(D)><<<grid, kThreads, split_smem(D), stream>>>(tmk, tmv, a);
     e = cudaGetLastError();
-  } else {  // may start while the previous kernel on the stream (the slot write) still runs
+  } else {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = split_smem(D);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (programmatic) {  // may start while the previous kernel (the slot write) still runs
+      attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[n].val.programmaticStreamSerializationAllowed = 1;
+      ++n;
+    }
+    if (cluster > 1) {  // the partitions of one (sequence, kv head) form a cluster
+      attr[n].id = cudaLaunchAttributeClusterDimension;
+      attr[n].val.clusterDim.x = (unsigned)cluster;
+      attr[n].val.clusterDim.y = 1;
+      attr[n].val.clusterDim.z = 1;
+      ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = n;
     e = cudaLaunchKernelEx(&cfg, decode_kernel<D, split_stages(D)>, tmk, tmv, a);
   }
   if (e != cudaSuccess) return cuda_error(e, "decode_kernel launch");
   return PKV_OK;
+}
+
+constexpr int persist_stages(int d) { return d == 64 ? 4 : 3; }
+constexpr size_t persist_smem(int d) {
+  return 1024 + (d == 64 ? PersistSmem<64, persist_stages(64)>::total
+                         : PersistSmem<128, persist_stages(128)>::total);
+}
+static_assert(persist_smem(64) * 3 + 3 * 1024 <= 228 * 1024 &&
+                  persist_smem(128) * 2 + 2 * 1024 <= 228 * 1024,
+              "the persistent kernel keeps decode_kernel's CTAs per SM");
+
+// Whether the persistent kernel takes the fused decode: many (sequence, kv head) units
+// (at least a wave of CTAs), a batch its per-CTA order tables hold, and a category
+// count (full-partition levels + last-partition chunk counts) within kMaxCategories.
+bool use_persistent(int32_t num_seqs, int32_t hkv, int32_t d, int32_t max_len, int32_t P,
+                    int sms) {
+  const int64_t units = (int64_t)num_seqs * hkv;
+  const int64_t R = ((int64_t)max_len + P - 1) / P;
+  const int64_t Q = P / kChunk;
+  return units >= (int64_t)sms * split_occupancy(d) && num_seqs <= kMaxPersistSeqs &&
+         P % kChunk == 0 && Q < kMaxCategories && R - 1 + Q <= kMaxCategories;
+}
+
+template <int D>
+int launch_persistent(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                      const int32_t *bt, int32_t max_blocks, const int32_t *lens, int32_t max_len,
+                      int32_t num_seqs, int32_t hq, const pkv_cache_desc &c, float scale,
+                      int32_t P, float *o_part, float *lse_part, pkv_bf16 *out,
+                      uint32_t *counters, uint32_t *sched, cudaStream_t stream,
+                      bool programmatic) {
+  constexpr int S = persist_stages(D);
+  CUtensorMap tmk, tmv;
+  int sms = 0;
+  {
+    std::lock_guard<std::mutex> lk(attn_mutex());
+    int rc = maps_for(k_cache, v_cache, c, &tmk, &tmv);
+    if (rc) return rc;
+    int dev = 0;
+    if ((rc = current_device(&dev))) return rc;
+    if ((rc = device_sms(&sms))) return rc;
+    const int vi = D == 64 ? 0 : 1;
+    if (!g_persist_attr[dev][vi]) {
+      cudaError_t e = cudaFuncSetAttribute(decode_persistent_kernel<D, S>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)persist_smem(D));
+      if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute");
+      e = cudaFuncSetAttribute(decode_persistent_kernel<D, S>,
+                               cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+      if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(carveout)");
+      g_persist_attr[dev][vi] = true;
+    }
+  }
+  DecodeArgs a;
+  a.q = q;
+  a.block_tables = bt;
+  a.context_lens = lens;
+  a.o_part = o_part;
+  a.lse_part = lse_part;
+  a.out = out;
+  a.counters = counters;
+  a.fused = 1;
+  a.num_blocks = c.num_blocks;
+  a.max_blocks = max_blocks;
+  a.max_context_len = max_len;
+  a.num_q_heads = hq;
+  a.num_kv_heads = c.num_kv_heads;
+  a.group = hq / c.num_kv_heads;
+  a.block_size = c.block_size;
+  a.log2_bs = ilog2(c.block_size);
+  a.box_rows = c.block_size < kChunk ? c.block_size : kChunk;
+  a.partition_tokens = P;
+  a.n_parts = (max_len + P - 1) / P;
+  a.scale_log2 = scale * kLog2e;
+  a.sched = sched;
+  a.num_seqs = num_seqs;
+  // one wave: every CTA starts at once, none waits for another
+  const int64_t items_max = (int64_t)num_seqs * c.num_kv_heads * a.n_parts;
+  const int64_t slots = (int64_t)sms * split_occupancy(D);
+  const unsigned grid = (unsigned)(items_max < slots ? items_max : slots);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = persist_smem(D);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = programmatic ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_persistent_kernel<D, S>, tmk, tmv, a);
+  if (e != cudaSuccess) return cuda_error(e, "decode_persistent_kernel launch");
+  return PKV_OK;
+}
+
+// The fused decode's kernel arrangement for these sizes on `sms` SMs (PKV_PATH_*).
+int decode_path(int32_t num_seqs, int32_t hkv, int32_t d, int32_t max_len, int32_t P, int sms) {
+  if (use_persistent(num_seqs, hkv, d, max_len, P, sms)) return PKV_PATH_PERSISTENT;
+  if (cluster_parts(num_seqs, hkv, d, max_len, P, sms) > 1) return PKV_PATH_CLUSTER;
+  return PKV_PATH_PARTITIONS;
 }
 
 int launch_combine(pkv_bf16 *out, const float *o_part, const float *lse_part, const int32_t *lens,
@@ -698,6 +1314,15 @@ PKV_API int32_t paged_decode_plan(int32_t num_seqs, int32_t num_q_heads, int32_t
       max_context_len <= 0)
     return 0;
   return plan_partition(num_seqs, num_kv_heads, head_dim, max_context_len, sms_or_default(num_sms));
+}
+
+PKV_API int32_t paged_decode_path(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t max_context_len, int32_t num_sms) {
+  const int32_t mlen = max_context_len > 0 ? max_context_len : 1;
+  const int sms = sms_or_default(num_sms);
+  const int32_t P = paged_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, mlen, sms);
+  if (P <= 0) return 0;
+  return decode_path(num_seqs, num_kv_heads, head_dim, mlen, P, sms);
 }
 
 PKV_API size_t paged_decode_split_workspace_size(int32_t num_seqs, int32_t num_q_heads,
@@ -807,12 +1432,25 @@ int decode_fused(pkv_bf16 *out, const pkv_bf16 *q, const pkv_bf16 *k_cache,
   uint32_t *counters = reinterpret_cast<uint32_t *>(ws + f.counters);
   float *o_part = reinterpret_cast<float *>(ws + f.o_part);
   float *lse_part = reinterpret_cast<float *>(ws + f.lse_part);
+  const int path = decode_path(num_seqs, cache->num_kv_heads, D, mlen, P, sms_or_default(0));
+  if (path == PKV_PATH_PERSISTENT) {
+    uint32_t *sched = reinterpret_cast<uint32_t *>(ws + f.sched);
+    return D == 64 ? launch_persistent<64>(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                           context_lens, mlen, num_seqs, num_q_heads, *cache,
+                                           scale, P, o_part, lse_part, out, counters, sched, s,
+                                           programmatic)
+                   : launch_persistent<128>(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                            context_lens, mlen, num_seqs, num_q_heads, *cache,
+                                            scale, P, o_part, lse_part, out, counters, sched, s,
+                                            programmatic);
+  }
+  const int cluster = path == PKV_PATH_CLUSTER ? (mlen + P - 1) / P : 0;
   return D == 64 ? launch_split<64>(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                     context_lens, mlen, num_seqs, num_q_heads, *cache, scale, P,
-                                    o_part, lse_part, out, counters, s, programmatic)
+                                    o_part, lse_part, out, counters, s, programmatic, cluster)
                  : launch_split<128>(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                      context_lens, mlen, num_seqs, num_q_heads, *cache, scale, P,
-                                     o_part, lse_part, out, counters, s, programmatic);
+                                     o_part, lse_part, out, counters, s, programmatic, cluster);
 }
 
 }  // namespace

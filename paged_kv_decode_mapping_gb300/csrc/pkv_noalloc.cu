@@ -77,11 +77,12 @@ PKV_API int paged_decode_attention_noalloc(pkv_bf16 *out, const pkv_bf16 *q,
   void *scratch = nullptr;
   int rc = scratch_address(&scratch);
   if (rc) return rc;
-  // The decode keeps one completion counter per (sequence, kv head) at the start of
-  // its workspace; they must be zero when the kernel starts.  A completed call leaves
-  // them zero, but clear them anyway so a call never depends on the previous one.
+  // The decode keeps one completion counter per (sequence, kv head), then two work
+  // scheduling words, at the start of its workspace; they must be zero when the kernel
+  // starts.  A completed call leaves them zero, but clear them anyway so a call never
+  // depends on the previous one.
   if (num_seqs > 0) {
-    const cudaError_t e = cudaMemsetAsync(scratch, 0, (size_t)num_seqs * cache->num_kv_heads * 4,
+    const cudaError_t e = cudaMemsetAsync(scratch, 0, (size_t)num_seqs * cache->num_kv_heads * 4 + 8,
                                           static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_error(e, "paged_decode_attention_noalloc: clear counters");
   }

@@ -161,6 +161,90 @@ def test_small_cases(B, oracle, D, BS, Hq, Hkv):
     assert_no_device_errors(B)
 
 
+# Few (sequence, kv head) units: the plan gives P = 512 here, so a unit has
+# ceil(max_len / 512) partitions.  2..8 of them form one thread-block cluster that merges
+# through distributed shared memory; 9 or more merge through global memory.
+CLUSTER_CASES = [
+    # D, BS, Hq, Hkv, lens, partitions
+    (64, 16, 8, 1, (4096,), 8),                      # the largest cluster
+    (64, 16, 8, 1, (4097,), 9),                      # one more: global-memory merge
+    (128, 32, 8, 1, (1025, 0, 1, 512, 513), 3),      # empty contexts and empty partitions
+    (64, 16, 32, 4, (2048, 1500, 3), 4),             # G = 8: two heads per CTA
+    (64, 16, 8, 1, (1000, 20), 2),                   # G = 8: four heads per CTA
+    (128, 16, 6, 2, (900, 1800), 4),                 # G = 3, head_dim 128
+    (64, 8, 2, 2, (600,), 2),                        # G = 1, two partitions
+]
+
+
+@pytest.mark.parametrize("D,BS,Hq,Hkv,lens,parts", CLUSTER_CASES)
+def test_cluster_merge_shapes(B, oracle, D, BS, Hq, Hkv, lens, parts):
+    w = W.small_workload(B=len(lens), Hq=Hq, Hkv=Hkv, D=D, BS=BS, lens=lens, seed=31 + D + Hq)
+    inp = W.make_inputs(w, poison=True)
+    P = B.paged_decode_plan(w.B, Hq, Hkv, D, inp["max_context_len"])
+    assert math.ceil(inp["max_context_len"] / P) == parts
+    assert B.paged_decode_path(w.B, Hq, Hkv, D, inp["max_context_len"]) == (
+        B.PATH_CLUSTER if parts <= 8 else B.PATH_PARTITIONS)
+    g = dev(inp)
+    out = step(B, g)
+    ref, kc_ref, _ = oracle.step(inp)
+    assert torch.equal(g["k_cache"].cpu().view(torch.int16), kc_ref.view(torch.int16))
+    check_attention(out, ref, f"{parts} partitions D={D} G={Hq // Hkv}")
+    o = out.cpu()
+    for b, L in enumerate(lens):
+        if L == 0:
+            assert torch.equal(o[b], torch.zeros_like(o[b]))
+    assert_no_device_errors(B)
+
+
+def _lens(n, lo, hi, seed, extra=()):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randint(lo, hi + 1, (n,), generator=g).tolist()
+    for i, v in enumerate(extra):
+        x[(7 * i + 3) % n] = v
+    return tuple(int(v) for v in x)
+
+
+# Many (sequence, kv head) units -- at least one wave of CTAs -- take the persistent
+# kernel (at most 1024 sequences); the batch over 1024 takes the grid kernel.
+PERSIST_CASES = [
+    # D, BS, Hq, Hkv, lens
+    (64, 16, 16, 4, _lens(120, 0, 3000, 1, (0, 1, 63, 64, 1024, 1025, 2048, 3000, 0))),
+    (128, 32, 24, 8, _lens(40, 0, 5000, 2, (0, 4096, 1, 2049))),
+    (64, 8, 8, 1, _lens(460, 1, 700, 3, (512, 513))),
+    (64, 256, 4, 4, _lens(116, 1, 2100, 4, (1024, 2048, 1))),
+    (64, 16, 2, 1, _lens(1100, 1, 300, 5)),
+    (64, 16, 8, 1, tuple(3000 if b == 17 else 0 for b in range(500))),
+]
+
+
+@pytest.mark.parametrize("D,BS,Hq,Hkv,lens", PERSIST_CASES)
+def test_many_units_decode(B, oracle, D, BS, Hq, Hkv, lens):
+    w = W.small_workload(B=len(lens), Hq=Hq, Hkv=Hkv, D=D, BS=BS, lens=lens, seed=41 + D + Hq,
+                         write="none")
+    inp = W.make_inputs(w, poison=True)
+    path = B.paged_decode_path(w.B, Hq, Hkv, D, inp["max_context_len"])
+    assert path == (B.PATH_PERSISTENT if w.B <= 1024 else B.PATH_PARTITIONS)
+    g = dev(inp)
+    ref = oracle.decode(inp["q"], inp["k_cache"], inp["v_cache"], inp["block_tables"],
+                        inp["context_lens"], inp["scale"])
+    nbytes = B.paged_decode_workspace_size(w.B, Hq, Hkv, D, inp["max_context_len"])
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    for call in range(3):  # the item counter and merge counters are reset by each call
+        out = torch.full_like(g["q"], float("nan"))
+        B.paged_decode_attention(out, g["q"], g["k_cache"], g["v_cache"], g["block_tables"],
+                                 g["context_lens"], inp["max_context_len"], inp["scale"],
+                                 workspace=ws)
+        check_attention(out, ref, f"call {call} D={D} BS={BS} G={Hq // Hkv} B={w.B}")
+        torch.cuda.synchronize()
+        head = ws[:w.B * Hkv * 4 + 8].view(torch.int32)
+        assert int(head.abs().sum()) == 0, "counters not back at zero"
+    o = out.cpu()
+    for b, L in enumerate(lens):
+        if L == 0:
+            assert torch.equal(o[b], torch.zeros_like(o[b]))
+    assert_no_device_errors(B)
+
+
 def test_large_ragged_batch(B, oracle):
     """Many (sequence, kv head) units with ragged contexts up to 512."""
     lens = tuple(int(x) for x in torch.randint(1, 513, (160,), generator=torch.Generator().manual_seed(4)))

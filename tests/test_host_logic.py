@@ -26,8 +26,9 @@ def test_plan_picks_partitions_from_context_length(B):
     assert B.paged_decode_plan(1, 32, 8, 64, 128, sms) == 128          # short: one partition
     assert B.paged_decode_plan(16, 32, 8, 64, 2048, sms) == 704        # 128 units x 3 = 384 CTAs
     assert B.paged_decode_plan(4, 24, 8, 128, 32768, sms) == 3648      # 32 units x 9 = 288 CTAs
-    assert B.paged_decode_plan(64, 24, 8, 128, 4096, sms) == 1024      # 512 units >= 304 slots
-    assert B.paged_decode_plan(256, 32, 4, 64, 8192, sms) == 1024
+    assert B.paged_decode_plan(64, 24, 8, 128, 4096, sms) == 1536      # 512 units >= 304 slots
+    assert B.paged_decode_plan(256, 32, 4, 64, 8192, sms) == 1536      # persistent work items
+    assert B.paged_decode_plan(2048, 8, 1, 64, 8192, sms) == 1024      # > 1024 sequences
     assert B.paged_decode_plan(256, 32, 4, 64, 300, sms) == 320        # short contexts stay whole
     assert B.paged_decode_plan(1, 8, 8, 64, 1, sms) == 64
     assert B.paged_decode_plan(0, 8, 8, 64, 4096, sms) == 0
@@ -39,6 +40,23 @@ def test_plan_picks_partitions_from_context_length(B):
         assert P % 64 == 0 and P >= min(512, -(-L // 64) * 64)
 
 
+def test_path_follows_the_plan(B):
+    sms = 152
+    P = lambda *a: B.paged_decode_path(*a, sms)
+    assert P(1, 32, 8, 64, 128) == B.PATH_PARTITIONS          # one partition: nothing to merge
+    assert P(16, 32, 8, 64, 2048) == B.PATH_CLUSTER           # 3 partitions per unit, one wave
+    assert P(4, 24, 8, 128, 32768) == B.PATH_PARTITIONS       # 9 partitions: above the cluster limit
+    assert P(1, 8, 1, 64, 4096) == B.PATH_CLUSTER             # 8 partitions: the largest cluster
+    assert P(1, 8, 1, 64, 4097) == B.PATH_PARTITIONS
+    assert P(64, 24, 8, 128, 4096) == B.PATH_PERSISTENT       # 512 units >= 304 slots
+    assert P(256, 32, 4, 64, 8192) == B.PATH_PERSISTENT
+    assert P(2048, 8, 1, 64, 8192) == B.PATH_PARTITIONS       # more sequences than its tables hold
+    assert P(400, 8, 1, 64, 4096) == B.PATH_PARTITIONS        # 400 units < 456 slots: whole
+    assert P(200, 8, 1, 64, 4096) == B.PATH_CLUSTER           # 2 partitions each, 400 CTAs
+    assert P(0, 8, 1, 64, 4096) == 0
+    assert P(2, 16, 1, 64, 4096) == 0                         # unsupported group
+
+
 def test_workspace_sizes(B):
     # o_part [B, Hq, n, D] fp32 + lse_part [B, Hq, n] fp32, each padded to 256 bytes
     n = math.ceil(32768 / 512)
@@ -47,11 +65,13 @@ def test_workspace_sizes(B):
     assert B.paged_decode_split_workspace_size(4, 24, 128, 32768, 512) == expect
     assert B.paged_decode_split_workspace_size(4, 24, 128, 0, 512) == 0
     assert B.paged_decode_split_workspace_size(4, 24, 128, 100, 0) == 0
-    # paged_decode_attention: counters [B*Hkv] u32, then the split layout for the planned P
-    P = B.paged_decode_plan(4, 24, 8, 128, 32768)
+    # paged_decode_attention: counters [B*Hkv] u32 and two scheduling words, then the
+    # split layout for the planned P
     up = lambda x: -(-x // 256) * 256
-    assert B.paged_decode_workspace_size(4, 24, 8, 128, 32768) == (
-        up(4 * 8 * 4) + B.paged_decode_split_workspace_size(4, 24, 128, 32768, P))
+    for (b, hkv) in ((4, 8), (64, 8), (1, 8)):
+        P = B.paged_decode_plan(b, 24, hkv, 128, 32768)
+        assert B.paged_decode_workspace_size(b, 24, hkv, 128, 32768) == (
+            up(b * hkv * 4 + 8) + B.paged_decode_split_workspace_size(b, 24, 128, 32768, P))
 
 
 @pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
