@@ -506,6 +506,29 @@ def run_kernel(args, w) -> None:
         unit, per = "TFLOP/s", flops / 1e12
         bound, peak = "tensor", peaks.get("bf16_tflops") or 1900.0
         metric = f"paged prefill attention (last min(L, {args.chunk}) tokens of each sequence) TFLOP/s"
+    elif args.kernel == "rope_step":
+        nb = algorithmic_bytes(inp)
+        kn, vn = inp["k_new"].to(device), inp["v_new"].to(device)
+        sm = inp["slot_mapping"].to(device)
+        qd = inp["q"].to(device)  # rotated in place by every call
+        out = torch.empty_like(qd)
+        pos = (inp["context_lens"].long() - 1).clamp(min=0).to(device)
+        maxpos = int(inp["max_context_len"]) + 1
+        half = D // 2
+        inv = 10000.0 ** (-torch.arange(half, dtype=torch.float64) * 2.0 / D)
+        ang = torch.arange(maxpos, dtype=torch.float64)[:, None] * inv[None, :]
+        cs = torch.cat([ang.cos(), ang.sin()], 1).float().to(device)
+        ws = torch.zeros(max(B.paged_decode_workspace_size(Bn, Hq, Hkv, D, inp["max_context_len"]), 16),
+                         dtype=torch.uint8, device=device)
+        # the step's bytes plus the in-place q rotation (read + write) and two table rows a token
+        nbytes = nb["step"] + Bn * Hq * D * 2 * 2 + Bn * D * 4 * 2
+
+        def fn(r):
+            B.paged_decode_step_rope(out, qd, kn, vn, sm, pos, cs, kcs[r], vcs[r], bt, cl,
+                                     inp["max_context_len"], inp["scale"], workspace=ws)
+        unit, per = "GB/s", nbytes / 1e9
+        bound, peak = "hbm", peaks.get("hbm_gbs") or 6800.0
+        metric = "decode step with RoPE (rotary write + fused decode) GB/s"
     else:  # rope_write
         T = Bn
         kn = torch.randn(T, Hkv, D, generator=gen).to(torch.bfloat16).to(device)
@@ -555,7 +578,8 @@ def run_kernel(args, w) -> None:
                  "steps": reps * R, "higher_is_better": True,
                  "roofline": {"bound": bound, "achieved": value, "peak": peak, "unit": unit,
                               "frac": value / peak, "traffic": None},
-                 "gpu_launches": reps * R, "clocks": clk})
+                 "gpu_launches": (2 if args.kernel == "rope_step" else 1) * reps * R,
+                 "clocks": clk})
     print(json.dumps(line), flush=True)
 
 
@@ -568,7 +592,7 @@ def main():
     ap.add_argument("--workload", type=int, default=2, choices=sorted(W.WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for the cpu_baseline object (0: skip)")
-    ap.add_argument("--kernel", choices=["step", "prefill", "rope_write"], default="step",
+    ap.add_argument("--kernel", choices=["step", "prefill", "rope_write", "rope_step"], default="step",
                     help="step: the decode step (the benchmark line); others time one kernel")
     ap.add_argument("--chunk", type=int, default=512, help="prefill: query tokens per sequence")
     args = ap.parse_args()

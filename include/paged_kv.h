@@ -217,6 +217,32 @@ int paged_decode_step(pkv_bf16 *out, const pkv_bf16 *q, const pkv_bf16 *k, const
                       void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * paged_decode_step_rope -- one whole decode step with rotary position embedding, as
+ * a model's attention layer runs it ("llm-stack", Serving engine: keys are rotated at
+ * their absolute positions before they enter the cache; "vLLM-Style Llama Inference
+ * Engine", How it works: write the new K/V into the paged cache, then one-token
+ * paged attention):
+ *   1. paged_kv_write_rope(k, v, q, num_q_heads, slot_mapping, positions, num_seqs,
+ *      cos_sin, max_position, rotary_dim, neox_style, k_cache, v_cache, cache):
+ *      q [num_seqs][num_q_heads][head_dim] is rotated IN PLACE, k is rotated and
+ *      written with v at slot_mapping[b];
+ *   2. paged_decode_attention over the updated caches with the rotated q.
+ * Token b is sequence b's new token (one per sequence; positions[b] is normally
+ * context_lens[b] - 1).  Arguments, layouts, workspace rules and results are those of
+ * the two calls; both are checked before either is enqueued.  The attention kernel is
+ * a programmatic dependent of the rotary write: its set-up overlaps the write, and it
+ * reads q and the caches only after the write's stores are visible.
+ */
+int paged_decode_step_rope(pkv_bf16 *out, pkv_bf16 *q, const pkv_bf16 *k, const pkv_bf16 *v,
+                           const int64_t *slot_mapping, const int64_t *positions,
+                           const float *cos_sin, int64_t max_position, int32_t rotary_dim,
+                           int32_t neox_style, pkv_bf16 *k_cache, pkv_bf16 *v_cache,
+                           const int32_t *block_tables, int32_t max_blocks_per_seq,
+                           const int32_t *context_lens, int32_t max_context_len,
+                           int32_t num_seqs, int32_t num_q_heads, const pkv_cache_desc *cache,
+                           float scale, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * paged_prefill_attention -- causal attention of each sequence's newest tokens over
  * the paged cache: prefill, chunked prefill, or recomputation after preemption
  * ("vLLM-Style Llama Inference Engine", How it works: prefill and recomputation use

@@ -66,6 +66,9 @@ _lib.paged_decode_attention.restype = ctypes.c_int
 _lib.paged_decode_step.argtypes = [_P, _P, _P, _P, _P, _i64, _P, _P, _P, _i32, _P, _i32, _i32,
                                    _i32, _D, _f32, _P, _sz, _P]
 _lib.paged_decode_step.restype = ctypes.c_int
+_lib.paged_decode_step_rope.argtypes = [_P, _P, _P, _P, _P, _P, _P, _i64, _i32, _i32, _P, _P, _P,
+                                        _i32, _P, _i32, _i32, _i32, _D, _f32, _P, _sz, _P]
+_lib.paged_decode_step_rope.restype = ctypes.c_int
 _lib.paged_prefill_attention.argtypes = [_P, _P, _P, _P, _P, _i32, _P, _i32, _P, _i32, _i32, _i32,
                                          _D, _f32, _P]
 _lib.paged_prefill_attention.restype = ctypes.c_int
@@ -273,6 +276,44 @@ def paged_decode_step(out: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: to
                                   block_tables.shape[1], _ptr(context_lens), int(max_context_len),
                                   B, Hq, ctypes.byref(d), float(scale), _ptr(workspace), ws_bytes,
                                   _stream(stream)), "paged_decode_step")
+
+
+def paged_decode_step_rope(out: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                           slot_mapping: torch.Tensor, positions: torch.Tensor,
+                           cos_sin: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           block_tables: torch.Tensor, context_lens: torch.Tensor,
+                           max_context_len: int, scale: float, rotary_dim: Optional[int] = None,
+                           neox_style: bool = True, workspace: Optional[torch.Tensor] = None,
+                           stream=None) -> None:
+    """One decode step with RoPE: rotate q (in place) and k at `positions`, write k/v at
+    their slots, then attention over the updated caches.  Token b is sequence b's."""
+    _decode_checks(q, k_cache, v_cache, block_tables, context_lens)
+    _need(out, "out", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1)
+    _need(positions, "positions", torch.int64, 1)
+    _need(cos_sin, "cos_sin", torch.float32, 2)
+    B, Hq, D = q.shape
+    if out.shape != q.shape or k.shape != v.shape or k.shape[0] != B or k.shape[2] != D:
+        raise ValueError("out/q, k/v shapes disagree (one new token per sequence)")
+    if not (slot_mapping.shape[0] == positions.shape[0] == B):
+        raise ValueError("slot_mapping and positions need one entry per sequence")
+    r = D if rotary_dim is None else int(rotary_dim)
+    if cos_sin.shape[1] != r:
+        raise ValueError("cos_sin must be [max_position, rotary_dim]")
+    need = paged_decode_workspace_size(B, Hq, k_cache.shape[1], D, max_context_len)
+    if workspace is None and need > 0:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    d = cache_desc(k_cache)
+    _check(_lib.paged_decode_step_rope(_ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(slot_mapping),
+                                       _ptr(positions), _ptr(cos_sin), cos_sin.shape[0], r,
+                                       1 if neox_style else 0, _ptr(k_cache), _ptr(v_cache),
+                                       _ptr(block_tables), block_tables.shape[1],
+                                       _ptr(context_lens), int(max_context_len), B, Hq,
+                                       ctypes.byref(d), float(scale), _ptr(workspace), ws_bytes,
+                                       _stream(stream)), "paged_decode_step_rope")
 
 
 def paged_prefill_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,

@@ -349,6 +349,7 @@ struct DecodeArgs {
   float scale_log2;            // scale * log2(e)
   uint32_t *sched;             // persistent: [0] next dynamic item, [1] CTAs finished
   int32_t num_seqs;            // persistent: sequences in the batch
+  int32_t q_wait;              // q is written by the preceding kernel: read it after that grid
 };
 
 // The end of one partition (any mode but the cluster merge), on the consumer warps
@@ -430,14 +431,16 @@ __global__ void __launch_bounds__(kThreads, 2)
   // consumer warps: the group's query rows as mma B fragments, also loaded up front
   uint32_t qb[KS][2];
   if (warp < kConsumerWarps) {
+    // In a step whose first kernel rotates q in place, q is read only after that grid.
+    if (a.q_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
     const int gid = lane >> 2, tig = lane & 3;
     const bool hv = gid < a.group;
     const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
         a.q + ((int64_t)b * a.num_q_heads + g * a.group + (hv ? gid : 0)) * D);
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      qb[ks][0] = hv ? __ldg(qrow + 8 * ks + tig) : 0u;
-      qb[ks][1] = hv ? __ldg(qrow + 8 * ks + 4 + tig) : 0u;
+      qb[ks][0] = hv ? __ldcg(qrow + 8 * ks + tig) : 0u;
+      qb[ks][1] = hv ? __ldcg(qrow + 8 * ks + 4 + tig) : 0u;
     }
   }
 
@@ -1105,7 +1108,8 @@ int launch_split(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_c
                  const int32_t *bt, int32_t max_blocks, const int32_t *lens, int32_t max_len,
                  int32_t num_seqs, int32_t hq, const pkv_cache_desc &c, float scale, int32_t P,
                  float *o_part, float *lse_part, pkv_bf16 *out, uint32_t *counters,
-                 cudaStream_t stream, bool programmatic = false, int cluster = 0) {
+                 cudaStream_t stream, bool programmatic = false, int cluster = 0,
+                 bool q_wait = false) {
   CUtensorMap tmk, tmv;
   {
     std::lock_guard<std::mutex> lk(attn_mutex());
@@ -1148,6 +1152,7 @@ int launch_split(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_c
   a.scale_log2 = scale * kLog2e;
   a.sched = nullptr;
   a.num_seqs = num_seqs;
+  a.q_wait = q_wait ? 1 : 0;
   dim3 grid((unsigned)a.n_parts, (unsigned)c.num_kv_heads, (unsigned)num_seqs);
   cudaError_t e;
   if (!programmatic && cluster <= 1) {
@@ -1254,6 +1259,7 @@ int launch_persistent(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16
   a.scale_log2 = scale * kLog2e;
   a.sched = sched;
   a.num_seqs = num_seqs;
+  a.q_wait = 0;  // q arrives by the producer's bulk copy, issued after its griddepcontrol.wait
   // one wave: every CTA starts at once, none waits for another
   const int64_t items_max = (int64_t)num_seqs * c.num_kv_heads * a.n_parts;
   const int64_t slots = (int64_t)sms * split_occupancy(D);
@@ -1410,7 +1416,7 @@ int decode_fused(pkv_bf16 *out, const pkv_bf16 *q, const pkv_bf16 *k_cache,
                  const int32_t *context_lens, int32_t max_context_len, int32_t num_seqs,
                  int32_t num_q_heads, const pkv_cache_desc *cache, float scale, void *workspace,
                  size_t workspace_bytes, cudaStream_t s, bool programmatic, bool launch,
-                 const char *fn) {
+                 const char *fn, bool q_wait = false) {
   int rc = check_decode(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                         max_context_len, num_seqs, num_q_heads, cache, fn);
   if (rc) return rc;
@@ -1447,10 +1453,12 @@ int decode_fused(pkv_bf16 *out, const pkv_bf16 *q, const pkv_bf16 *k_cache,
   const int cluster = path == PKV_PATH_CLUSTER ? (mlen + P - 1) / P : 0;
   return D == 64 ? launch_split<64>(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                     context_lens, mlen, num_seqs, num_q_heads, *cache, scale, P,
-                                    o_part, lse_part, out, counters, s, programmatic, cluster)
+                                    o_part, lse_part, out, counters, s, programmatic, cluster,
+                                    q_wait)
                  : launch_split<128>(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                      context_lens, mlen, num_seqs, num_q_heads, *cache, scale, P,
-                                     o_part, lse_part, out, counters, s, programmatic, cluster);
+                                     o_part, lse_part, out, counters, s, programmatic, cluster,
+                                     q_wait);
 }
 
 }  // namespace
@@ -1490,6 +1498,35 @@ PKV_API int paged_decode_step(pkv_bf16 *out, const pkv_bf16 *q, const pkv_bf16 *
     rc = decode_fused(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                       max_context_len, num_seqs, num_q_heads, cache, scale, workspace,
                       workspace_bytes, s, num_tokens > 0, true, "paged_decode_step");
+  if (!rc) clear_error();
+  return rc;
+}
+
+PKV_API int paged_decode_step_rope(pkv_bf16 *out, pkv_bf16 *q, const pkv_bf16 *k,
+                                   const pkv_bf16 *v, const int64_t *slot_mapping,
+                                   const int64_t *positions, const float *cos_sin,
+                                   int64_t max_position, int32_t rotary_dim, int32_t neox_style,
+                                   pkv_bf16 *k_cache, pkv_bf16 *v_cache,
+                                   const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t *context_lens, int32_t max_context_len,
+                                   int32_t num_seqs, int32_t num_q_heads,
+                                   const pkv_cache_desc *cache, float scale, void *workspace,
+                                   size_t workspace_bytes, void *stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // check both halves before enqueuing either; token b is sequence b's new token
+  int rc = check_write_rope(k, v, q, num_q_heads, slot_mapping, positions, num_seqs, cos_sin,
+                            max_position, rotary_dim, k_cache, v_cache, cache);
+  if (!rc)
+    rc = decode_fused(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                      max_context_len, num_seqs, num_q_heads, cache, scale, workspace,
+                      workspace_bytes, s, false, false, "paged_decode_step_rope");
+  if (rc) return rc;
+  rc = launch_write_rope(k, v, q, num_q_heads, slot_mapping, positions, num_seqs, cos_sin,
+                         max_position, rotary_dim, neox_style, k_cache, v_cache, *cache, s);
+  if (!rc)
+    rc = decode_fused(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                      max_context_len, num_seqs, num_q_heads, cache, scale, workspace,
+                      workspace_bytes, s, num_seqs > 0, true, "paged_decode_step_rope", true);
   if (!rc) clear_error();
   return rc;
 }

@@ -30,6 +30,17 @@ int launch_write(const pkv_bf16 *k, const pkv_bf16 *v, const int64_t *slot_mappi
                  int64_t num_tokens, pkv_bf16 *k_cache, pkv_bf16 *v_cache,
                  const pkv_cache_desc &c, cudaStream_t stream);
 
+// The slot write with rotary embedding, split the same way.
+int check_write_rope(const void *k, const void *v, const void *q, int32_t num_q_heads,
+                     const int64_t *slot_mapping, const int64_t *positions, int64_t num_tokens,
+                     const float *cos_sin, int64_t max_position, int32_t rotary_dim,
+                     const void *k_cache, const void *v_cache, const pkv_cache_desc *cache);
+int launch_write_rope(const pkv_bf16 *k, const pkv_bf16 *v, pkv_bf16 *q, int32_t num_q_heads,
+                      const int64_t *slot_mapping, const int64_t *positions, int64_t num_tokens,
+                      const float *cos_sin, int64_t max_position, int32_t rotary_dim,
+                      int32_t neox_style, pkv_bf16 *k_cache, pkv_bf16 *v_cache,
+                      const pkv_cache_desc &c, cudaStream_t stream);
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // ---- shared by the attention kernels (decode and prefill) ----------------------

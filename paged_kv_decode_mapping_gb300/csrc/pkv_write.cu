@@ -249,13 +249,12 @@ PKV_API int paged_kv_write(const pkv_bf16 *k, const pkv_bf16 *v, const int64_t *
   return rc;
 }
 
-PKV_API int paged_kv_write_rope(const pkv_bf16 *k, const pkv_bf16 *v, pkv_bf16 *q,
-                                int32_t num_q_heads, const int64_t *slot_mapping,
-                                const int64_t *positions, int64_t num_tokens,
-                                const float *cos_sin, int64_t max_position, int32_t rotary_dim,
-                                int32_t neox_style, pkv_bf16 *k_cache, pkv_bf16 *v_cache,
-                                const pkv_cache_desc *cache, void *stream) {
-  using namespace pkv;
+namespace pkv {
+
+int check_write_rope(const void *k, const void *v, const void *q, int32_t num_q_heads,
+                     const int64_t *slot_mapping, const int64_t *positions, int64_t num_tokens,
+                     const float *cos_sin, int64_t max_position, int32_t rotary_dim,
+                     const void *k_cache, const void *v_cache, const pkv_cache_desc *cache) {
   int rc = check_write(k, v, slot_mapping, num_tokens, k_cache, v_cache, cache);
   if (rc) return rc;
   if (rotary_dim <= 0 || rotary_dim % 16 != 0 || rotary_dim > cache->head_dim)
@@ -264,13 +263,19 @@ PKV_API int paged_kv_write_rope(const pkv_bf16 *k, const pkv_bf16 *v, pkv_bf16 *
                      rotary_dim);
   if (max_position <= 0) return set_error(PKV_ERR_SHAPE, "paged_kv_write_rope: max_position <= 0");
   if (q && num_q_heads <= 0) return set_error(PKV_ERR_SHAPE, "paged_kv_write_rope: num_q_heads <= 0");
-  if (num_tokens == 0) {
-    clear_error();
-    return PKV_OK;
-  }
+  if (num_tokens == 0) return PKV_OK;
   if (!positions || !cos_sin) return set_error(PKV_ERR_NULL, "paged_kv_write_rope: NULL positions/cos_sin");
   if (!aligned16(cos_sin) || (q && !aligned16(q)) || (reinterpret_cast<uintptr_t>(positions) & 7u))
     return set_error(PKV_ERR_ALIGN, "paged_kv_write_rope: cos_sin and q 16-byte, positions 8-byte aligned");
+  return PKV_OK;
+}
+
+int launch_write_rope(const pkv_bf16 *k, const pkv_bf16 *v, pkv_bf16 *q, int32_t num_q_heads,
+                      const int64_t *slot_mapping, const int64_t *positions, int64_t num_tokens,
+                      const float *cos_sin, int64_t max_position, int32_t rotary_dim,
+                      int32_t neox_style, pkv_bf16 *k_cache, pkv_bf16 *v_cache,
+                      const pkv_cache_desc &c, cudaStream_t stream) {
+  if (num_tokens == 0) return PKV_OK;
   RopeArgs a;
   a.k = reinterpret_cast<const uint4 *>(k);
   a.v = reinterpret_cast<const uint4 *>(v);
@@ -282,21 +287,39 @@ PKV_API int paged_kv_write_rope(const pkv_bf16 *k, const pkv_bf16 *v, pkv_bf16 *
   a.v_cache = reinterpret_cast<uint4 *>(v_cache);
   a.num_tokens = num_tokens;
   a.max_position = max_position;
-  a.num_blocks = cache->num_blocks;
+  a.num_blocks = c.num_blocks;
   a.num_q_heads = q ? num_q_heads : 0;
-  a.num_kv_heads = cache->num_kv_heads;
-  a.block_size = cache->block_size;
-  a.head_dim = cache->head_dim;
+  a.num_kv_heads = c.num_kv_heads;
+  a.block_size = c.block_size;
+  a.head_dim = c.head_dim;
   a.rotary_dim = rotary_dim;
   a.neox = neox_style ? 1 : 0;
-  const int units = (a.neox ? rotary_dim / 16 : rotary_dim / 8) + (cache->head_dim - rotary_dim) / 8;
-  const int64_t work = num_tokens * ((int64_t)(cache->num_kv_heads + a.num_q_heads) * units +
-                                     (int64_t)cache->num_kv_heads * (cache->head_dim / 8));
+  const int units = (a.neox ? rotary_dim / 16 : rotary_dim / 8) + (c.head_dim - rotary_dim) / 8;
+  const int64_t work = num_tokens * ((int64_t)(c.num_kv_heads + a.num_q_heads) * units +
+                                     (int64_t)c.num_kv_heads * (c.head_dim / 8));
   int64_t blocks = (work + 255) / 256;
   if (blocks > 65535LL * 32) blocks = 65535LL * 32;
-  kv_write_rope_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  kv_write_rope_kernel<<<(unsigned)blocks, 256, 0, stream>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "paged_kv_write_rope launch");
-  clear_error();
   return PKV_OK;
+}
+
+}  // namespace pkv
+
+PKV_API int paged_kv_write_rope(const pkv_bf16 *k, const pkv_bf16 *v, pkv_bf16 *q,
+                                int32_t num_q_heads, const int64_t *slot_mapping,
+                                const int64_t *positions, int64_t num_tokens,
+                                const float *cos_sin, int64_t max_position, int32_t rotary_dim,
+                                int32_t neox_style, pkv_bf16 *k_cache, pkv_bf16 *v_cache,
+                                const pkv_cache_desc *cache, void *stream) {
+  using namespace pkv;
+  int rc = check_write_rope(k, v, q, num_q_heads, slot_mapping, positions, num_tokens, cos_sin,
+                            max_position, rotary_dim, k_cache, v_cache, cache);
+  if (!rc)
+    rc = launch_write_rope(k, v, q, num_q_heads, slot_mapping, positions, num_tokens, cos_sin,
+                           max_position, rotary_dim, neox_style, k_cache, v_cache, *cache,
+                           static_cast<cudaStream_t>(stream));
+  if (!rc) clear_error();
+  return rc;
 }

@@ -606,6 +606,44 @@ def test_rope_write_then_decode(B, oracle):
     assert torch.equal(g["q"].cpu().view(torch.int16), qr.view(torch.int16))
 
 
+STEP_ROPE_CASES = [
+    # D, BS, Hq, Hkv, lens, rotary_dim, neox, path
+    (64, 16, 8, 2, (37, 100, 5), 64, True, "partitions"),
+    (128, 16, 8, 2, (1500, 700), 128, False, "cluster"),
+    (64, 16, 16, 4, _lens(120, 1, 3000, 6, (1, 1536, 1537)), 32, True, "persistent"),
+    (128, 32, 24, 8, _lens(40, 1, 4000, 7), 64, False, "persistent"),
+]
+
+
+@pytest.mark.parametrize("D,BS,Hq,Hkv,lens,r,neox,path", STEP_ROPE_CASES)
+def test_decode_step_rope(B, oracle, D, BS, Hq, Hkv, lens, r, neox, path):
+    """paged_decode_step_rope: q rotated in place and k rotated and written bit for bit
+    like the oracle; the attention (a programmatic dependent that reads q after the
+    rotary write) within tolerance of the oracle over the rotated q and caches."""
+    w = W.small_workload(B=len(lens), Hq=Hq, Hkv=Hkv, D=D, BS=BS, lens=lens, seed=51 + D + r)
+    inp = W.make_inputs(w, poison=True)
+    want = {"partitions": B.PATH_PARTITIONS, "cluster": B.PATH_CLUSTER,
+            "persistent": B.PATH_PERSISTENT}[path]
+    assert B.paged_decode_path(w.B, Hq, Hkv, D, inp["max_context_len"]) == want
+    pos = (inp["context_lens"].long() - 1).clamp(min=0)
+    cs = rope_table(inp["max_context_len"] + 1, r).float()
+    kc, vc, qr = oracle.kv_write_rope(inp["k_new"], inp["v_new"], inp["slot_mapping"], pos, cs,
+                                      inp["k_cache"], inp["v_cache"], q=inp["q"], rotary_dim=r,
+                                      neox_style=neox)
+    ref = oracle.decode(qr, kc, vc, inp["block_tables"], inp["context_lens"], inp["scale"])
+    g = dev(inp)
+    out = torch.empty_like(g["q"])
+    B.paged_decode_step_rope(out, g["q"], g["k_new"], g["v_new"], g["slot_mapping"], pos.cuda(),
+                             cs.cuda(), g["k_cache"], g["v_cache"], g["block_tables"],
+                             g["context_lens"], g["max_context_len"], g["scale"], rotary_dim=r,
+                             neox_style=neox)
+    check_attention(out, ref, f"rope step {path} D={D} r={r}")
+    assert torch.equal(g["q"].cpu().view(torch.int16), qr.view(torch.int16))
+    assert torch.equal(g["k_cache"].cpu().view(torch.int16), kc.view(torch.int16))
+    assert torch.equal(g["v_cache"].cpu().view(torch.int16), vc.view(torch.int16))
+    assert_no_device_errors(B)
+
+
 def test_rope_position_out_of_range_is_flagged(B):
     k = torch.zeros(2, 1, 64, dtype=torch.bfloat16, device="cuda")
     kc = torch.zeros(4, 1, 16, 64, dtype=torch.bfloat16, device="cuda")
