@@ -11,21 +11,11 @@
 namespace pkv {
 
 // ===========================================================================
-// prefill_kernel: causal attention of each sequence's newest tokens over the paged cache
+// Paged prefill: causal attention of each sequence's newest tokens over the paged cache
 // ("vLLM-Style Llama Inference Engine", How it works: prefill and recomputation use
 // causal attention).  Sequence b holds L_b tokens; its last n_b = query_start[b+1] -
 // query_start[b] are the queries; query i sits at position L_b - n_b + i and sees keys
-// t <= that position.
-//
-// One CTA owns one (sequence, kv head, tile of 64 query rows), a row being a (query
-// token, head of the group) pair; warp w owns rows 16w .. 16w+15 of the tile and walks
-// all keys up to the tile's last position, so every K/V byte staged by the producer is
-// used by 64 rows.  Per 64-key stage: S = Q . K^T as mma.sync m16n8k16 (Q: A operand from
-// registers; K^T: B operand from the swizzled stage via ldmatrix), online softmax per row
-// in fp32 (base 2), O += P . V with P reused from the accumulator registers (as bf16 hi +
-// lo) and V through ldmatrix.trans.  Keys past a row's position are masked; V rows past
-// the range are zeroed in registers.  The producer warp and TMA ring are the decode
-// kernel's.
+// t <= that position.  A query row is a (query token, head of the kv head's group) pair.
 struct PrefillArgs {
   const uint16_t *q;            // [Nq][Hq][D]
   const int32_t *block_tables;  // [B][max_blocks]
@@ -37,23 +27,113 @@ struct PrefillArgs {
   float scale_log2;
 };
 
-template <int D, int STAGES>
-__global__ void __launch_bounds__(kThreads, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                   const PrefillArgs a) {
-  constexpr int kTileBytes = kChunk * D * 2;
-  constexpr int kStageBytes = 2 * kTileBytes;
-  constexpr int KS = D / 16;  // k steps over the head dim
-  constexpr int DT = D / 8;   // 8-wide output tiles over the head dim
+// ===========================================================================
+// prefill_tc_kernel: the same causal attention on the 5th-generation tensor cores.
+//
+// One CTA owns one (sequence, kv head, tile of 128 query rows) and walks the keys up to
+// the tile's last position in blocks of 128.  Warps 0-3 run the softmax with one thread
+// per row, warp 4 is the TMA producer, and one thread of warp 5 issues the tensor-core
+// instructions:
+//   S_j = Q . K_j^T   tcgen05.mma M=128 N=128 K=D, Q and K_j K-major in shared memory
+//                     (128-byte swizzle), S in TMEM, two buffers: S_{j+1} is computed
+//                     while the softmax works on S_j;
+//   softmax            per row in fp32, base 2, read straight out of TMEM; P_j =
+//                     exp2(S - m) rounded to bf16 into shared memory (K-major);
+//   O += P_j . V_j    tcgen05.mma M=128 N=D K=128, V_j MN-major, O in TMEM.
+// A row's reference max m moves only when a block raises it by more than 8 (a factor
+// 256): then O and the row sum are rescaled in TMEM.  Otherwise P is taken against the
+// older m, which the final division by the row sum cancels.  The row sum adds the
+// bf16-rounded P values that the tensor cores multiply.  K and V stream through
+// separate rings so that K runs a block ahead of V.
+constexpr int kTcRows = 128;     // query rows per CTA
+constexpr int kTcKeys = 128;     // keys per block
+constexpr int kTcThreads = 192;  // softmax warps 0-3, producer warp 4, MMA warp 5
+constexpr float kTcRescale = 8.f;
 
+template <int D>
+struct TcSmem {
+  static constexpr int KS = D == 64 ? 3 : 2;           // stages of each ring
+  static constexpr uint32_t kSub = kTcKeys * 128;      // one 64-dim sub-tile of 128 rows
+  static constexpr uint32_t kTile = kSub * (D / 64);   // one K or V block / the Q tile
+  static constexpr uint32_t k = 0;
+  static constexpr uint32_t v = k + KS * kTile;
+  static constexpr uint32_t q = v + KS * kTile;        // [D/64][128 rows][128 B]
+  static constexpr uint32_t p = q + kTile;             // [2][128 rows][128 B]
+  static constexpr uint32_t bars = p + 2 * kSub;
+  static constexpr int kBars = 4 * KS + 8;
+  static constexpr uint32_t tslot = bars + kBars * 8;
+  static constexpr uint32_t flag = tslot + 8;
+  static constexpr uint32_t total = flag + 8;
+};
+
+// Loads keys [k0, k0 + nk) of one kv head into a block tile [D/64][128][128 B] (one TMA
+// box of min(BS, 64) rows per lane), completing on `bar`.  win/tb: this ring's window of
+// 32 block-table entries.
+template <int D>
+__device__ __forceinline__ void tc_load_block(const CUtensorMap *tm, uint32_t dst, uint32_t bar,
+                                              int k0, int nk, int &win, int &tb,
+                                              const int32_t *trow, int lb_last,
+                                              const PrefillArgs &a, int g, int lane,
+                                              uint64_t policy) {
+  const int rb = a.box_rows;
+  const int nbox = (nk + rb - 1) / rb;
+  const int lb_hi = (k0 + (nbox - 1) * rb) >> a.log2_bs;
+  if (lb_hi >= win + 32 || (k0 >> a.log2_bs) < win) {
+    win = k0 >> a.log2_bs;
+    tb = (win + lane <= lb_last) ? __ldg(trow + win + lane) : 0;
+  }
+  const int key = k0 + lane * rb;
+  const int src = min(max((key >> a.log2_bs) - win, 0), 31);
+  const int64_t phys_raw = __shfl_sync(0xffffffffu, tb, src);
+  if (lane == 0) dev::mbar_arrive_expect_tx(bar, (uint32_t)nbox * rb * 128u * (D / 64));
+  __syncwarp();
+  if (lane < nbox) {
+    int64_t phys = phys_raw;
+    if (phys < 0 || phys >= a.num_blocks) {
+      raise_error(PKV_DEVERR_BLOCK_ID);
+      phys = 0;
+    }
+    const int off = key & (a.block_size - 1);
+    const int32_t row = (int32_t)((phys * a.num_kv_heads + g) * a.block_size + off);
+    const uint32_t d = dst + (uint32_t)(lane * rb) * 128u;
+    if constexpr (D == 64) {
+      dev::tma_load_2d(d, tm, 0, row, bar, policy);
+    } else {
+#pragma unroll
+      for (int hh = 0; hh < D / 64; ++hh)
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(d + hh * TcSmem<D>::kSub),
+            "l"(reinterpret_cast<uint64_t>(tm)), "r"(0), "r"(hh), "r"(row), "r"(bar), "l"(policy)
+            : "memory");
+    }
+  }
+  __syncwarp();
+}
+
+template <int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmv, const PrefillArgs a) {
+  using SL = TcSmem<D>;
+  constexpr int KS = SL::KS;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = dev::smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t *const base_ptr = smem_raw + (base - raw);
-  const uint32_t bar_full = base + STAGES * kStageBytes;
-  const uint32_t bar_empty = bar_full + STAGES * 8;
-  volatile int *const s_flag =
-      reinterpret_cast<volatile int *>(base_ptr + STAGES * kStageBytes + STAGES * 16);
+  uint8_t *const bp = smem_raw + (base - raw);
+  const uint32_t bars = base + SL::bars;
+  auto k_full = [&](int s) { return bars + 8u * s; };
+  auto k_empty = [&](int s) { return bars + 8u * (KS + s); };
+  auto v_full = [&](int s) { return bars + 8u * (2 * KS + s); };
+  auto v_empty = [&](int s) { return bars + 8u * (3 * KS + s); };
+  auto s_full = [&](int i) { return bars + 8u * (4 * KS + i); };
+  auto s_free = [&](int i) { return bars + 8u * (4 * KS + 2 + i); };
+  const uint32_t p_full = bars + 8u * (4 * KS + 4);
+  const uint32_t pv_done = bars + 8u * (4 * KS + 5);
+  const uint32_t q_ready = bars + 8u * (4 * KS + 6);
+  const uint32_t mma_done = bars + 8u * (4 * KS + 7);
+  volatile uint32_t *const s_tmem = reinterpret_cast<volatile uint32_t *>(bp + SL::tslot);
+  volatile int *const s_flag = reinterpret_cast<volatile int *>(bp + SL::flag);
 
   const int tile = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -67,230 +147,269 @@ __global__ void __launch_bounds__(kThreads, 1)
     L = L < 0 ? 0 : (L > a.cap ? a.cap : L);
     n = n < 0 ? 0 : (n > L ? L : n);
   }
-  const int rows = n * G;                 // query rows of this (b, g)
-  const int row0 = tile * 64;
+  const int rows = n * G;  // query rows of this (b, g)
+  const int row0 = tile * kTcRows;
   if (row0 >= rows) return;
-  const int last_row = min(row0 + 64, rows) - 1;
+  const int last_row = min(row0 + kTcRows, rows) - 1;
   const int t_end = L - n + last_row / G + 1;  // keys the tile needs: [0, t_end)
-  const int n_chunks = (t_end + kChunk - 1) / kChunk;
+  const int nblk = (t_end + kTcKeys - 1) / kTcKeys;
 
   if (tid == 0) {
-#pragma unroll
-    for (int s = 0; s < STAGES; ++s) {
-      dev::mbar_init(bar_full + 8 * s, 1);
-      dev::mbar_init(bar_empty + 8 * s, kConsumerWarps);
+    // one arrival each (the producer, or a tensor-core commit), except s_free, p_full and
+    // q_ready: one arrival per softmax warp
+    for (int i = 0; i < SL::kBars; ++i) {
+      const uint32_t bar = bars + 8u * i;
+      const bool per_warp = bar == s_free(0) || bar == s_free(1) || bar == p_full || bar == q_ready;
+      dev::mbar_init(bar, per_warp ? 4u : 1u);
     }
     *s_flag = 0;
     dev::fence_mbar_init();
   }
+  if (warp == 0) dev::tmem_alloc(base + SL::tslot, 512);
+  dev::tc_fence_before();
   __syncthreads();
+  dev::tc_fence_after();
+  const uint32_t tmem = *s_tmem;  // S buffers at columns 0 and 128, O at 256
 
-  if (warp == kConsumerWarps) {
+  auto fail = [&](bool ok) {
+    if (!ok) {
+      raise_error(PKV_DEVERR_TIMEOUT);
+      *s_flag = 1;
+    }
+    return ok;
+  };
+  int k_issued = 0, v_issued = 0;  // producer: blocks loaded into each ring
+
+  if (warp == 4) {
     // ------------------------------------------------------------- producer warp
-    const uint64_t policy = dev::policy_evict_first();
+    // every query tile of this (sequence, kv head) reads the same blocks: keep them in L2
+    const uint64_t policy = dev::policy_evict_last();
     const int32_t *trow = a.block_tables + (int64_t)b * a.max_blocks;
-    const int rb = a.box_rows;
-    const uint32_t box_bytes = (uint32_t)rb * 128u;
     const int lb_last = (t_end - 1) >> a.log2_bs;
-    int win = 0;
-    int tb = (lane <= lb_last) ? __ldg(trow + lane) : 0;
-    for (int c = 0; c < n_chunks; ++c) {
-      const int s = c % STAGES;
-      if (c >= STAGES &&
-          !__all_sync(0xffffffffu, dev::mbar_wait(bar_empty + 8 * s, ((c / STAGES) - 1) & 1))) {
-        if (lane == 0) {
-          raise_error(PKV_DEVERR_TIMEOUT);
-          *s_flag = 1;
+    int kwin = 0, vwin = 0;
+    int ktb = (lane <= lb_last) ? __ldg(trow + lane) : 0;
+    int vtb = ktb;
+    for (int j = 0; j <= nblk; ++j) {  // K runs one block ahead of V
+      if (j < nblk) {
+        const int s = j % KS;
+        if (j >= KS && !__all_sync(0xffffffffu, dev::mbar_wait(k_empty(s), ((j / KS) - 1) & 1))) {
+          if (lane == 0) fail(false);
+          break;
         }
-        break;
+        tc_load_block<D>(&tmk, base + SL::k + s * SL::kTile, k_full(s), j * kTcKeys,
+                         min(kTcKeys, t_end - j * kTcKeys), kwin, ktb, trow, lb_last, a, g, lane,
+                         policy);
+        k_issued = j + 1;
       }
-      const int k0 = c * kChunk;
-      const int nk = min(kChunk, t_end - k0);
-      const int nbox = (nk + rb - 1) / rb;
-      const int lb_hi = (k0 + (nbox - 1) * rb) >> a.log2_bs;
-      if (lb_hi >= win + 32) {
-        win = k0 >> a.log2_bs;
-        tb = (win + lane <= lb_last) ? __ldg(trow + win + lane) : 0;
-      }
-      const int key = k0 + lane * rb;
-      const int src = min(max((key >> a.log2_bs) - win, 0), 31);
-      const int64_t phys_raw = __shfl_sync(0xffffffffu, tb, src);
-      if (lane == 0) dev::mbar_arrive_expect_tx(bar_full + 8 * s, 2u * nbox * box_bytes * (D / 64));
-      __syncwarp();
-      if (lane < nbox) {
-        int64_t phys = phys_raw;
-        if (phys < 0 || phys >= a.num_blocks) {
-          raise_error(PKV_DEVERR_BLOCK_ID);
-          phys = 0;
+      if (j >= 1) {
+        const int jv = j - 1, s = jv % KS;
+        if (jv >= KS && !__all_sync(0xffffffffu, dev::mbar_wait(v_empty(s), ((jv / KS) - 1) & 1))) {
+          if (lane == 0) fail(false);
+          break;
         }
-        const int off = key & (a.block_size - 1);
-        const int32_t row = (int32_t)((phys * a.num_kv_heads + g) * a.block_size + off);
-        const uint32_t dk = base + s * kStageBytes + lane * box_bytes;
-        issue_box<D>(dk, dk + kTileBytes, &tmk, &tmv, row, bar_full + 8 * s, policy);
+        tc_load_block<D>(&tmv, base + SL::v + s * SL::kTile, v_full(s), jv * kTcKeys,
+                         min(kTcKeys, t_end - jv * kTcKeys), vwin, vtb, trow, lb_last, a, g, lane,
+                         policy);
+        v_issued = jv + 1;
       }
-      __syncwarp();
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------- tensor-core issue (one thread)
+    if (lane == 0) {
+      constexpr uint32_t id_s = dev::idesc_bf16_f32(kTcRows, kTcKeys, 0);
+      constexpr uint32_t id_o = dev::idesc_bf16_f32(kTcRows, D, 1);
+      bool ok = fail(dev::mbar_wait(q_ready, 0));
+      auto issue_s = [&](int j) {
+        const int s = j % KS;
+        if (!fail(dev::mbar_wait(k_full(s), (j / KS) & 1))) return false;
+        if (j >= 2 && !fail(dev::mbar_wait(s_free(j & 1), ((j >> 1) - 1) & 1))) return false;
+        dev::tc_fence_after();
+        const uint32_t kt = base + SL::k + s * SL::kTile;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * SL::kSub + (ks & 3) * 32;
+          dev::umma_bf16(tmem + 128u * (j & 1), dev::smem_desc(base + SL::q + off, 16, 1024),
+                         dev::smem_desc(kt + off, 16, 1024), id_s, ks > 0 ? 1u : 0u);
+        }
+        dev::umma_commit(s_full(j & 1));
+        dev::umma_commit(k_empty(s));
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; ok && j < nblk; ++j) {
+        if (j + 1 < nblk && !(ok = issue_s(j + 1))) break;
+        const int s = j % KS;
+        if (!(ok = fail(dev::mbar_wait(p_full, j & 1)))) break;
+        if (!(ok = fail(dev::mbar_wait(v_full(s), (j / KS) & 1)))) break;
+        dev::tc_fence_after();
+        const uint32_t vt = base + SL::v + s * SL::kTile;
+#pragma unroll
+        for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+          const uint32_t poff = (kk >> 2) * SL::kSub + (kk & 3) * 32;
+          dev::umma_bf16(tmem + 256u, dev::smem_desc(base + SL::p + poff, 16, 1024),
+                         dev::smem_desc(vt + kk * 2048u, SL::kSub, 1024), id_o,
+                         (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        dev::umma_commit(pv_done);
+        dev::umma_commit(v_empty(s));
+      }
+      dev::umma_commit(mma_done);  // arrives once everything issued above has completed
     }
   } else {
-    // ----------------------------------------------------------- consumer warps
-    const int gid = lane >> 2, tig = lane & 3;
-    // this thread's two rows: tile rows 16*warp + gid and + 8
-    const int ra = row0 + 16 * warp + gid, rbw = ra + 8;
-    const bool va = ra < rows, vb = rbw < rows;
-    const int pa = va ? L - n + ra / G : -1, pb = vb ? L - n + rbw / G : -1;  // positions
-    const bool warp_live = __any_sync(0xffffffffu, va || vb);
-    // Q as the A operand: a0a1 (row a, dims 16ks+2tig..), a2a3 (row b), a4a5 / a6a7: dims + 8
-    uint32_t qa[KS][4];
+    // ------------------------------------------------------ softmax warps (row = tid)
+    const int r = tid;
+    const int gr = row0 + r;
+    const bool valid = gr < rows;
+    const int qi = valid ? gr / G : last_row / G;
+    const int h = valid ? gr - (gr / G) * G : 0;
+    const int pos = L - n + qi;                    // keys t <= pos are seen
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    // the tile's query rows into shared memory (K-major, 128-byte swizzle); zeros past the end
     {
-      const uint32_t *qra = reinterpret_cast<const uint32_t *>(
-          a.q + ((int64_t)(q0 + (va ? ra / G : 0)) * a.num_q_heads + g * G + (va ? ra % G : 0)) * D);
-      const uint32_t *qrb = reinterpret_cast<const uint32_t *>(
-          a.q + ((int64_t)(q0 + (vb ? rbw / G : 0)) * a.num_q_heads + g * G + (vb ? rbw % G : 0)) * D);
+      const uint4 *src = reinterpret_cast<const uint4 *>(
+          a.q + ((int64_t)(q0 + qi) * a.num_q_heads + g * G + h) * D);
 #pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        qa[ks][0] = va ? __ldg(qra + 8 * ks + tig) : 0u;
-        qa[ks][1] = vb ? __ldg(qrb + 8 * ks + tig) : 0u;
-        qa[ks][2] = va ? __ldg(qra + 8 * ks + 4 + tig) : 0u;
-        qa[ks][3] = vb ? __ldg(qrb + 8 * ks + 4 + tig) : 0u;
+      for (int c = 0; c < D / 8; ++c) {
+        const uint4 v = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4 *>(bp + SL::q + (c >> 3) * SL::kSub + r * 128 +
+                                   (((c & 7) ^ (r & 7)) << 4)) = v;
       }
-    }
-    float o[DT][4];
-#pragma unroll
-    for (int dt = 0; dt < DT; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
-    float ma = -INFINITY, mb = -INFINITY, la = 0.f, lb = 0.f;
-    const int lj = lane >> 3, lr = lane & 7;
-
-    for (int c = 0; c < n_chunks; ++c) {
-      const int s = c % STAGES;
-      if (!__all_sync(0xffffffffu, dev::mbar_wait(bar_full + 8 * s, (c / STAGES) & 1))) {
-        if (lane == 0) {
-          raise_error(PKV_DEVERR_TIMEOUT);
-          *s_flag = 1;
-        }
-        break;
-      }
-      const int k0 = c * kChunk;
-      if (warp_live) {
-        const uint32_t kb = base + s * kStageBytes, vbase = kb + kTileBytes;
-        // S (16 rows x 64 keys) = Q . K^T, eight 8-key n tiles
-        float sc[8][4];
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {  // keys 16m .. 16m+15: n tiles 2m, 2m+1
-            uint32_t bk[4];
-            dev::ldsm_x4(bk, kb + tile_off(16 * m + lr + ((lj >> 1) << 3), 2 * ks + (lj & 1)));
-            dev::mma_bf16_16816(sc[2 * m], qa[ks], bk[0], bk[1]);
-            dev::mma_bf16_16816(sc[2 * m + 1], qa[ks], bk[2], bk[3]);
-          }
-        }
-        // causal mask and base-2 scale; row max over the quad
-        float mxa = -INFINITY, mxb = -INFINITY;
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-          const int key = k0 + 8 * nt + 2 * tig;
-          sc[nt][0] = key <= pa ? sc[nt][0] * a.scale_log2 : -INFINITY;
-          sc[nt][1] = key + 1 <= pa ? sc[nt][1] * a.scale_log2 : -INFINITY;
-          sc[nt][2] = key <= pb ? sc[nt][2] * a.scale_log2 : -INFINITY;
-          sc[nt][3] = key + 1 <= pb ? sc[nt][3] * a.scale_log2 : -INFINITY;
-          mxa = fmaxf(mxa, fmaxf(sc[nt][0], sc[nt][1]));
-          mxb = fmaxf(mxb, fmaxf(sc[nt][2], sc[nt][3]));
-        }
-#pragma unroll
-        for (int x = 1; x < 4; x <<= 1) {
-          mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, x));
-          mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, x));
-        }
-        const float mna = fmaxf(ma, mxa), mnb = fmaxf(mb, mxb);
-        // a row that has seen no key yet keeps -inf: subtract 0 then (ex2(-inf) = 0, no NaN)
-        const float ua = mna == -INFINITY ? 0.f : mna, ub = mnb == -INFINITY ? 0.f : mnb;
-        const float ala = dev::ex2(ma - ua), alb = dev::ex2(mb - ub);
-        ma = mna;
-        mb = mnb;
-        la *= ala;
-        lb *= alb;
-#pragma unroll
-        for (int dt = 0; dt < DT; ++dt) {
-          o[dt][0] *= ala;
-          o[dt][1] *= ala;
-          o[dt][2] *= alb;
-          o[dt][3] *= alb;
-        }
-        uint32_t ph[4][4], pl[4][4];  // P as A operands, per 16-key group: hi and residual
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-          const float p0 = dev::ex2(sc[nt][0] - ua), p1 = dev::ex2(sc[nt][1] - ua);
-          const float p2 = dev::ex2(sc[nt][2] - ub), p3 = dev::ex2(sc[nt][3] - ub);
-          la += p0 + p1;
-          lb += p2 + p3;
-          const uint32_t h01 = dev::pack_bf16x2(p0, p1), h23 = dev::pack_bf16x2(p2, p3);
-          const uint32_t r01 = dev::pack_bf16x2(p0 - dev::bf16lo_to_f32(h01), p1 - dev::bf16hi_to_f32(h01));
-          const uint32_t r23 = dev::pack_bf16x2(p2 - dev::bf16lo_to_f32(h23), p3 - dev::bf16hi_to_f32(h23));
-          const int m = nt >> 1, hi = nt & 1;  // a0a1/a2a3 from the even tile, a4a5/a6a7 odd
-          ph[m][2 * hi] = h01;
-          ph[m][2 * hi + 1] = h23;
-          pl[m][2 * hi] = r01;
-          pl[m][2 * hi + 1] = r23;
-        }
-        // O += P . V; V rows past the range zeroed in registers
-        const int nk = t_end - k0;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-          if (nk < 16 * m + 16) {
-            const int kk = 16 * m + 2 * tig;
-            mlo = (kk < nk ? 0x0000ffffu : 0u) | (kk + 1 < nk ? 0xffff0000u : 0u);
-            mhi = (kk + 8 < nk ? 0x0000ffffu : 0u) | (kk + 9 < nk ? 0xffff0000u : 0u);
-          }
-#pragma unroll
-          for (int dt = 0; dt < DT; dt += 2) {
-            uint32_t bv[4];  // (keys 0-7, dims dt), (keys 8-15, dims dt), (keys 0-7, dt+1), (8-15, dt+1)
-            dev::ldsm_x4_trans(bv, vbase + tile_off(16 * m + lr + ((lj & 1) << 3), dt + (lj >> 1)));
-            bv[0] &= mlo;
-            bv[1] &= mhi;
-            bv[2] &= mlo;
-            bv[3] &= mhi;
-            dev::mma_bf16_16816(o[dt], ph[m], bv[0], bv[1]);
-            dev::mma_bf16_16816(o[dt], pl[m], bv[0], bv[1]);
-            dev::mma_bf16_16816(o[dt + 1], ph[m], bv[2], bv[3]);
-            dev::mma_bf16_16816(o[dt + 1], pl[m], bv[2], bv[3]);
-          }
-        }
-      }
+      dev::fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) dev::mbar_arrive(bar_empty + 8 * s);
+      if (lane == 0) dev::mbar_arrive(q_ready);
     }
-    // ---- normalise and store this thread's rows
+    float m_ref = -INFINITY, lsum = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nblk; ++j) {
+      const int k0 = j * kTcKeys;
+      const int nk = min(kTcKeys, t_end - k0);
+      const int lim = min(pos, t_end - 1) - k0;  // columns c <= lim are seen by this row
+      if (!(ok = __all_sync(0xffffffffu, dev::mbar_wait(s_full(j & 1), (j >> 1) & 1)))) break;
+      dev::tc_fence_after();
+      const uint32_t st = tmem + lane_base + 128u * (j & 1);
+      // pass 1: the block's row max
+      float bmax = -INFINITY;
 #pragma unroll
-    for (int x = 1; x < 4; x <<= 1) {
-      la += __shfl_xor_sync(0xffffffffu, la, x);
-      lb += __shfl_xor_sync(0xffffffffu, lb, x);
+      for (int ch = 0; ch < kTcKeys / 32; ++ch) {
+        uint32_t x[32];
+        dev::tmem_ld32(st + ch * 32, x);
+        dev::tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (ch * 32 + i <= lim) bmax = fmaxf(bmax, __uint_as_float(x[i]) * a.scale_log2);
+      }
+      if (j > 0) {  // P is free and O stable once the previous block's P.V has completed
+        if (!(ok = __all_sync(0xffffffffu, dev::mbar_wait(pv_done, (j - 1) & 1)))) break;
+        dev::tc_fence_after();
+        const bool need = bmax > m_ref + kTcRescale;
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_new = fmaxf(m_ref, bmax);
+          const float f = need ? dev::ex2(m_ref - m_new) : 1.f;
+#pragma unroll
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t o[32];
+            dev::tmem_ld32(tmem + lane_base + 256u + ch * 32, o);
+            dev::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+            dev::tmem_st32(tmem + lane_base + 256u + ch * 32, o);
+          }
+          dev::tmem_wait_st();
+          lsum *= f;
+          if (need) m_ref = m_new;
+        }
+      } else {
+        m_ref = bmax;  // block 0 holds key 0, which every row sees
+      }
+      // pass 2: P = exp2(S - m_ref) as bf16 into shared memory; the row sum of what was stored
+#pragma unroll
+      for (int ch = 0; ch < kTcKeys / 32; ++ch) {
+        uint32_t x[32];
+        dev::tmem_ld32(st + ch * 32, x);
+        dev::tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c = ch * 32 + 2 * i;
+          const float p0 = c <= lim ? dev::ex2(__uint_as_float(x[2 * i]) * a.scale_log2 - m_ref) : 0.f;
+          const float p1 =
+              c + 1 <= lim ? dev::ex2(__uint_as_float(x[2 * i + 1]) * a.scale_log2 - m_ref) : 0.f;
+          pk[i] = dev::pack_bf16x2(p0, p1);
+          lsum += dev::bf16lo_to_f32(pk[i]) + dev::bf16hi_to_f32(pk[i]);
+        }
+        const uint32_t prow = SL::p + (ch >> 1) * SL::kSub + r * 128;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c16 = (ch & 1) * 4 + u;
+          *reinterpret_cast<uint4 *>(bp + prow + ((c16 ^ (r & 7)) << 4)) =
+              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      }
+      if (nk < kTcKeys) {  // last block: V rows past the keys hold stale or unowned data
+        const int s = j % KS;
+        if (!(ok = __all_sync(0xffffffffu, dev::mbar_wait(v_full(s), (j / KS) & 1)))) break;
+        const uint32_t vt = SL::v + s * SL::kTile;
+        for (int idx = r; idx < (kTcKeys - nk) * (D / 8); idx += kTcRows) {
+          const int row = nk + idx / (D / 8), c = idx % (D / 8);
+          *reinterpret_cast<uint4 *>(bp + vt + (c >> 3) * SL::kSub + row * 128 +
+                                     (((c & 7) ^ (row & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      dev::tc_fence_before();
+      dev::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        dev::mbar_arrive(s_free(j & 1));
+        dev::mbar_arrive(p_full);
+      }
     }
-    if (!*s_flag) {
-      const float ia = 1.f / la, ib = 1.f / lb;
-      uint32_t *oa = reinterpret_cast<uint32_t *>(
-          a.out + ((int64_t)(q0 + (va ? ra / G : 0)) * a.num_q_heads + g * G + (va ? ra % G : 0)) * D);
-      uint32_t *ob = reinterpret_cast<uint32_t *>(
-          a.out + ((int64_t)(q0 + (vb ? rbw / G : 0)) * a.num_q_heads + g * G + (vb ? rbw % G : 0)) * D);
+    if (!ok && lane == 0) fail(false);
+    // epilogue: O / l as bf16
+    if (ok && __all_sync(0xffffffffu, dev::mbar_wait(pv_done, (nblk - 1) & 1))) {
+      dev::tc_fence_after();
+      const float inv = 1.f / lsum;
+      uint4 *dst = reinterpret_cast<uint4 *>(
+          a.out + ((int64_t)(q0 + qi) * a.num_q_heads + g * G + h) * D);
 #pragma unroll
-      for (int dt = 0; dt < DT; ++dt) {
-        if (va) oa[4 * dt + tig] = dev::pack_bf16x2(o[dt][0] * ia, o[dt][1] * ia);
-        if (vb) ob[4 * dt + tig] = dev::pack_bf16x2(o[dt][2] * ib, o[dt][3] * ib);
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t o[32];
+        dev::tmem_ld32(tmem + lane_base + 256u + ch * 32, o);
+        dev::tmem_wait_ld();
+        if (valid) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w4[e] = dev::pack_bf16x2(__uint_as_float(o[8 * u + 2 * e]) * inv,
+                                       __uint_as_float(o[8 * u + 2 * e + 1]) * inv);
+            dst[ch * 4 + u] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
+        }
       }
     }
   }
 
-  __syncthreads();
-  if (tid == 0 && *s_flag) {
-    for (int s = 0; s < STAGES; ++s) {
-      const int c_last = s + ((n_chunks - 1 - s) / STAGES) * STAGES;
-      if (c_last >= 0 && c_last < n_chunks) (void)dev::mbar_wait(bar_full + 8 * s, (c_last / STAGES) & 1);
+  // ---- teardown: no tensor-core op or copy may still be in flight when TMEM is freed
+  if (tid == 0) (void)dev::mbar_wait(mma_done, 0);
+  if (warp == 4 && lane == 0 && *s_flag) {
+    for (int s = 0; s < KS; ++s) {
+      const int kl = s + ((k_issued - 1 - s) / KS) * KS;
+      if (kl >= 0 && kl < k_issued) (void)dev::mbar_wait(k_full(s), (kl / KS) & 1);
+      const int vl = s + ((v_issued - 1 - s) / KS) * KS;
+      if (vl >= 0 && vl < v_issued) (void)dev::mbar_wait(v_full(s), (vl / KS) & 1);
     }
   }
+  dev::tc_fence_before();
+  __syncthreads();
+  dev::tc_fence_after();
+  if (warp == 0) dev::tmem_dealloc(tmem, 512);
 }
 
 cudaError_t read_prefill_errors(uint32_t *flags, int clear) { return read_tu_errors(flags, clear); }
+
+constexpr size_t tc_smem(int d) { return 1024 + (d == 64 ? TcSmem<64>::total : TcSmem<128>::total); }
+static_assert(tc_smem(64) <= 227 * 1024 && tc_smem(128) <= 227 * 1024, "prefill tile fits a CTA");
 
 namespace {
 bool g_prefill_attr[kMaxDevices][2];  // dynamic smem attribute of prefill_kernel set
@@ -316,10 +435,10 @@ PKV_API int paged_prefill_attention(pkv_bf16 *out, const pkv_bf16 *q, const pkv_
     return PKV_OK;
   }
   if (!out || !query_start) return set_error(PKV_ERR_NULL, "paged_prefill_attention: NULL out/query_start");
-  if (reinterpret_cast<uintptr_t>(out) & 3u)
-    return set_error(PKV_ERR_ALIGN, "paged_prefill_attention: out must be 4-byte aligned");
+  if (!aligned16(out))
+    return set_error(PKV_ERR_ALIGN, "paged_prefill_attention: out must be 16-byte aligned");
   const int G = num_q_heads / cache->num_kv_heads;
-  const int64_t tiles = ((int64_t)max_query_len * G + 63) / 64;
+  const int64_t tiles = ((int64_t)max_query_len * G + kTcRows - 1) / kTcRows;
   if (tiles > 0x7fffffffLL) return set_error(PKV_ERR_UNSUPPORTED, "paged_prefill_attention: too many query rows");
   CUtensorMap tmk, tmv;
   const int D = cache->head_dim;
@@ -330,12 +449,12 @@ PKV_API int paged_prefill_attention(pkv_bf16 *out, const pkv_bf16 *q, const pkv_
     if ((rc = current_device(&dev))) return rc;
     const int vi = D == 64 ? 0 : 1;
     if (!g_prefill_attr[dev][vi]) {
-      cudaError_t e = D == 64 ? cudaFuncSetAttribute(prefill_kernel<64, split_stages(64)>,
+      cudaError_t e = D == 64 ? cudaFuncSetAttribute(prefill_tc_kernel<64>,
                                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     (int)split_smem(64))
-                              : cudaFuncSetAttribute(prefill_kernel<128, split_stages(128)>,
+                                                     (int)tc_smem(64))
+                              : cudaFuncSetAttribute(prefill_tc_kernel<128>,
                                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     (int)split_smem(128));
+                                                     (int)tc_smem(128));
       if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute");
       g_prefill_attr[dev][vi] = true;
     }
@@ -359,11 +478,11 @@ PKV_API int paged_prefill_attention(pkv_bf16 *out, const pkv_bf16 *q, const pkv_
   dim3 grid((unsigned)tiles, (unsigned)cache->num_kv_heads, (unsigned)num_seqs);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (D == 64)
-    prefill_kernel<64, split_stages(64)><<<grid, kThreads, split_smem(64), s>>>(tmk, tmv, a);
+    prefill_tc_kernel<64><<<grid, kTcThreads, tc_smem(64), s>>>(tmk, tmv, a);
   else
-    prefill_kernel<128, split_stages(128)><<<grid, kThreads, split_smem(128), s>>>(tmk, tmv, a);
+    prefill_tc_kernel<128><<<grid, kTcThreads, tc_smem(128), s>>>(tmk, tmv, a);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_error(e, "prefill_kernel launch");
+  if (e != cudaSuccess) return cuda_error(e, "prefill_tc_kernel launch");
   clear_error();
   return PKV_OK;
 }

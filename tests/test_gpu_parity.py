@@ -686,6 +686,29 @@ def test_prefill_matches_oracle(B, oracle, D, BS, Hq, Hkv, lens, chunks):
     assert_no_device_errors(B)
 
 
+@pytest.mark.parametrize("D,BS,Hq,Hkv", [(128, 32, 8, 2), (64, 16, 12, 4)])
+def test_prefill_wide_scores_and_full_tiles(B, oracle, D, BS, Hq, Hkv):
+    """Scores spread wide (scale 1): a row's running max often jumps by more than 2^8,
+    so the rescale of O in TMEM runs.  Several full 128-row tiles per (sequence, kv
+    head), causal diagonals inside key blocks, and a ragged last block."""
+    import itertools
+    lens, chunks = (1100, 400, 129), (260, 400, 3)
+    w = W.small_workload(B=len(lens), Hq=Hq, Hkv=Hkv, D=D, BS=BS, lens=lens, seed=61 + D,
+                         write="none")
+    inp = W.make_inputs(w, poison=True)
+    gen = torch.Generator().manual_seed(62)
+    qs = torch.tensor([0] + list(itertools.accumulate(chunks)), dtype=torch.int32)
+    q = torch.randn(int(qs[-1]), Hq, D, generator=gen).to(torch.bfloat16)
+    ref = oracle.prefill(q, inp["k_cache"], inp["v_cache"], inp["block_tables"], inp["context_lens"],
+                         qs, 1.0)
+    g = dev(inp)
+    out = torch.full((int(qs[-1]), Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    B.paged_prefill_attention(out, q.cuda(), g["k_cache"], g["v_cache"], g["block_tables"],
+                              g["context_lens"], inp["max_context_len"], qs.cuda(), max(chunks), 1.0)
+    check_attention(out, ref, f"prefill scale 1 D={D} G={Hq // Hkv}")
+    assert_no_device_errors(B)
+
+
 def test_prefill_single_token_chunks_equal_decode(B, oracle):
     """A chunk of one token per sequence is a decode step."""
     w = W.small_workload(B=3, Hq=32, Hkv=8, D=64, BS=16, lens=(5, 900, 2048), seed=51, write="none")
