@@ -58,9 +58,10 @@ struct TcSmem {
   static constexpr uint32_t k = 0;
   static constexpr uint32_t v = k + KS * kTile;
   static constexpr uint32_t q = v + KS * kTile;        // [D/64][128 rows][128 B]
-  static constexpr uint32_t p = q + kTile;             // [2][128 rows][128 B]
-  static constexpr uint32_t bars = p + 2 * kSub;
-  static constexpr int kBars = 4 * KS + 8;
+  static constexpr uint32_t p = q + kTile;             // two buffers of [2][128 rows][128 B]
+  static constexpr uint32_t kP = 2 * kSub;
+  static constexpr uint32_t bars = p + 2 * kP;
+  static constexpr int kBars = 4 * KS + 10;
   static constexpr uint32_t tslot = bars + kBars * 8;
   static constexpr uint32_t flag = tslot + 8;
   static constexpr uint32_t total = flag + 8;
@@ -126,12 +127,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   auto k_empty = [&](int s) { return bars + 8u * (KS + s); };
   auto v_full = [&](int s) { return bars + 8u * (2 * KS + s); };
   auto v_empty = [&](int s) { return bars + 8u * (3 * KS + s); };
+  // two of each of these, one per S (and P) buffer, so that no barrier can run two
+  // phases ahead of its waiter
   auto s_full = [&](int i) { return bars + 8u * (4 * KS + i); };
   auto s_free = [&](int i) { return bars + 8u * (4 * KS + 2 + i); };
-  const uint32_t p_full = bars + 8u * (4 * KS + 4);
-  const uint32_t pv_done = bars + 8u * (4 * KS + 5);
-  const uint32_t q_ready = bars + 8u * (4 * KS + 6);
-  const uint32_t mma_done = bars + 8u * (4 * KS + 7);
+  auto p_full = [&](int i) { return bars + 8u * (4 * KS + 4 + i); };
+  auto pv_done = [&](int i) { return bars + 8u * (4 * KS + 6 + i); };
+  const uint32_t q_ready = bars + 8u * (4 * KS + 8);
+  const uint32_t mma_done = bars + 8u * (4 * KS + 9);
   volatile uint32_t *const s_tmem = reinterpret_cast<volatile uint32_t *>(bp + SL::tslot);
   volatile int *const s_flag = reinterpret_cast<volatile int *>(bp + SL::flag);
 
@@ -159,7 +162,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // q_ready: one arrival per softmax warp
     for (int i = 0; i < SL::kBars; ++i) {
       const uint32_t bar = bars + 8u * i;
-      const bool per_warp = bar == s_free(0) || bar == s_free(1) || bar == p_full || bar == q_ready;
+      const bool per_warp = bar == s_free(0) || bar == s_free(1) || bar == p_full(0) ||
+                            bar == p_full(1) || bar == q_ready;
       dev::mbar_init(bar, per_warp ? 4u : 1u);
     }
     *s_flag = 0;
@@ -239,18 +243,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int j = 0; ok && j < nblk; ++j) {
         if (j + 1 < nblk && !(ok = issue_s(j + 1))) break;
         const int s = j % KS;
-        if (!(ok = fail(dev::mbar_wait(p_full, j & 1)))) break;
+        if (!(ok = fail(dev::mbar_wait(p_full(j & 1), (j >> 1) & 1)))) break;
         if (!(ok = fail(dev::mbar_wait(v_full(s), (j / KS) & 1)))) break;
         dev::tc_fence_after();
         const uint32_t vt = base + SL::v + s * SL::kTile;
+        const uint32_t pb = base + SL::p + (j & 1) * SL::kP;
 #pragma unroll
         for (int kk = 0; kk < kTcKeys / 16; ++kk) {
           const uint32_t poff = (kk >> 2) * SL::kSub + (kk & 3) * 32;
-          dev::umma_bf16(tmem + 256u, dev::smem_desc(base + SL::p + poff, 16, 1024),
+          dev::umma_bf16(tmem + 256u, dev::smem_desc(pb + poff, 16, 1024),
                          dev::smem_desc(vt + kk * 2048u, SL::kSub, 1024), id_o,
                          (j > 0 || kk > 0) ? 1u : 0u);
         }
-        dev::umma_commit(pv_done);
+        dev::umma_commit(pv_done(j & 1));
         dev::umma_commit(v_empty(s));
       }
       dev::umma_commit(mma_done);  // arrives once everything issued above has completed
@@ -286,23 +291,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int lim = min(pos, t_end - 1) - k0;  // columns c <= lim are seen by this row
       if (!(ok = __all_sync(0xffffffffu, dev::mbar_wait(s_full(j & 1), (j >> 1) & 1)))) break;
       dev::tc_fence_after();
-      const uint32_t st = tmem + lane_base + 128u * (j & 1);
-      // pass 1: the block's row max
-      float bmax = -INFINITY;
+      // the block's S row into registers; the MMA warp may then refill the buffer
+      uint32_t sv[kTcKeys];
 #pragma unroll
-      for (int ch = 0; ch < kTcKeys / 32; ++ch) {
-        uint32_t x[32];
-        dev::tmem_ld32(st + ch * 32, x);
-        dev::tmem_wait_ld();
+      for (int ch = 0; ch < kTcKeys / 32; ++ch)
+        dev::tmem_ld32(tmem + lane_base + 128u * (j & 1) + ch * 32,
+                       *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * ch));
+      dev::tmem_wait_ld();
+      dev::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) dev::mbar_arrive(s_free(j & 1));
+      const bool whole = __all_sync(0xffffffffu, lim >= kTcKeys - 1);  // no column masked
+      // pass 1: the block's row max (eight independent chains)
+      float mx[8];
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (ch * 32 + i <= lim) bmax = fmaxf(bmax, __uint_as_float(x[i]) * a.scale_log2);
+      for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
+      if (whole) {
+#pragma unroll
+        for (int i = 0; i < kTcKeys; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(sv[i]) * a.scale_log2);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kTcKeys; ++i)
+          mx[i & 7] = fmaxf(mx[i & 7], i <= lim ? __uint_as_float(sv[i]) * a.scale_log2 : -INFINITY);
       }
-      if (j > 0) {  // P is free and O stable once the previous block's P.V has completed
-        if (!(ok = __all_sync(0xffffffffu, dev::mbar_wait(pv_done, (j - 1) & 1)))) break;
-        dev::tc_fence_after();
+      const float bmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      if (j > 0) {
         const bool need = bmax > m_ref + kTcRescale;
-        if (__any_sync(0xffffffffu, need)) {
+        if (__any_sync(0xffffffffu, need)) {  // O moves: wait until the previous P.V is in
+          if (!(ok = __all_sync(0xffffffffu,
+                                dev::mbar_wait(pv_done((j - 1) & 1), ((j - 1) >> 1) & 1))))
+            break;
+          dev::tc_fence_after();
           const float m_new = fmaxf(m_ref, bmax);
           const float f = need ? dev::ex2(m_ref - m_new) : 1.f;
 #pragma unroll
@@ -321,30 +341,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       } else {
         m_ref = bmax;  // block 0 holds key 0, which every row sees
       }
-      // pass 2: P = exp2(S - m_ref) as bf16 into shared memory; the row sum of what was stored
+      // this P buffer is free once the P.V of two blocks back has completed
+      if (j >= 2 && !(ok = __all_sync(0xffffffffu,
+                                      dev::mbar_wait(pv_done(j & 1), ((j - 2) >> 1) & 1))))
+        break;
+      // pass 2: P = exp2(S - m_ref) as bf16 into shared memory, and its row sum
+      float ls[8];
 #pragma unroll
-      for (int ch = 0; ch < kTcKeys / 32; ++ch) {
-        uint32_t x[32];
-        dev::tmem_ld32(st + ch * 32, x);
-        dev::tmem_wait_ld();
-        uint32_t pk[16];
+      for (int u = 0; u < 8; ++u) ls[u] = 0.f;
+      const uint32_t pb = SL::p + (j & 1) * SL::kP + r * 128;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int c = ch * 32 + 2 * i;
-          const float p0 = c <= lim ? dev::ex2(__uint_as_float(x[2 * i]) * a.scale_log2 - m_ref) : 0.f;
-          const float p1 =
-              c + 1 <= lim ? dev::ex2(__uint_as_float(x[2 * i + 1]) * a.scale_log2 - m_ref) : 0.f;
-          pk[i] = dev::pack_bf16x2(p0, p1);
-          lsum += dev::bf16lo_to_f32(pk[i]) + dev::bf16hi_to_f32(pk[i]);
+      for (int c16 = 0; c16 < kTcKeys / 8; ++c16) {  // 16-byte chunks of 8 keys
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = 8 * c16 + 2 * e;
+          float p0 = dev::ex2(fmaf(__uint_as_float(sv[c]), a.scale_log2, -m_ref));
+          float p1 = dev::ex2(fmaf(__uint_as_float(sv[c + 1]), a.scale_log2, -m_ref));
+          if (!whole) {
+            p0 = c <= lim ? p0 : 0.f;
+            p1 = c + 1 <= lim ? p1 : 0.f;
+          }
+          pk[e] = dev::pack_bf16x2(p0, p1);
+          // sum what the tensor cores multiply: with a stale reference max the largest
+          // P is not a power of two, and only this keeps the weights a convex combination
+          ls[(2 * e) & 7] += dev::bf16lo_to_f32(pk[e]);
+          ls[(2 * e + 1) & 7] += dev::bf16hi_to_f32(pk[e]);
         }
-        const uint32_t prow = SL::p + (ch >> 1) * SL::kSub + r * 128;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int c16 = (ch & 1) * 4 + u;
-          *reinterpret_cast<uint4 *>(bp + prow + ((c16 ^ (r & 7)) << 4)) =
-              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-        }
+        *reinterpret_cast<uint4 *>(bp + pb + (c16 >> 3) * SL::kSub + (((c16 & 7) ^ (r & 7)) << 4)) =
+            make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
+      lsum += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       if (nk < kTcKeys) {  // last block: V rows past the keys hold stale or unowned data
         const int s = j % KS;
         if (!(ok = __all_sync(0xffffffffu, dev::mbar_wait(v_full(s), (j / KS) & 1)))) break;
@@ -358,14 +385,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       dev::tc_fence_before();
       dev::fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        dev::mbar_arrive(s_free(j & 1));
-        dev::mbar_arrive(p_full);
-      }
+      if (lane == 0) dev::mbar_arrive(p_full(j & 1));
     }
     if (!ok && lane == 0) fail(false);
     // epilogue: O / l as bf16
-    if (ok && __all_sync(0xffffffffu, dev::mbar_wait(pv_done, (nblk - 1) & 1))) {
+    if (ok && __all_sync(0xffffffffu, dev::mbar_wait(pv_done((nblk - 1) & 1), ((nblk - 1) >> 1) & 1))) {
       dev::tc_fence_after();
       const float inv = 1.f / lsum;
       uint4 *dst = reinterpret_cast<uint4 *>(
