@@ -291,28 +291,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int lim = min(pos, t_end - 1) - k0;  // columns c <= lim are seen by this row
       if (!(ok = __all_sync(0xffffffffu, dev::mbar_wait(s_full(j & 1), (j >> 1) & 1)))) break;
       dev::tc_fence_after();
-      // the block's S row into registers; the MMA warp may then refill the buffer
-      uint32_t sv[kTcKeys];
-#pragma unroll
-      for (int ch = 0; ch < kTcKeys / 32; ++ch)
-        dev::tmem_ld32(tmem + lane_base + 128u * (j & 1) + ch * 32,
-                       *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * ch));
-      dev::tmem_wait_ld();
-      dev::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) dev::mbar_arrive(s_free(j & 1));
+      // S row of this block: four chunks of 32 columns, read from TMEM in each pass
+      const uint32_t sbase = tmem + lane_base + 128u * (j & 1);
       const bool whole = __all_sync(0xffffffffu, lim >= kTcKeys - 1);  // no column masked
       // pass 1: the block's row max (eight independent chains)
       float mx[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
-      if (whole) {
+#pragma unroll 1
+      for (int ch = 0; ch < kTcKeys / 32; ++ch) {
+        uint32_t x[32];
+        dev::tmem_ld32(sbase + ch * 32, x);
+        dev::tmem_wait_ld();
+        const int lc = lim - ch * 32;
+        if (whole) {
 #pragma unroll
-        for (int i = 0; i < kTcKeys; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(sv[i]) * a.scale_log2);
-      } else {
+          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(x[i]) * a.scale_log2);
+        } else {
 #pragma unroll
-        for (int i = 0; i < kTcKeys; ++i)
-          mx[i & 7] = fmaxf(mx[i & 7], i <= lim ? __uint_as_float(sv[i]) * a.scale_log2 : -INFINITY);
+          for (int i = 0; i < 32; ++i)
+            mx[i & 7] = fmaxf(mx[i & 7], i <= lc ? __uint_as_float(x[i]) * a.scale_log2 : -INFINITY);
+        }
       }
       const float bmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
@@ -325,7 +324,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           dev::tc_fence_after();
           const float m_new = fmaxf(m_ref, bmax);
           const float f = need ? dev::ex2(m_ref - m_new) : 1.f;
-#pragma unroll
+#pragma unroll 1
           for (int ch = 0; ch < D / 32; ++ch) {
             uint32_t o[32];
             dev::tmem_ld32(tmem + lane_base + 256u + ch * 32, o);
@@ -349,29 +348,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float ls[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) ls[u] = 0.f;
-      const uint32_t pb = SL::p + (j & 1) * SL::kP + r * 128;
+      const uint32_t prow = SL::p + (j & 1) * SL::kP + r * 128;
+#pragma unroll 1
+      for (int ch = 0; ch < kTcKeys / 32; ++ch) {
+        uint32_t x[32];
+        dev::tmem_ld32(sbase + ch * 32, x);
+        dev::tmem_wait_ld();
+        const int lc = whole ? 32 : lim - ch * 32;
+        uint32_t pk[16];
 #pragma unroll
-      for (int c16 = 0; c16 < kTcKeys / 8; ++c16) {  // 16-byte chunks of 8 keys
-        uint32_t pk[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c = 8 * c16 + 2 * e;
-          float p0 = dev::ex2(fmaf(__uint_as_float(sv[c]), a.scale_log2, -m_ref));
-          float p1 = dev::ex2(fmaf(__uint_as_float(sv[c + 1]), a.scale_log2, -m_ref));
-          if (!whole) {
-            p0 = c <= lim ? p0 : 0.f;
-            p1 = c + 1 <= lim ? p1 : 0.f;
-          }
+        for (int e = 0; e < 16; ++e) {
+          float p0 = dev::ex2(fmaf(__uint_as_float(x[2 * e]), a.scale_log2, -m_ref));
+          float p1 = dev::ex2(fmaf(__uint_as_float(x[2 * e + 1]), a.scale_log2, -m_ref));
+          p0 = 2 * e <= lc ? p0 : 0.f;
+          p1 = 2 * e + 1 <= lc ? p1 : 0.f;
           pk[e] = dev::pack_bf16x2(p0, p1);
           // sum what the tensor cores multiply: with a stale reference max the largest
           // P is not a power of two, and only this keeps the weights a convex combination
           ls[(2 * e) & 7] += dev::bf16lo_to_f32(pk[e]);
           ls[(2 * e + 1) & 7] += dev::bf16hi_to_f32(pk[e]);
         }
-        *reinterpret_cast<uint4 *>(bp + pb + (c16 >> 3) * SL::kSub + (((c16 & 7) ^ (r & 7)) << 4)) =
-            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        const uint32_t dst = prow + (ch >> 1) * SL::kSub;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c16 = (ch & 1) * 4 + u;
+          *reinterpret_cast<uint4 *>(bp + dst + ((c16 ^ (r & 7)) << 4)) =
+              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
       }
       lsum += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      // S read: the MMA warp may refill this buffer
+      dev::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) dev::mbar_arrive(s_free(j & 1));
       if (nk < kTcKeys) {  // last block: V rows past the keys hold stale or unowned data
         const int s = j % KS;
         if (!(ok = __all_sync(0xffffffffu, dev::mbar_wait(v_full(s), (j / KS) & 1)))) break;
@@ -394,7 +403,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float inv = 1.f / lsum;
       uint4 *dst = reinterpret_cast<uint4 *>(
           a.out + ((int64_t)(q0 + qi) * a.num_q_heads + g * G + h) * D);
-#pragma unroll
+#pragma unroll 1
       for (int ch = 0; ch < D / 32; ++ch) {
         uint32_t o[32];
         dev::tmem_ld32(tmem + lane_base + 256u + ch * 32, o);
