@@ -354,6 +354,23 @@ def run_ours(args, w) -> None:
     t_step = timed(*g_step)
     clk = clocks.stop()
     t_dec = timed(*g_dec)
+
+    # spread of the step time: 200 replays of the R-step graph, each timed by its own
+    # events on the stream (outside the timed region above)
+    def spread(full, n=200):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        with torch.cuda.stream(stream):
+            evs[0].record(stream)
+            for i in range(n):
+                full.replay()
+                evs[i + 1].record(stream)
+        torch.cuda.synchronize()
+        per = sorted(evs[i].elapsed_time(evs[i + 1]) * 1e3 / R for i in range(n))
+        pick = lambda f: per[min(n - 1, int(f * n))]
+        return {"p10_us": pick(0.1), "p50_us": pick(0.5), "p90_us": pick(0.9), "samples": n,
+                "steps_per_sample": R}
+
+    step_spread = spread(g_step[0])
     t_step_max = reduce_max(t_step, world, device)
     bytes_all = reduce_sum(nb["step"] * args.steps, world, device)
     value = bytes_all / t_step_max / 1e9
@@ -443,6 +460,7 @@ def run_ours(args, w) -> None:
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": config_dict(w, inp, args, world),
         "hbm_frac_of_peak": value / peak,
+        "spread": step_spread,
         "plan": {"partition_tokens": P, "n_parts": math.ceil(max_len / P), "path": path,
                  "pool_copies": R},
         "roofline": {"bound": "hbm", "kernel": decode_name,
