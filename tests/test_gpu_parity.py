@@ -709,6 +709,64 @@ def test_prefill_wide_scores_and_full_tiles(B, oracle, D, BS, Hq, Hkv):
     assert_no_device_errors(B)
 
 
+@pytest.mark.parametrize("wid", [2, 3, 4, 5])
+def test_workload_prefill_sampled(B, oracle, wid):
+    """Prefill of the last min(L, 512) tokens of every sequence at the workload's full size
+    (the configuration bench.py --kernel prefill times).  Sampled against the oracle: the
+    last 8 query rows of four sequences; the oracle runs just those 8 queries, which sit at
+    the same positions."""
+    import itertools
+    w = W.WORKLOADS[wid]
+    inp = W.make_inputs(w, poison=True)
+    Bn, Hq, D = inp["q"].shape
+    lens = inp["context_lens"].long()
+    chunks = torch.clamp(lens, max=512)
+    qs = torch.tensor([0] + list(itertools.accumulate(chunks.tolist())), dtype=torch.int32)
+    gen = torch.Generator().manual_seed(70 + wid)
+    q = torch.randn(int(qs[-1]), Hq, D, generator=gen).to(torch.bfloat16)
+    g = dev(inp)
+    out = torch.full((int(qs[-1]), Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    B.paged_prefill_attention(out, q.cuda(), g["k_cache"], g["v_cache"], g["block_tables"],
+                              g["context_lens"], inp["max_context_len"], qs.cuda(),
+                              int(chunks.max()), inp["scale"])
+    torch.cuda.synchronize()
+    assert_no_device_errors(B)
+    got = out.cpu()
+    assert torch.isfinite(got.float()).all(), "a query row was not written"
+    for b in sorted({0, Bn // 3, (2 * Bn) // 3, Bn - 1}):
+        n = min(8, int(chunks[b]))
+        rows = slice(int(qs[b + 1]) - n, int(qs[b + 1]))
+        ref = oracle.prefill(q[rows], inp["k_cache"], inp["v_cache"], inp["block_tables"][b:b + 1],
+                             inp["context_lens"][b:b + 1],
+                             torch.tensor([0, n], dtype=torch.int32), inp["scale"])
+        check_attention(got[rows], ref, f"{w.name} sequence {b}")
+
+
+@pytest.mark.parametrize("wid", [2, 4])
+def test_workload_decode_step_rope(B, oracle, wid):
+    """paged_decode_step_rope at the workload's full size (bench.py --kernel rope_step):
+    q and both caches bit for bit, every output within tolerance."""
+    w = W.WORKLOADS[wid]
+    inp = W.make_inputs(w, poison=True)
+    D = inp["q"].shape[2]
+    pos = (inp["context_lens"].long() - 1).clamp(min=0)
+    cs = rope_table(inp["max_context_len"] + 1, D).float()
+    kc, vc, qr = oracle.kv_write_rope(inp["k_new"], inp["v_new"], inp["slot_mapping"], pos, cs,
+                                      inp["k_cache"], inp["v_cache"], q=inp["q"])
+    ref = oracle.decode(qr, kc, vc, inp["block_tables"], inp["context_lens"], inp["scale"])
+    g = dev(inp)
+    out = torch.empty_like(g["q"])
+    B.paged_decode_step_rope(out, g["q"], g["k_new"], g["v_new"], g["slot_mapping"], pos.cuda(),
+                             cs.cuda(), g["k_cache"], g["v_cache"], g["block_tables"],
+                             g["context_lens"], g["max_context_len"], g["scale"])
+    torch.cuda.synchronize()
+    assert_no_device_errors(B)
+    assert torch.equal(g["q"].cpu().view(torch.int16), qr.view(torch.int16))
+    assert torch.equal(g["k_cache"].cpu().view(torch.int16), kc.view(torch.int16))
+    assert torch.equal(g["v_cache"].cpu().view(torch.int16), vc.view(torch.int16))
+    check_attention(out, ref, f"{w.name} rope step")
+
+
 def test_prefill_single_token_chunks_equal_decode(B, oracle):
     """A chunk of one token per sequence is a decode step."""
     w = W.small_workload(B=3, Hq=32, Hkv=8, D=64, BS=16, lens=(5, 900, 2048), seed=51, write="none")
