@@ -99,6 +99,41 @@ def test_workload_fused_step_entry_point(B, oracle, wid):
     check_attention(out, ref, w.name + " (paged_decode_step)")
 
 
+@pytest.mark.parametrize("D,Hq,Hkv,lens,path", [
+    (64, 8, 2, (1500, 700), "cluster"),
+    (128, 24, 8, (5000, 4100, 300, 9000), "partitions"),
+    (64, 4, 4, (100, 37), "partitions"),
+])
+def test_step_writes_inside_the_range(B, oracle, D, Hq, Hkv, lens, path):
+    """paged_decode_step whose slots land inside the sequences' ranges, not only at their
+    ends (a block read by the first chunk of a partition, a block in the middle): the
+    decode reads blocks the write does not touch before that grid finishes, and must
+    read the touched ones after it."""
+    w = W.small_workload(B=len(lens), Hq=Hq, Hkv=Hkv, D=D, BS=16, lens=lens, seed=81 + D,
+                         write="none")
+    inp = W.make_inputs(w, poison=True)
+    want = {"cluster": B.PATH_CLUSTER, "partitions": B.PATH_PARTITIONS}[path]
+    assert B.paged_decode_path(w.B, Hq, Hkv, D, inp["max_context_len"]) == want
+    tb = inp["block_tables"]
+    slot = lambda b, t: int(tb[b, t // 16]) * 16 + t % 16
+    slots = [slot(0, 5), slot(0, lens[0] // 2), slot(1, lens[1] - 1), -1, slot(0, lens[0] - 1)]
+    gen = torch.Generator().manual_seed(82)
+    T = len(slots)
+    kn = torch.randn(T, Hkv, D, generator=gen).to(torch.bfloat16)
+    vn = torch.randn(T, Hkv, D, generator=gen).to(torch.bfloat16)
+    sm = torch.tensor(slots, dtype=torch.int64)
+    kc, vc = oracle.kv_write(kn, vn, sm, inp["k_cache"], inp["v_cache"])
+    ref = oracle.decode(inp["q"], kc, vc, tb, inp["context_lens"], inp["scale"])
+    g = dev(inp)
+    out = torch.empty_like(g["q"])
+    B.paged_decode_step(out, g["q"], kn.cuda(), vn.cuda(), sm.cuda(), g["k_cache"], g["v_cache"],
+                        g["block_tables"], g["context_lens"], g["max_context_len"], g["scale"])
+    torch.cuda.synchronize()
+    assert_no_device_errors(B)
+    assert torch.equal(g["k_cache"].cpu().view(torch.int16), kc.view(torch.int16))
+    check_attention(out, ref, f"writes inside the range ({path})")
+
+
 @pytest.mark.parametrize("wid", [2, 5])
 def test_workload_explicit_partition(B, oracle, wid):
     """The workload's own partition size (512 tokens for the long-context case) through the
