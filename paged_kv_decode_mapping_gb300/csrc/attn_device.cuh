@@ -1,8 +1,7 @@
-// attn_device.cuh -- device pieces shared by the attention kernels (decode and
-// prefill): the per-translation-unit error word, the consumer-warp barrier, the
-// swizzled stage layout and the TMA box issue of one KV block.  Included by each
-// attention .cu file; every includer gets its own error word, read through
-// read_tu_errors().
+// attn_device.cuh -- device pieces of the attention kernels: the per-translation-unit
+// error word (decode and prefill; every includer gets its own, read through
+// read_tu_errors()), and for the decode kernels the consumer-warp barrier, the
+// swizzled stage layout and the TMA box issue of one KV block.
 #pragma once
 
 #include <cuda.h>

@@ -53,7 +53,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kMaxDevices = 64;
 
-// Stages of the TMA ring and the dynamic shared memory of one attention CTA.
+// Stages of the TMA ring and the dynamic shared memory of one decode CTA.
 constexpr int split_stages(int d) { return d == 64 ? 4 : 3; }
 constexpr size_t split_smem(int d) {
   return 1024 + (size_t)split_stages(d) * 2 * kChunk * d * 2 + split_stages(d) * 16 + 16;
