@@ -439,10 +439,380 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 0) dev::tmem_dealloc(tmem, 512);
 }
 
+// ===========================================================================
+// prefill_tc2_kernel: head_dim 64, two query tiles per CTA in ping-pong.
+//
+// At head_dim 64 the softmax is heavy against the tensor work, so a CTA owns 256 query
+// rows as two 128-row tiles of the same (sequence, kv head): softmax warpgroup t (warps
+// 4t .. 4t+3) owns tile t.  The tensor-core thread issues PV_0(j), S_0(j+1), PV_1(j),
+// S_1(j+1), so while one warpgroup works on its S the tensor core works on the other
+// tile, and every K/V block staged feeds 256 rows.  Each tile has one S buffer and one
+// P buffer: S_t(j+1) is issued only once the softmax has released S_t(j) (p_full), and
+// the commit that announces S_t(j+1) covers every earlier tensor-core operation,
+// including PV_t(j), so when a tile's next S arrives its O is stable and its P free.
+// Row arithmetic (positions, masking, lazy rescale, bf16 row sums) is the one-tile
+// kernel's.
+constexpr int kTc2Threads = 320;  // softmax warpgroups 0 and 1, producer warp 8, MMA warp 9
+
+struct Tc2Smem {
+  static constexpr int KS = 3;                       // stages of each ring
+  static constexpr uint32_t kSub = kTcKeys * 128;    // 128 rows x 128 B
+  static constexpr uint32_t kTile = kSub;            // one K or V block / one Q tile (D = 64)
+  static constexpr uint32_t k = 0;
+  static constexpr uint32_t v = k + KS * kTile;
+  static constexpr uint32_t q = v + KS * kTile;      // two Q tiles
+  static constexpr uint32_t p = q + 2 * kTile;       // two P buffers [2][128 rows][128 B]
+  static constexpr uint32_t kP = 2 * kSub;
+  static constexpr uint32_t bars = p + 2 * kP;
+  static constexpr int kBars = 4 * KS + 8;
+  static constexpr uint32_t tslot = bars + kBars * 8;
+  static constexpr uint32_t flag = tslot + 8;
+  static constexpr uint32_t total = flag + 8;
+};
+
+__global__ void __launch_bounds__(kTc2Threads, 1)
+    prefill_tc2_kernel(const __grid_constant__ CUtensorMap tmk,
+                       const __grid_constant__ CUtensorMap tmv, const PrefillArgs a) {
+  constexpr int D = 64;
+  using SL = Tc2Smem;
+  constexpr int KS = SL::KS;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = dev::smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t *const bp = smem_raw + (base - raw);
+  const uint32_t bars = base + SL::bars;
+  auto k_full = [&](int s) { return bars + 8u * s; };
+  auto k_empty = [&](int s) { return bars + 8u * (KS + s); };
+  auto v_full = [&](int s) { return bars + 8u * (2 * KS + s); };
+  auto v_empty = [&](int s) { return bars + 8u * (3 * KS + s); };
+  auto s_full = [&](int t) { return bars + 8u * (4 * KS + t); };
+  auto p_full = [&](int t) { return bars + 8u * (4 * KS + 2 + t); };
+  auto pv_done = [&](int t) { return bars + 8u * (4 * KS + 4 + t); };
+  const uint32_t q_ready = bars + 8u * (4 * KS + 6);
+  const uint32_t mma_done = bars + 8u * (4 * KS + 7);
+  volatile uint32_t *const s_tmem = reinterpret_cast<volatile uint32_t *>(bp + SL::tslot);
+  volatile int *const s_flag = reinterpret_cast<volatile int *>(bp + SL::flag);
+
+  const int tile = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = a.group;
+
+  int L = __ldg(a.context_lens + b);
+  const int q0 = __ldg(a.query_start + b);
+  int n = __ldg(a.query_start + b + 1) - q0;
+  if (L < 0 || L > a.cap || n < 0 || n > L) {
+    if (tid == 0 && tile == 0) raise_error(PKV_DEVERR_CONTEXT_LEN);
+    L = L < 0 ? 0 : (L > a.cap ? a.cap : L);
+    n = n < 0 ? 0 : (n > L ? L : n);
+  }
+  const int rows = n * G;
+  const int row0 = tile * 2 * kTcRows;
+  if (row0 >= rows) return;
+  // per tile: its last row, the keys it needs [0, t_end_t), its blocks
+  int t_end_t[2], nblk_t[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int first = row0 + t * kTcRows;
+    if (first >= rows) {
+      t_end_t[t] = 0;
+      nblk_t[t] = 0;
+    } else {
+      const int last = min(first + kTcRows, rows) - 1;
+      t_end_t[t] = L - n + last / G + 1;
+      nblk_t[t] = (t_end_t[t] + kTcKeys - 1) / kTcKeys;
+    }
+  }
+  const int t_end = max(t_end_t[0], t_end_t[1]);  // keys the CTA stages
+  const int nblk = max(nblk_t[0], nblk_t[1]);
+  auto nblk_of = [&](int t) { return t ? nblk_t[1] : nblk_t[0]; };
+
+  if (tid == 0) {
+    for (int i = 0; i < SL::kBars; ++i) {
+      const uint32_t bar = bars + 8u * i;
+      const bool per_warp = bar == p_full(0) || bar == p_full(1);
+      dev::mbar_init(bar, per_warp ? 4u : (bar == q_ready ? 8u : 1u));
+    }
+    *s_flag = 0;
+    dev::fence_mbar_init();
+  }
+  if (warp == 0) dev::tmem_alloc(base + SL::tslot, 512);
+  dev::tc_fence_before();
+  __syncthreads();
+  dev::tc_fence_after();
+  const uint32_t tmem = *s_tmem;  // S of tile t at column 128 t, O of tile t at 256 + 64 t
+
+  auto fail = [&](bool ok) {
+    if (!ok) {
+      raise_error(PKV_DEVERR_TIMEOUT);
+      *s_flag = 1;
+    }
+    return ok;
+  };
+  int k_issued = 0, v_issued = 0;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------- producer warp
+    const uint64_t policy = dev::policy_evict_last();
+    const int32_t *trow = a.block_tables + (int64_t)b * a.max_blocks;
+    const int lb_last = (t_end - 1) >> a.log2_bs;
+    int kwin = 0, vwin = 0;
+    int ktb = (lane <= lb_last) ? __ldg(trow + lane) : 0;
+    int vtb = ktb;
+    for (int j = 0; j <= nblk; ++j) {  // K runs one block ahead of V
+      if (j < nblk) {
+        const int s = j % KS;
+        if (j >= KS && !__all_sync(0xffffffffu, dev::mbar_wait(k_empty(s), ((j / KS) - 1) & 1))) {
+          if (lane == 0) fail(false);
+          break;
+        }
+        tc_load_block<D>(&tmk, base + SL::k + s * SL::kTile, k_full(s), j * kTcKeys,
+                         min(kTcKeys, t_end - j * kTcKeys), kwin, ktb, trow, lb_last, a, g, lane,
+                         policy);
+        k_issued = j + 1;
+      }
+      if (j >= 1) {
+        const int jv = j - 1, s = jv % KS;
+        if (jv >= KS && !__all_sync(0xffffffffu, dev::mbar_wait(v_empty(s), ((jv / KS) - 1) & 1))) {
+          if (lane == 0) fail(false);
+          break;
+        }
+        tc_load_block<D>(&tmv, base + SL::v + s * SL::kTile, v_full(s), jv * kTcKeys,
+                         min(kTcKeys, t_end - jv * kTcKeys), vwin, vtb, trow, lb_last, a, g, lane,
+                         policy);
+        v_issued = jv + 1;
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------- tensor-core issue (one thread)
+    if (lane == 0) {
+      constexpr uint32_t id_s = dev::idesc_bf16_f32(kTcRows, kTcKeys, 0);
+      constexpr uint32_t id_o = dev::idesc_bf16_f32(kTcRows, D, 1);
+      bool ok = fail(dev::mbar_wait(q_ready, 0));
+      int k_waited = 0;  // K blocks whose k_full this thread has seen
+      auto need_k = [&](int j) {
+        if (j < k_waited) return true;
+        if (!fail(dev::mbar_wait(k_full(j % KS), (j / KS) & 1))) return false;
+        k_waited = j + 1;
+        dev::tc_fence_after();
+        return true;
+      };
+      auto issue_s = [&](int t, int j) {
+        const uint32_t kt = base + SL::k + (j % KS) * SL::kTile;
+        const uint32_t qt = base + SL::q + t * SL::kTile;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          dev::umma_bf16(tmem + 128u * t, dev::smem_desc(qt + ks * 32, 16, 1024),
+                         dev::smem_desc(kt + ks * 32, 16, 1024), id_s, ks > 0 ? 1u : 0u);
+        dev::umma_commit(s_full(t));
+        // K_j is free once the last tile that reads it has its S
+        if (t == 1 || j >= nblk_of(1)) dev::umma_commit(k_empty(j % KS));
+      };
+      if (ok && (ok = need_k(0))) {
+        issue_s(0, 0);
+        if (nblk_of(1) > 0) issue_s(1, 0);
+      }
+      for (int j = 0; ok && j < nblk; ++j) {
+        bool v_seen = false;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j >= nblk_of(t)) continue;
+          if (!(ok = fail(dev::mbar_wait(p_full(t), j & 1)))) break;
+          if (!v_seen) {
+            if (!(ok = fail(dev::mbar_wait(v_full(j % KS), (j / KS) & 1)))) break;
+            v_seen = true;
+          }
+          dev::tc_fence_after();
+          const uint32_t vt = base + SL::v + (j % KS) * SL::kTile;
+          const uint32_t pb = base + SL::p + t * SL::kP;
+#pragma unroll
+          for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+            const uint32_t poff = (kk >> 2) * SL::kSub + (kk & 3) * 32;
+            dev::umma_bf16(tmem + 256u + 64u * t, dev::smem_desc(pb + poff, 16, 1024),
+                           dev::smem_desc(vt + kk * 2048u, SL::kSub, 1024), id_o,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          dev::umma_commit(pv_done(t));
+          if (j + 1 < nblk_of(t)) {
+            if (!(ok = need_k(j + 1))) break;
+            issue_s(t, j + 1);
+          }
+        }
+        if (ok) dev::umma_commit(v_empty(j % KS));
+      }
+      dev::umma_commit(mma_done);
+    }
+  } else {
+    // ------------------------------------------------- softmax warpgroup t, row = lane
+    const int t = warp >> 2;
+    const int r = 32 * (warp & 3) + lane;
+    const int gr = row0 + t * kTcRows + r;
+    const bool valid = gr < rows;
+    const int last_row_t = min(row0 + t * kTcRows + kTcRows, rows) - 1;
+    const int qi = valid ? gr / G : (last_row_t >= 0 ? last_row_t / G : 0);
+    const int h = valid ? gr - (gr / G) * G : 0;
+    const int pos = L - n + qi;
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const uint32_t sb = tmem + lane_base + 128u * t;
+    const uint32_t ob = tmem + lane_base + 256u + 64u * t;
+    {  // this tile's query rows (zeros past the end)
+      const uint4 *src = reinterpret_cast<const uint4 *>(
+          a.q + ((int64_t)(q0 + qi) * a.num_q_heads + g * G + h) * D);
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) {
+        const uint4 v = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4 *>(bp + SL::q + t * SL::kTile + r * 128 + ((c ^ (r & 7)) << 4)) = v;
+      }
+      dev::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) dev::mbar_arrive(q_ready);
+    }
+    const int nb = nblk_of(t);
+    const int te = t ? t_end_t[1] : t_end_t[0];
+    float m_ref = -INFINITY, lsum = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nb; ++j) {
+      const int k0 = j * kTcKeys;
+      const int lim = min(pos, te - 1) - k0;
+      if (!(ok = __all_sync(0xffffffffu, dev::mbar_wait(s_full(t), j & 1)))) break;
+      dev::tc_fence_after();
+      const bool whole = __all_sync(0xffffffffu, lim >= kTcKeys - 1);
+      float mx[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
+#pragma unroll 1
+      for (int ch = 0; ch < kTcKeys / 32; ++ch) {
+        uint32_t x[32];
+        dev::tmem_ld32(sb + ch * 32, x);
+        dev::tmem_wait_ld();
+        const int lc = lim - ch * 32;
+        if (whole) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(x[i]) * a.scale_log2);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            mx[i & 7] = fmaxf(mx[i & 7], i <= lc ? __uint_as_float(x[i]) * a.scale_log2 : -INFINITY);
+        }
+      }
+      const float bmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      // S_t(j) arrived: every earlier tensor-core operation, PV_t(j-1) included, is done,
+      // so O_t is stable and the P buffer free
+      if (j > 0) {
+        const bool need = bmax > m_ref + kTcRescale;
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_new = fmaxf(m_ref, bmax);
+          const float f = need ? dev::ex2(m_ref - m_new) : 1.f;
+#pragma unroll 1
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t o[32];
+            dev::tmem_ld32(ob + ch * 32, o);
+            dev::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+            dev::tmem_st32(ob + ch * 32, o);
+          }
+          dev::tmem_wait_st();
+          lsum *= f;
+          if (need) m_ref = m_new;
+        }
+      } else {
+        m_ref = bmax;
+      }
+      float ls[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) ls[u] = 0.f;
+      const uint32_t prow = SL::p + t * SL::kP + r * 128;
+#pragma unroll 1
+      for (int ch = 0; ch < kTcKeys / 32; ++ch) {
+        uint32_t x[32];
+        dev::tmem_ld32(sb + ch * 32, x);
+        dev::tmem_wait_ld();
+        const int lc = whole ? 32 : lim - ch * 32;
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float p0 = dev::ex2(fmaf(__uint_as_float(x[2 * e]), a.scale_log2, -m_ref));
+          float p1 = dev::ex2(fmaf(__uint_as_float(x[2 * e + 1]), a.scale_log2, -m_ref));
+          p0 = 2 * e <= lc ? p0 : 0.f;
+          p1 = 2 * e + 1 <= lc ? p1 : 0.f;
+          pk[e] = dev::pack_bf16x2(p0, p1);
+          ls[(2 * e) & 7] += dev::bf16lo_to_f32(pk[e]);
+          ls[(2 * e + 1) & 7] += dev::bf16hi_to_f32(pk[e]);
+        }
+        const uint32_t dst = prow + (ch >> 1) * SL::kSub;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c16 = (ch & 1) * 4 + u;
+          *reinterpret_cast<uint4 *>(bp + dst + ((c16 ^ (r & 7)) << 4)) =
+              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      }
+      lsum += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      const int nk = min(kTcKeys, t_end - k0);  // keys the CTA staged in this block
+      if (nk < kTcKeys) {  // the CTA's last block: V rows past its keys are stale or unowned
+        const int s = j % KS;
+        if (!(ok = __all_sync(0xffffffffu, dev::mbar_wait(v_full(s), (j / KS) & 1)))) break;
+        const uint32_t vt = SL::v + s * SL::kTile;
+        for (int idx = r; idx < (kTcKeys - nk) * (D / 8); idx += kTcRows) {
+          const int row = nk + idx / (D / 8), c = idx % (D / 8);
+          *reinterpret_cast<uint4 *>(bp + vt + row * 128 + ((c ^ (row & 7)) << 4)) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      dev::tc_fence_before();
+      dev::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) dev::mbar_arrive(p_full(t));
+    }
+    if (!ok && lane == 0) fail(false);
+    if (ok && nb > 0 && __all_sync(0xffffffffu, dev::mbar_wait(pv_done(t), (nb - 1) & 1))) {
+      dev::tc_fence_after();
+      const float inv = 1.f / lsum;
+      uint4 *dst = reinterpret_cast<uint4 *>(
+          a.out + ((int64_t)(q0 + qi) * a.num_q_heads + g * G + h) * D);
+#pragma unroll 1
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t o[32];
+        dev::tmem_ld32(ob + ch * 32, o);
+        dev::tmem_wait_ld();
+        if (valid) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w4[e] = dev::pack_bf16x2(__uint_as_float(o[8 * u + 2 * e]) * inv,
+                                       __uint_as_float(o[8 * u + 2 * e + 1]) * inv);
+            dst[ch * 4 + u] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
+        }
+      }
+    } else if (ok && nb > 0 && lane == 0) {
+      fail(false);
+    }
+  }
+
+  if (tid == 0) (void)dev::mbar_wait(mma_done, 0);
+  if (warp == 8 && lane == 0 && *s_flag) {
+    for (int s = 0; s < KS; ++s) {
+      const int kl = s + ((k_issued - 1 - s) / KS) * KS;
+      if (kl >= 0 && kl < k_issued) (void)dev::mbar_wait(k_full(s), (kl / KS) & 1);
+      const int vl = s + ((v_issued - 1 - s) / KS) * KS;
+      if (vl >= 0 && vl < v_issued) (void)dev::mbar_wait(v_full(s), (vl / KS) & 1);
+    }
+  }
+  dev::tc_fence_before();
+  __syncthreads();
+  dev::tc_fence_after();
+  if (warp == 0) dev::tmem_dealloc(tmem, 512);
+}
+
 cudaError_t read_prefill_errors(uint32_t *flags, int clear) { return read_tu_errors(flags, clear); }
 
 constexpr size_t tc_smem(int d) { return 1024 + (d == 64 ? TcSmem<64>::total : TcSmem<128>::total); }
 static_assert(tc_smem(64) <= 227 * 1024 && tc_smem(128) <= 227 * 1024, "prefill tile fits a CTA");
+constexpr size_t tc2_smem() { return 1024 + Tc2Smem::total; }
+static_assert(tc2_smem() <= 227 * 1024, "two prefill tiles fit a CTA");
 
 namespace {
 bool g_prefill_attr[kMaxDevices][2];  // dynamic smem attribute of prefill_kernel set
@@ -471,7 +841,9 @@ PKV_API int paged_prefill_attention(pkv_bf16 *out, const pkv_bf16 *q, const pkv_
   if (!aligned16(out))
     return set_error(PKV_ERR_ALIGN, "paged_prefill_attention: out must be 16-byte aligned");
   const int G = num_q_heads / cache->num_kv_heads;
-  const int64_t tiles = ((int64_t)max_query_len * G + kTcRows - 1) / kTcRows;
+  // head_dim 64: two 128-row tiles per CTA (prefill_tc2_kernel); 128: one
+  const int64_t rows_per_cta = cache->head_dim == 64 ? 2 * kTcRows : kTcRows;
+  const int64_t tiles = ((int64_t)max_query_len * G + rows_per_cta - 1) / rows_per_cta;
   if (tiles > 0x7fffffffLL) return set_error(PKV_ERR_UNSUPPORTED, "paged_prefill_attention: too many query rows");
   CUtensorMap tmk, tmv;
   const int D = cache->head_dim;
@@ -482,9 +854,9 @@ PKV_API int paged_prefill_attention(pkv_bf16 *out, const pkv_bf16 *q, const pkv_
     if ((rc = current_device(&dev))) return rc;
     const int vi = D == 64 ? 0 : 1;
     if (!g_prefill_attr[dev][vi]) {
-      cudaError_t e = D == 64 ? cudaFuncSetAttribute(prefill_tc_kernel<64>,
+      cudaError_t e = D == 64 ? cudaFuncSetAttribute(prefill_tc2_kernel,
                                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     (int)tc_smem(64))
+                                                     (int)tc2_smem())
                               : cudaFuncSetAttribute(prefill_tc_kernel<128>,
                                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                      (int)tc_smem(128));
@@ -511,7 +883,7 @@ PKV_API int paged_prefill_attention(pkv_bf16 *out, const pkv_bf16 *q, const pkv_
   dim3 grid((unsigned)tiles, (unsigned)cache->num_kv_heads, (unsigned)num_seqs);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (D == 64)
-    prefill_tc_kernel<64><<<grid, kTcThreads, tc_smem(64), s>>>(tmk, tmv, a);
+    prefill_tc2_kernel<<<grid, kTc2Threads, tc2_smem(), s>>>(tmk, tmv, a);
   else
     prefill_tc_kernel<128><<<grid, kTcThreads, tc_smem(128), s>>>(tmk, tmv, a);
   cudaError_t e = cudaGetLastError();
