@@ -454,42 +454,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // kernel's.
 constexpr int kTc2Threads = 320;  // softmax warpgroups 0 and 1, producer warp 8, MMA warp 9
 
+template <int D>
 struct Tc2Smem {
-  static constexpr int KS = 3;                       // stages of each ring
-  static constexpr uint32_t kSub = kTcKeys * 128;    // 128 rows x 128 B
-  static constexpr uint32_t kTile = kSub;            // one K or V block / one Q tile (D = 64)
+  static constexpr int KSK = D == 64 ? 3 : 2;        // stages of the K ring
+  static constexpr int KSV = D == 64 ? 3 : 1;        // stages of the V ring
+  static constexpr uint32_t kSub = kTcKeys * 128;    // 128 rows x 128 B (64 dims)
+  static constexpr uint32_t kTile = kSub * (D / 64); // one K or V block / one Q tile
   static constexpr uint32_t k = 0;
-  static constexpr uint32_t v = k + KS * kTile;
-  static constexpr uint32_t q = v + KS * kTile;      // two Q tiles
+  static constexpr uint32_t v = k + KSK * kTile;
+  static constexpr uint32_t q = v + KSV * kTile;     // two Q tiles
   static constexpr uint32_t p = q + 2 * kTile;       // two P buffers [2][128 rows][128 B]
   static constexpr uint32_t kP = 2 * kSub;
   static constexpr uint32_t bars = p + 2 * kP;
-  static constexpr int kBars = 4 * KS + 8;
+  static constexpr int kBars = 2 * KSK + 2 * KSV + 8;
   static constexpr uint32_t tslot = bars + kBars * 8;
   static constexpr uint32_t flag = tslot + 8;
   static constexpr uint32_t total = flag + 8;
 };
 
+template <int D>
 __global__ void __launch_bounds__(kTc2Threads, 1)
     prefill_tc2_kernel(const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, const PrefillArgs a) {
-  constexpr int D = 64;
-  using SL = Tc2Smem;
-  constexpr int KS = SL::KS;
+  using SL = Tc2Smem<D>;
+  constexpr int KSK = SL::KSK, KSV = SL::KSV;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = dev::smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *const bp = smem_raw + (base - raw);
   const uint32_t bars = base + SL::bars;
+  constexpr int R4 = 2 * KSK + 2 * KSV;  // barriers of the two rings
   auto k_full = [&](int s) { return bars + 8u * s; };
-  auto k_empty = [&](int s) { return bars + 8u * (KS + s); };
-  auto v_full = [&](int s) { return bars + 8u * (2 * KS + s); };
-  auto v_empty = [&](int s) { return bars + 8u * (3 * KS + s); };
-  auto s_full = [&](int t) { return bars + 8u * (4 * KS + t); };
-  auto p_full = [&](int t) { return bars + 8u * (4 * KS + 2 + t); };
-  auto pv_done = [&](int t) { return bars + 8u * (4 * KS + 4 + t); };
-  const uint32_t q_ready = bars + 8u * (4 * KS + 6);
-  const uint32_t mma_done = bars + 8u * (4 * KS + 7);
+  auto k_empty = [&](int s) { return bars + 8u * (KSK + s); };
+  auto v_full = [&](int s) { return bars + 8u * (2 * KSK + s); };
+  auto v_empty = [&](int s) { return bars + 8u * (2 * KSK + KSV + s); };
+  auto s_full = [&](int t) { return bars + 8u * (R4 + t); };
+  auto p_full = [&](int t) { return bars + 8u * (R4 + 2 + t); };
+  auto pv_done = [&](int t) { return bars + 8u * (R4 + 4 + t); };
+  const uint32_t q_ready = bars + 8u * (R4 + 6);
+  const uint32_t mma_done = bars + 8u * (R4 + 7);
   volatile uint32_t *const s_tmem = reinterpret_cast<volatile uint32_t *>(bp + SL::tslot);
   volatile int *const s_flag = reinterpret_cast<volatile int *>(bp + SL::flag);
 
@@ -539,7 +542,7 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
   dev::tc_fence_before();
   __syncthreads();
   dev::tc_fence_after();
-  const uint32_t tmem = *s_tmem;  // S of tile t at column 128 t, O of tile t at 256 + 64 t
+  const uint32_t tmem = *s_tmem;  // S of tile t at column 128 t, O of tile t at 256 + D t
 
   auto fail = [&](bool ok) {
     if (!ok) {
@@ -560,8 +563,8 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
     int vtb = ktb;
     for (int j = 0; j <= nblk; ++j) {  // K runs one block ahead of V
       if (j < nblk) {
-        const int s = j % KS;
-        if (j >= KS && !__all_sync(0xffffffffu, dev::mbar_wait(k_empty(s), ((j / KS) - 1) & 1))) {
+        const int s = j % KSK;
+        if (j >= KSK && !__all_sync(0xffffffffu, dev::mbar_wait(k_empty(s), ((j / KSK) - 1) & 1))) {
           if (lane == 0) fail(false);
           break;
         }
@@ -571,8 +574,8 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
         k_issued = j + 1;
       }
       if (j >= 1) {
-        const int jv = j - 1, s = jv % KS;
-        if (jv >= KS && !__all_sync(0xffffffffu, dev::mbar_wait(v_empty(s), ((jv / KS) - 1) & 1))) {
+        const int jv = j - 1, s = jv % KSV;
+        if (jv >= KSV && !__all_sync(0xffffffffu, dev::mbar_wait(v_empty(s), ((jv / KSV) - 1) & 1))) {
           if (lane == 0) fail(false);
           break;
         }
@@ -591,21 +594,23 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
       int k_waited = 0;  // K blocks whose k_full this thread has seen
       auto need_k = [&](int j) {
         if (j < k_waited) return true;
-        if (!fail(dev::mbar_wait(k_full(j % KS), (j / KS) & 1))) return false;
+        if (!fail(dev::mbar_wait(k_full(j % KSK), (j / KSK) & 1))) return false;
         k_waited = j + 1;
         dev::tc_fence_after();
         return true;
       };
       auto issue_s = [&](int t, int j) {
-        const uint32_t kt = base + SL::k + (j % KS) * SL::kTile;
+        const uint32_t kt = base + SL::k + (j % KSK) * SL::kTile;
         const uint32_t qt = base + SL::q + t * SL::kTile;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          dev::umma_bf16(tmem + 128u * t, dev::smem_desc(qt + ks * 32, 16, 1024),
-                         dev::smem_desc(kt + ks * 32, 16, 1024), id_s, ks > 0 ? 1u : 0u);
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * SL::kSub + (ks & 3) * 32;
+          dev::umma_bf16(tmem + 128u * t, dev::smem_desc(qt + off, 16, 1024),
+                         dev::smem_desc(kt + off, 16, 1024), id_s, ks > 0 ? 1u : 0u);
+        }
         dev::umma_commit(s_full(t));
         // K_j is free once the last tile that reads it has its S
-        if (t == 1 || j >= nblk_of(1)) dev::umma_commit(k_empty(j % KS));
+        if (t == 1 || j >= nblk_of(1)) dev::umma_commit(k_empty(j % KSK));
       };
       if (ok && (ok = need_k(0))) {
         issue_s(0, 0);
@@ -617,16 +622,16 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
           if (j >= nblk_of(t)) continue;
           if (!(ok = fail(dev::mbar_wait(p_full(t), j & 1)))) break;
           if (!v_seen) {
-            if (!(ok = fail(dev::mbar_wait(v_full(j % KS), (j / KS) & 1)))) break;
+            if (!(ok = fail(dev::mbar_wait(v_full(j % KSV), (j / KSV) & 1)))) break;
             v_seen = true;
           }
           dev::tc_fence_after();
-          const uint32_t vt = base + SL::v + (j % KS) * SL::kTile;
+          const uint32_t vt = base + SL::v + (j % KSV) * SL::kTile;
           const uint32_t pb = base + SL::p + t * SL::kP;
 #pragma unroll
           for (int kk = 0; kk < kTcKeys / 16; ++kk) {
             const uint32_t poff = (kk >> 2) * SL::kSub + (kk & 3) * 32;
-            dev::umma_bf16(tmem + 256u + 64u * t, dev::smem_desc(pb + poff, 16, 1024),
+            dev::umma_bf16(tmem + 256u + (uint32_t)(D * t), dev::smem_desc(pb + poff, 16, 1024),
                            dev::smem_desc(vt + kk * 2048u, SL::kSub, 1024), id_o,
                            (j > 0 || kk > 0) ? 1u : 0u);
           }
@@ -636,7 +641,7 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
             issue_s(t, j + 1);
           }
         }
-        if (ok) dev::umma_commit(v_empty(j % KS));
+        if (ok) dev::umma_commit(v_empty(j % KSV));
       }
       dev::umma_commit(mma_done);
     }
@@ -652,14 +657,15 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
     const int pos = L - n + qi;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const uint32_t sb = tmem + lane_base + 128u * t;
-    const uint32_t ob = tmem + lane_base + 256u + 64u * t;
+    const uint32_t ob = tmem + lane_base + 256u + (uint32_t)(D * t);
     {  // this tile's query rows (zeros past the end)
       const uint4 *src = reinterpret_cast<const uint4 *>(
           a.q + ((int64_t)(q0 + qi) * a.num_q_heads + g * G + h) * D);
 #pragma unroll
       for (int c = 0; c < D / 8; ++c) {
         const uint4 v = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4 *>(bp + SL::q + t * SL::kTile + r * 128 + ((c ^ (r & 7)) << 4)) = v;
+        *reinterpret_cast<uint4 *>(bp + SL::q + t * SL::kTile + (c >> 3) * SL::kSub + r * 128 +
+                                   (((c & 7) ^ (r & 7)) << 4)) = v;
       }
       dev::fence_proxy_async_smem();
       __syncwarp();
@@ -750,13 +756,13 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
       lsum += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       const int nk = min(kTcKeys, t_end - k0);  // keys the CTA staged in this block
       if (nk < kTcKeys) {  // the CTA's last block: V rows past its keys are stale or unowned
-        const int s = j % KS;
-        if (!(ok = __all_sync(0xffffffffu, dev::mbar_wait(v_full(s), (j / KS) & 1)))) break;
+        const int s = j % KSV;
+        if (!(ok = __all_sync(0xffffffffu, dev::mbar_wait(v_full(s), (j / KSV) & 1)))) break;
         const uint32_t vt = SL::v + s * SL::kTile;
         for (int idx = r; idx < (kTcKeys - nk) * (D / 8); idx += kTcRows) {
           const int row = nk + idx / (D / 8), c = idx % (D / 8);
-          *reinterpret_cast<uint4 *>(bp + vt + row * 128 + ((c ^ (row & 7)) << 4)) =
-              make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4 *>(bp + vt + (c >> 3) * SL::kSub + row * 128 +
+                                     (((c & 7) ^ (row & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
         }
       }
       dev::tc_fence_before();
@@ -794,11 +800,13 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
 
   if (tid == 0) (void)dev::mbar_wait(mma_done, 0);
   if (warp == 8 && lane == 0 && *s_flag) {
-    for (int s = 0; s < KS; ++s) {
-      const int kl = s + ((k_issued - 1 - s) / KS) * KS;
-      if (kl >= 0 && kl < k_issued) (void)dev::mbar_wait(k_full(s), (kl / KS) & 1);
-      const int vl = s + ((v_issued - 1 - s) / KS) * KS;
-      if (vl >= 0 && vl < v_issued) (void)dev::mbar_wait(v_full(s), (vl / KS) & 1);
+    for (int s = 0; s < KSK; ++s) {
+      const int kl = s + ((k_issued - 1 - s) / KSK) * KSK;
+      if (kl >= 0 && kl < k_issued) (void)dev::mbar_wait(k_full(s), (kl / KSK) & 1);
+    }
+    for (int s = 0; s < KSV; ++s) {
+      const int vl = s + ((v_issued - 1 - s) / KSV) * KSV;
+      if (vl >= 0 && vl < v_issued) (void)dev::mbar_wait(v_full(s), (vl / KSV) & 1);
     }
   }
   dev::tc_fence_before();
@@ -811,11 +819,14 @@ cudaError_t read_prefill_errors(uint32_t *flags, int clear) { return read_tu_err
 
 constexpr size_t tc_smem(int d) { return 1024 + (d == 64 ? TcSmem<64>::total : TcSmem<128>::total); }
 static_assert(tc_smem(64) <= 227 * 1024 && tc_smem(128) <= 227 * 1024, "prefill tile fits a CTA");
-constexpr size_t tc2_smem() { return 1024 + Tc2Smem::total; }
-static_assert(tc2_smem() <= 227 * 1024, "two prefill tiles fit a CTA");
+constexpr size_t tc2_smem(int d) {
+  return 1024 + (d == 64 ? Tc2Smem<64>::total : Tc2Smem<128>::total);
+}
+static_assert(tc2_smem(64) <= 227 * 1024 && tc2_smem(128) <= 227 * 1024,
+              "two prefill tiles fit a CTA");
 
 namespace {
-bool g_prefill_attr[kMaxDevices][2];  // dynamic smem attribute of prefill_kernel set
+bool g_prefill_attr[kMaxDevices][4];  // dynamic smem attribute set: [D 64/128][one/two tiles]
 }  // namespace
 
 }  // namespace pkv
@@ -841,9 +852,18 @@ PKV_API int paged_prefill_attention(pkv_bf16 *out, const pkv_bf16 *q, const pkv_
   if (!aligned16(out))
     return set_error(PKV_ERR_ALIGN, "paged_prefill_attention: out must be 16-byte aligned");
   const int G = num_q_heads / cache->num_kv_heads;
-  // head_dim 64: two 128-row tiles per CTA (prefill_tc2_kernel); 128: one
-  const int64_t rows_per_cta = cache->head_dim == 64 ? 2 * kTcRows : kTcRows;
-  const int64_t tiles = ((int64_t)max_query_len * G + rows_per_cta - 1) / rows_per_cta;
+  // Two 128-row tiles per CTA (prefill_tc2_kernel) when that still makes at least two
+  // waves of CTAs; otherwise one tile per CTA (prefill_tc_kernel), e.g. a few long
+  // sequences, where halving the CTAs would leave SMs idle.
+  const int64_t units = (int64_t)num_seqs * cache->num_kv_heads;
+  const int64_t tiles2 = ((int64_t)max_query_len * G + 2 * kTcRows - 1) / (2 * kTcRows);
+  int sms = 0;
+  {
+    std::lock_guard<std::mutex> lk(attn_mutex());
+    if ((rc = device_sms(&sms))) return rc;
+  }
+  const bool two = tiles2 * units >= 2 * (int64_t)sms;
+  const int64_t tiles = two ? tiles2 : ((int64_t)max_query_len * G + kTcRows - 1) / kTcRows;
   if (tiles > 0x7fffffffLL) return set_error(PKV_ERR_UNSUPPORTED, "paged_prefill_attention: too many query rows");
   CUtensorMap tmk, tmv;
   const int D = cache->head_dim;
@@ -852,14 +872,23 @@ PKV_API int paged_prefill_attention(pkv_bf16 *out, const pkv_bf16 *q, const pkv_
     if ((rc = maps_for(k_cache, v_cache, *cache, &tmk, &tmv))) return rc;
     int dev = 0;
     if ((rc = current_device(&dev))) return rc;
-    const int vi = D == 64 ? 0 : 1;
+    const int vi = (D == 64 ? 0 : 2) + (two ? 1 : 0);
     if (!g_prefill_attr[dev][vi]) {
-      cudaError_t e = D == 64 ? cudaFuncSetAttribute(prefill_tc2_kernel,
-                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     (int)tc2_smem())
-                              : cudaFuncSetAttribute(prefill_tc_kernel<128>,
-                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     (int)tc_smem(128));
+      cudaError_t e;
+      if (two)
+        e = D == 64 ? cudaFuncSetAttribute(prefill_tc2_kernel<64>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)tc2_smem(64))
+                    : cudaFuncSetAttribute(prefill_tc2_kernel<128>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)tc2_smem(128));
+      else
+        e = D == 64 ? cudaFuncSetAttribute(prefill_tc_kernel<64>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)tc_smem(64))
+                    : cudaFuncSetAttribute(prefill_tc_kernel<128>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)tc_smem(128));
       if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute");
       g_prefill_attr[dev][vi] = true;
     }
@@ -882,8 +911,12 @@ PKV_API int paged_prefill_attention(pkv_bf16 *out, const pkv_bf16 *q, const pkv_
   a.scale_log2 = scale * kLog2e;
   dim3 grid((unsigned)tiles, (unsigned)cache->num_kv_heads, (unsigned)num_seqs);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (D == 64)
-    prefill_tc2_kernel<<<grid, kTc2Threads, tc2_smem(), s>>>(tmk, tmv, a);
+  if (two && D == 64)
+    prefill_tc2_kernel<64><<<grid, kTc2Threads, tc2_smem(64), s>>>(tmk, tmv, a);
+  else if (two)
+    prefill_tc2_kernel<128><<<grid, kTc2Threads, tc2_smem(128), s>>>(tmk, tmv, a);
+  else if (D == 64)
+    prefill_tc_kernel<64><<<grid, kTcThreads, tc_smem(64), s>>>(tmk, tmv, a);
   else
     prefill_tc_kernel<128><<<grid, kTcThreads, tc_smem(128), s>>>(tmk, tmv, a);
   cudaError_t e = cudaGetLastError();

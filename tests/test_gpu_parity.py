@@ -802,6 +802,31 @@ def test_workload_decode_step_rope(B, oracle, wid):
     check_attention(out, ref, f"{w.name} rope step")
 
 
+@pytest.mark.parametrize("D,BS", [(64, 16), (128, 32)])
+def test_prefill_two_tiles_ragged(B, oracle, D, BS):
+    """Enough (sequence, kv head) units (40 x 8 = 320 >= two waves on 152 SMs) that the
+    launcher gives each CTA two 128-row query tiles: ragged lengths, chunk sizes from one
+    token to the whole sequence, tiles whose second half is empty."""
+    import itertools
+    gen = torch.Generator().manual_seed(90 + D)
+    lens = [int(x) for x in torch.randint(1, 261, (40,), generator=gen)]
+    chunks = [max(1, int(torch.randint(0, L + 1, (1,), generator=gen))) for L in lens]
+    chunks[0], chunks[1] = lens[0], 1
+    w = W.small_workload(B=40, Hq=16, Hkv=8, D=D, BS=BS, lens=tuple(lens), seed=91 + D, write="none")
+    inp = W.make_inputs(w, poison=True)
+    qs = torch.tensor([0] + list(itertools.accumulate(chunks)), dtype=torch.int32)
+    q = torch.randn(int(qs[-1]), 16, D, generator=gen).to(torch.bfloat16)
+    ref = oracle.prefill(q, inp["k_cache"], inp["v_cache"], inp["block_tables"], inp["context_lens"],
+                         qs, inp["scale"])
+    g = dev(inp)
+    out = torch.full((int(qs[-1]), 16, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    B.paged_prefill_attention(out, q.cuda(), g["k_cache"], g["v_cache"], g["block_tables"],
+                              g["context_lens"], inp["max_context_len"], qs.cuda(), max(chunks),
+                              inp["scale"])
+    check_attention(out, ref, f"two-tile prefill D={D} BS={BS}")
+    assert_no_device_errors(B)
+
+
 def test_prefill_single_token_chunks_equal_decode(B, oracle):
     """A chunk of one token per sequence is a decode step."""
     w = W.small_workload(B=3, Hq=32, Hkv=8, D=64, BS=16, lens=(5, 900, 2048), seed=51, write="none")
