@@ -280,6 +280,41 @@ def test_many_units_decode(B, oracle, D, BS, Hq, Hkv, lens):
     assert_no_device_errors(B)
 
 
+def test_very_long_contexts(B, oracle):
+    """131072 and 70001 tokens: the plan cuts each (sequence, kv head) into well over a
+    hundred partitions merged by the last one through global memory (the merge folds them
+    8 at a time), and a chunked prefill of the last 512 tokens walks ~1000 key blocks of
+    128 per tile."""
+    import itertools
+    lens = (131072, 70001)
+    w = W.small_workload(B=2, Hq=8, Hkv=1, D=128, BS=32, lens=lens, seed=95, write="last")
+    inp = W.make_inputs(w, poison=True)
+    P = B.paged_decode_plan(2, 8, 1, 128, inp["max_context_len"])
+    assert math.ceil(inp["max_context_len"] / P) > 100
+    assert B.paged_decode_path(2, 8, 1, 128, inp["max_context_len"]) == B.PATH_PARTITIONS
+    g = dev(inp)
+    out = step(B, g)
+    ref, kc_ref, vc_ref = oracle.step(inp)
+    assert torch.equal(g["k_cache"].cpu().view(torch.int16), kc_ref.view(torch.int16))
+    check_attention(out, ref, "131072 tokens")
+    # chunked prefill over the updated cache, sampled rows
+    chunks = (512, 512)
+    qs = torch.tensor([0] + list(itertools.accumulate(chunks)), dtype=torch.int32)
+    q = torch.randn(1024, 8, 128, generator=torch.Generator().manual_seed(96)).to(torch.bfloat16)
+    po = torch.full((1024, 8, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    B.paged_prefill_attention(po, q.cuda(), g["k_cache"], g["v_cache"], g["block_tables"],
+                              g["context_lens"], inp["max_context_len"], qs.cuda(), 512, inp["scale"])
+    got = po.cpu()
+    assert torch.isfinite(got.float()).all()
+    for b in (0, 1):
+        rows = slice(int(qs[b + 1]) - 4, int(qs[b + 1]))
+        pref = oracle.prefill(q[rows], kc_ref, vc_ref, inp["block_tables"][b:b + 1],
+                              inp["context_lens"][b:b + 1], torch.tensor([0, 4], dtype=torch.int32),
+                              inp["scale"])
+        check_attention(got[rows], pref, f"prefill at {lens[b]} tokens")
+    assert_no_device_errors(B)
+
+
 def test_large_ragged_batch(B, oracle):
     """Many (sequence, kv head) units with ragged contexts up to 512."""
     lens = tuple(int(x) for x in torch.randint(1, 513, (160,), generator=torch.Generator().manual_seed(4)))
