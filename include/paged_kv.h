@@ -256,7 +256,9 @@ int paged_decode_step_rope(pkv_bf16 *out, pkv_bf16 *q, const pkv_bf16 *k, const 
  *   out[row][h] = bf16( sum_{t <= p} softmax_t(scale * <q[row][h], K_t>) V_t )
  * with K_t, V_t read through block_tables as in paged_decode_attention (same head
  * mapping, sizes and alignment rules; out is 16-byte aligned).  max_query_len >= every
- * n_b sizes the grid.  Every out row of a query is written; nothing else.
+ * n_b sizes the grid; a sequence with more queries raises PKV_DEVERR_CONTEXT_LEN and
+ * its rows past max_query_len are not written.  Every out row of a query is written;
+ * nothing else.
  */
 int paged_prefill_attention(pkv_bf16 *out, const pkv_bf16 *q, const pkv_bf16 *k_cache,
                             const pkv_bf16 *v_cache, const int32_t *block_tables,

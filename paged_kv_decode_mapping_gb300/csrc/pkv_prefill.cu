@@ -152,6 +152,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   const int rows = n * G;  // query rows of this (b, g)
   const int row0 = tile * kTcRows;
+  // rows past the grid (n_b > max_query_len) would go unwritten: flag it
+  if (tile == 0 && tid == 0 && (int64_t)rows > (int64_t)gridDim.x * kTcRows)
+    raise_error(PKV_DEVERR_CONTEXT_LEN);
   if (row0 >= rows) return;
   const int last_row = min(row0 + kTcRows, rows) - 1;
   const int t_end = L - n + last_row / G + 1;  // keys the tile needs: [0, t_end)
@@ -510,6 +513,9 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
   }
   const int rows = n * G;
   const int row0 = tile * 2 * kTcRows;
+  // rows past the grid (n_b > max_query_len) would go unwritten: flag it
+  if (tile == 0 && tid == 0 && (int64_t)rows > (int64_t)gridDim.x * 2 * kTcRows)
+    raise_error(PKV_DEVERR_CONTEXT_LEN);
   if (row0 >= rows) return;
   // per tile: its last row, the keys it needs [0, t_end_t), its blocks
   int t_end_t[2], nblk_t[2];

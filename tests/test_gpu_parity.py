@@ -505,6 +505,14 @@ def test_device_error_bits(B):
                              90, inp["scale"])
     assert B.pkv_device_errors(clear=True) & 4
     assert B.pkv_device_errors(clear=True) == 0
+    # a prefill whose max_query_len understates a sequence's query count: flagged
+    qs = torch.tensor([0, 80, 90], dtype=torch.int32, device="cuda")
+    qp = torch.zeros(90, 8, 64, dtype=torch.bfloat16, device="cuda")
+    po = torch.empty_like(qp)
+    B.paged_prefill_attention(po, qp, g["k_cache"], g["v_cache"], g["block_tables"],
+                              g["context_lens"], 90, qs, 10, inp["scale"])
+    assert B.pkv_device_errors(clear=True) & 4
+    assert B.pkv_device_errors(clear=True) == 0
 
 
 # ------------------------------------------------------- block-manager driven steps
