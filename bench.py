@@ -201,9 +201,20 @@ def time_oracle(inp: dict, budget_s: float, max_reps: int = 1000) -> dict:
         if el >= budget_s or reps >= max_reps:
             break
     per = el / reps
+    # the same step on one thread (a fifth of the budget, at least one step)
+    t1, reps1 = time.perf_counter(), 0
+    while True:
+        orc.step(inp, num_threads=1)
+        reps1 += 1
+        el1 = time.perf_counter() - t1
+        if el1 >= budget_s / 5 or reps1 >= max_reps:
+            break
+    per1 = el1 / reps1
     return {"value": nbytes / per / 1e9, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+            "value_1_thread": nbytes / per1 / 1e9,
             "sample": f"{reps} full write+decode steps of the workload, fp64, OpenMP over "
-                      f"(sequence, head) rows on {os.cpu_count()} threads; {per * 1e3:.1f} ms/step"}
+                      f"(sequence, head) rows on {os.cpu_count()} threads; {per * 1e3:.1f} ms/step "
+                      f"({per1 * 1e3:.1f} ms/step on one thread, {reps1} steps)"}
 
 
 def run_reference(args, w) -> None:
