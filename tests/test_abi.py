@@ -106,6 +106,43 @@ def test_write_argument_errors(B):
     assert lib.paged_kv_write(None, None, None, 0, None, None, ctypes.byref(d), None) == 0
 
 
+def test_rope_step_argument_errors(B):
+    lib = B.lib()
+    d = _desc(B)
+
+    def call(rotary_dim=64, positions=FAKE, cos_sin=FAKE, desc=d, out=FAKE):
+        # out, q, k, v, slots, positions, cos_sin, max_position, rotary_dim, neox,
+        # k_cache, v_cache, tables, max_blocks, lens, max_len, num_seqs, hq, desc, scale,
+        # workspace, bytes, stream
+        return lib.paged_decode_step_rope(out, FAKE, FAKE, FAKE, FAKE, positions, cos_sin, 128,
+                                          rotary_dim, 1, FAKE, FAKE, FAKE, 8, FAKE, 100, 2, 8,
+                                          ctypes.byref(desc), 0.125, None, 0, None)
+
+    assert call(rotary_dim=24) == -3 and "rotary_dim" in B.pkv_last_error()
+    assert call(rotary_dim=128) == -3                   # more than head_dim
+    assert call(positions=None) == -1
+    assert call(cos_sin=None) == -1
+    assert call(cos_sin=ctypes.c_void_p((1 << 20) + 4)) == -5
+    assert call(desc=_desc(B, d=96)) == -3
+    assert call(out=None) == -1
+
+
+def test_prefill_argument_errors(B):
+    lib = B.lib()
+    d = _desc(B)
+
+    def call(out=FAKE, qs=FAKE, max_len=100, max_q=16, desc=d):
+        return lib.paged_prefill_attention(out, FAKE, FAKE, FAKE, FAKE, 8, FAKE, max_len, qs, max_q,
+                                           2, 8, ctypes.byref(desc), 0.125, None)
+
+    assert call(max_q=101) == -2                          # more queries than context
+    assert call(qs=None) == -1
+    assert call(out=None) == -1
+    assert call(out=ctypes.c_void_p((1 << 20) + 8)) == -5  # 8-byte aligned: not enough
+    assert call(desc=_desc(B, d=96)) == -3
+    assert call(max_q=0) == 0                             # nothing to do
+
+
 def test_empty_batch_is_a_no_op(B):
     lib = B.lib()
     d = _desc(B)
