@@ -443,18 +443,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }
 
 // ===========================================================================
-// prefill_tc2_kernel: head_dim 64, two query tiles per CTA in ping-pong.
+// prefill_tc2_kernel: two query tiles per CTA in ping-pong.
 //
-// At head_dim 64 the softmax is heavy against the tensor work, so a CTA owns 256 query
-// rows as two 128-row tiles of the same (sequence, kv head): softmax warpgroup t (warps
-// 4t .. 4t+3) owns tile t.  The tensor-core thread issues PV_0(j), S_0(j+1), PV_1(j),
-// S_1(j+1), so while one warpgroup works on its S the tensor core works on the other
-// tile, and every K/V block staged feeds 256 rows.  Each tile has one S buffer and one
-// P buffer: S_t(j+1) is issued only once the softmax has released S_t(j) (p_full), and
-// the commit that announces S_t(j+1) covers every earlier tensor-core operation,
-// including PV_t(j), so when a tile's next S arrives its O is stable and its P free.
+// A CTA owns 256 query rows as two 128-row tiles of the same (sequence, kv head):
+// softmax warpgroup t (warps 4t .. 4t+3) owns tile t.  The tensor-core thread issues
+// S_0(j+1), PV_0(j), S_1(j+1), PV_1(j), so while one warpgroup works on its S the tensor
+// core works on the other tile, and every K/V block staged feeds 256 rows.  Each tile
+// has one S buffer and one P buffer: S_t(j+1) is issued once the softmax has released
+// S_t(j) (p_full), ahead of PV_t(j), so the softmax can take the next row max while
+// PV_t(j) runs; it waits for PV_t(j) (pv_done) before it rescales O_t or overwrites P_t.
 // Row arithmetic (positions, masking, lazy rescale, bf16 row sums) is the one-tile
-// kernel's.
+// kernel's.  head_dim 64: K and V rings of 3; head_dim 128: K ring of 2, V ring of 1.
 constexpr int kTc2Threads = 320;  // softmax warpgroups 0 and 1, producer warp 8, MMA warp 9
 
 template <int D>
@@ -627,11 +626,17 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
         for (int t = 0; t < 2 && ok; ++t) {
           if (j >= nblk_of(t)) continue;
           if (!(ok = fail(dev::mbar_wait(p_full(t), j & 1)))) break;
+          dev::tc_fence_after();
+          // S_t(j+1) first: the softmax can start on it while the tensor core runs PV_t(j)
+          if (j + 1 < nblk_of(t)) {
+            if (!(ok = need_k(j + 1))) break;
+            issue_s(t, j + 1);
+          }
           if (!v_seen) {
             if (!(ok = fail(dev::mbar_wait(v_full(j % KSV), (j / KSV) & 1)))) break;
             v_seen = true;
+            dev::tc_fence_after();
           }
-          dev::tc_fence_after();
           const uint32_t vt = base + SL::v + (j % KSV) * SL::kTile;
           const uint32_t pb = base + SL::p + t * SL::kP;
 #pragma unroll
@@ -642,10 +647,6 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
                            (j > 0 || kk > 0) ? 1u : 0u);
           }
           dev::umma_commit(pv_done(t));
-          if (j + 1 < nblk_of(t)) {
-            if (!(ok = need_k(j + 1))) break;
-            issue_s(t, j + 1);
-          }
         }
         if (ok) dev::umma_commit(v_empty(j % KSV));
       }
@@ -707,8 +708,8 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
       }
       const float bmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      // S_t(j) arrived: every earlier tensor-core operation, PV_t(j-1) included, is done,
-      // so O_t is stable and the P buffer free
+      // O_t is stable and the P buffer free once PV_t(j-1) has completed
+      if (j > 0 && !(ok = __all_sync(0xffffffffu, dev::mbar_wait(pv_done(t), (j - 1) & 1)))) break;
       if (j > 0) {
         const bool need = bmax > m_ref + kTcRescale;
         if (__any_sync(0xffffffffu, need)) {
