@@ -287,6 +287,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0) dev::mbar_arrive(q_ready);
     }
     float m_ref = -INFINITY, lsum = 0.f;
+    const bool pos_scale = a.scale_log2 > 0.f;
     bool ok = true;
     for (int j = 0; j < nblk; ++j) {
       const int k0 = j * kTcKeys;
@@ -307,17 +308,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         dev::tmem_ld32(sbase + ch * 32, x);
         dev::tmem_wait_ld();
         const int lc = lim - ch * 32;
-        if (whole) {
+        // with a positive scale the max of the raw scores, scaled once, is the max of
+        // the scaled scores (rounding is monotonic)
+        const float sc = pos_scale ? 1.f : a.scale_log2;
+        if (whole && pos_scale) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(x[i]) * a.scale_log2);
+          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(x[i]));
+        } else if (whole) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(x[i]) * sc);
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            mx[i & 7] = fmaxf(mx[i & 7], i <= lc ? __uint_as_float(x[i]) * a.scale_log2 : -INFINITY);
+            mx[i & 7] = fmaxf(mx[i & 7], i <= lc ? __uint_as_float(x[i]) * sc : -INFINITY);
         }
       }
-      const float bmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      float bmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      if (pos_scale) bmax *= a.scale_log2;
       if (j > 0) {
         const bool need = bmax > m_ref + kTcRescale;
         if (__any_sync(0xffffffffu, need)) {  // O moves: wait until the previous P.V is in
@@ -363,8 +371,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int e = 0; e < 16; ++e) {
           float p0 = dev::ex2(fmaf(__uint_as_float(x[2 * e]), a.scale_log2, -m_ref));
           float p1 = dev::ex2(fmaf(__uint_as_float(x[2 * e + 1]), a.scale_log2, -m_ref));
-          p0 = 2 * e <= lc ? p0 : 0.f;
-          p1 = 2 * e + 1 <= lc ? p1 : 0.f;
+          if (!whole) {
+            p0 = 2 * e <= lc ? p0 : 0.f;
+            p1 = 2 * e + 1 <= lc ? p1 : 0.f;
+          }
           pk[e] = dev::pack_bf16x2(p0, p1);
           // sum what the tensor cores multiply: with a stale reference max the largest
           // P is not a power of two, and only this keeps the weights a convex combination
@@ -681,6 +691,7 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
     const int nb = nblk_of(t);
     const int te = t ? t_end_t[1] : t_end_t[0];
     float m_ref = -INFINITY, lsum = 0.f;
+    const bool pos_scale = a.scale_log2 > 0.f;
     bool ok = true;
     for (int j = 0; j < nb; ++j) {
       const int k0 = j * kTcKeys;
@@ -697,17 +708,24 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
         dev::tmem_ld32(sb + ch * 32, x);
         dev::tmem_wait_ld();
         const int lc = lim - ch * 32;
-        if (whole) {
+        // with a positive scale the max of the raw scores, scaled once, is the max of
+        // the scaled scores (rounding is monotonic)
+        const float sc = pos_scale ? 1.f : a.scale_log2;
+        if (whole && pos_scale) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(x[i]) * a.scale_log2);
+          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(x[i]));
+        } else if (whole) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(x[i]) * sc);
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            mx[i & 7] = fmaxf(mx[i & 7], i <= lc ? __uint_as_float(x[i]) * a.scale_log2 : -INFINITY);
+            mx[i & 7] = fmaxf(mx[i & 7], i <= lc ? __uint_as_float(x[i]) * sc : -INFINITY);
         }
       }
-      const float bmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      float bmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      if (pos_scale) bmax *= a.scale_log2;
       // O_t is stable and the P buffer free once PV_t(j-1) has completed
       if (j > 0 && !(ok = __all_sync(0xffffffffu, dev::mbar_wait(pv_done(t), (j - 1) & 1)))) break;
       if (j > 0) {
@@ -746,8 +764,10 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
         for (int e = 0; e < 16; ++e) {
           float p0 = dev::ex2(fmaf(__uint_as_float(x[2 * e]), a.scale_log2, -m_ref));
           float p1 = dev::ex2(fmaf(__uint_as_float(x[2 * e + 1]), a.scale_log2, -m_ref));
-          p0 = 2 * e <= lc ? p0 : 0.f;
-          p1 = 2 * e + 1 <= lc ? p1 : 0.f;
+          if (!whole) {
+            p0 = 2 * e <= lc ? p0 : 0.f;
+            p1 = 2 * e + 1 <= lc ? p1 : 0.f;
+          }
           pk[e] = dev::pack_bf16x2(p0, p1);
           ls[(2 * e) & 7] += dev::bf16lo_to_f32(pk[e]);
           ls[(2 * e + 1) & 7] += dev::bf16hi_to_f32(pk[e]);
