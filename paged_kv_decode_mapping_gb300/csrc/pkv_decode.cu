@@ -137,16 +137,15 @@ __device__ __forceinline__ void warp_tile(WarpAcc<D> &acc, const uint32_t (&qb)[
   }
 }
 
-// Partitions one cluster merges (portable cluster size).
-constexpr int kMaxClusterParts = 8;
-// Where a CTA publishes its per-head results for the cluster merge: after the merge
-// area of its four warps, inside the (then free) stage ring.
-template <int D>
-constexpr uint32_t kPubOffset =
-    ((kConsumerWarps * kMaxGroup * D + 2 * kConsumerWarps * kMaxGroup) * 4 + 1023) & ~1023u;
-static_assert(kPubOffset<64> + (kMaxGroup * 64 + kMaxGroup) * 4 <= 4 * 2 * kChunk * 64 * 2 &&
-                  kPubOffset<128> + (kMaxGroup * 128 + kMaxGroup) * 4 <= 3 * 2 * kChunk * 128 * 2,
-              "the published results must fit in the stage ring");
+// Receive slots the largest case needs: n * ceil(G / n) over cluster sizes n >= 2 and
+// groups G <= kMaxGroup.
+constexpr int recv_slots_needed() {
+  int m = 0;
+  for (int n = 2; n <= kMaxClusterParts; ++n)
+    for (int g = 1; g <= kMaxGroup; ++g) m = n * ((g + n - 1) / n) > m ? n * ((g + n - 1) / n) : m;
+  return m;
+}
+static_assert(recv_slots_needed() <= kRecvSlots, "cluster merge receive area");
 
 // Merge area of the four warps: red_o [warps][G][D], red_m / red_l [warps][8].
 struct MergeArea {
@@ -273,14 +272,14 @@ __device__ __forceinline__ void merge_rows(uint16_t *dst, const float *o_rows,
   }
 }
 
-// Cluster merge: every CTA of the cluster (one per partition of a (sequence, kv head))
-// published, in its own shared memory at `pub`, the normalised output [kMaxGroup][D]
-// and then the base-2 lse [kMaxGroup] of each head (-inf for a partition without
-// keys).  One warp merges head h over the n CTAs, reading them through distributed
-// shared memory; each lane owns D/32 dims.  All -inf (empty context): zeros.
+// Cluster merge of one query head on the CTA that owns it: receive-area rows
+// u * hpo + j (u = 0 .. n-1; j = the head's index among the CTA's heads) hold partition
+// u's normalised output [D] and its base-2 lse (-inf for a partition without keys).
+// One warp; each lane owns D/32 dims.  All -inf (empty context): zeros.
 template <int D>
-__device__ __forceinline__ void cluster_merge_head(uint16_t *dst, uint32_t pub, int h, int n,
-                                                   int lane) {
+__device__ __forceinline__ void recv_merge_head(uint16_t *dst, const float *recv_o,
+                                                const float *recv_l, int j, int hpo, int n,
+                                                int lane) {
   constexpr int VPL = D / 32;
   float lk[kMaxClusterParts], ov[kMaxClusterParts][VPL];
   float M = -INFINITY;
@@ -290,15 +289,15 @@ __device__ __forceinline__ void cluster_merge_head(uint16_t *dst, uint32_t pub, 
 #pragma unroll
     for (int v = 0; v < VPL; ++v) ov[u][v] = 0.f;
     if (u < n) {
-      const uint32_t peer = dev::mapa(pub, (uint32_t)u);
-      lk[u] = dev::ld_dsmem(peer + (uint32_t)(kMaxGroup * D + h) * 4u);
-      const uint32_t src = peer + (uint32_t)(h * D + lane * VPL) * 4u;
+      const int slot = u * hpo + j;
+      lk[u] = recv_l[slot];
+      const float *src = recv_o + slot * D + lane * VPL;
       if constexpr (VPL == 2) {
-        const float2 t2 = dev::ld_dsmem_v2(src);
+        const float2 t2 = *reinterpret_cast<const float2 *>(src);
         ov[u][0] = t2.x;
         ov[u][1] = t2.y;
       } else {
-        const float4 t4 = dev::ld_dsmem_v4(src);
+        const float4 t4 = *reinterpret_cast<const float4 *>(src);
         ov[u][0] = t4.x;
         ov[u][1] = t4.y;
         ov[u][2] = t4.z;
@@ -418,6 +417,13 @@ __global__ void __launch_bounds__(kThreads, 2)
   volatile int *const s_flag =
       reinterpret_cast<volatile int *>(base_ptr + STAGES * kStageBytes + STAGES * 16);
   volatile int *const s_last = s_flag + 1;
+  // Cluster merge: a barrier whose phase completes when every CTA of the cluster has
+  // pushed its results here, and the area they land in (rows of D floats, then the lse).
+  const uint32_t bar_merge = bar_full + STAGES * 16 + 8;
+  const uint32_t recv = bar_merge + 8;
+  const float *const recv_o =
+      reinterpret_cast<const float *>(base_ptr + STAGES * kStageBytes + STAGES * 16 + 16);
+  const float *const recv_l = recv_o + kRecvSlots * D;
 
   // grid: x = partition (fastest), y = kv head, z = sequence
   const int part = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -470,10 +476,19 @@ __global__ void __launch_bounds__(kThreads, 2)
       dev::mbar_init(bar_full + 8 * s, 1);
       dev::mbar_init(bar_empty + 8 * s, kConsumerWarps);
     }
+    if (cluster) {  // armed for the bytes the cluster pushes here: see the merge below
+      const int n = (int)dev::cluster_nctarank(), rank = (int)dev::cluster_ctarank();
+      const int owned = rank < a.group ? (a.group - rank + n - 1) / n : 0;
+      dev::mbar_init(bar_merge, 1);
+      dev::mbar_arrive_expect_tx(bar_merge, (uint32_t)(n * owned * (D + 1) * 4));
+    }
     *s_flag = 0;
     dev::fence_mbar_init();
   }
   __syncthreads();
+  // Every thread arrives on the cluster barrier now and waits on it before its first
+  // access to another CTA's shared memory: by then every merge barrier is initialised.
+  if (cluster) dev::cluster_arrive_relaxed();
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------- producer warp
@@ -523,6 +538,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       __syncwarp();
     }
+    if (cluster) dev::cluster_wait();
   } else {
     // ----------------------------------------------------------- consumer warps
     WarpAcc<D> acc;
@@ -554,41 +570,50 @@ __global__ void __launch_bounds__(kThreads, 2)
     warp_stash<D>(acc, r, a.group, warp, lane);
     consumer_bar();
     const int nparts_b = (L + a.partition_tokens - 1) / a.partition_tokens;  // non-empty ones
-    if (cluster) {  // publish (normalised o, base-2 lse) per head for the cluster merge
-      float *pub_o = reinterpret_cast<float *>(base_ptr + kPubOffset<D>);
-      float *pub_l = pub_o + kMaxGroup * D;
-      for (int i = tid; i < a.group * D; i += kConsumers) {
-        const int h = i / D, d = i - h * D;
-        float M2, den;
-        const float val = cta_merge<D>(r, a.group, h, d, &M2, &den);
-        const bool live = den > 0.f;  // false (or NaN) when this range had no keys
-        pub_o[h * D + d] = live ? val : 0.f;
-        if (d == 0) pub_l[h] = live ? M2 + log2f(den) : -INFINITY;
+    if (cluster) {
+      // Cluster merge.  CTA rank h % n merges head h.  Every CTA pushes its (normalised
+      // o, base-2 lse) of each head into the owner's receive area with asynchronous
+      // stores that count their bytes off the owner's merge barrier, which its one
+      // arrival at set-up armed for all n * (heads owned) * (D + 1) * 4 bytes.  The
+      // phase completes when the last byte has landed: the owner then merges from its
+      // own shared memory, which nobody touches again, so no CTA waits for its peers
+      // to finish reading and there is no closing cluster barrier.  Every wait on the
+      // way to the pushes is bounded, so they all come; if the merge barrier still
+      // times out, the CTA records the error and skips the merge.
+      dev::cluster_wait();
+      const int n = (int)dev::cluster_nctarank();
+      const int rank = (int)dev::cluster_ctarank();
+      if (n == a.n_parts && n <= kMaxClusterParts) {
+        const int hpo = (a.group + n - 1) / n;  // heads each CTA merges, at most
+        for (int i = tid; i < a.group * D; i += kConsumers) {
+          const int h = i / D, d = i - h * D;
+          float M2, den;
+          const float val = cta_merge<D>(r, a.group, h, d, &M2, &den);
+          const bool live = den > 0.f;  // false (or NaN) when this range had no keys
+          const int slot = rank * hpo + h / n;
+          const uint32_t dst = dev::mapa(recv, (uint32_t)(h % n));
+          const uint32_t dbar = dev::mapa(bar_merge, (uint32_t)(h % n));
+          dev::st_async(dst + (uint32_t)(slot * D + d) * 4u, live ? val : 0.f, dbar);
+          if (d == 0)
+            dev::st_async(dst + (uint32_t)(kRecvSlots * D + slot) * 4u,
+                          live ? M2 + log2f(den) : -INFINITY, dbar);
+        }
+        if (__all_sync(0xffffffffu, dev::mbar_wait_cluster(bar_merge, 0))) {
+          const int64_t head0 = (int64_t)b * a.num_q_heads + g * a.group;
+          for (int j = warp; j < hpo; j += kConsumerWarps) {
+            const int h = rank + n * j;
+            if (h < a.group)
+              recv_merge_head<D>(a.out + (head0 + h) * D, recv_o, recv_l, j, hpo, n, lane);
+          }
+        } else if (lane == 0) {
+          raise_error(PKV_DEVERR_TIMEOUT);
+        }
+      } else if (tid == 0 && rank == 0) {
+        raise_error(PKV_DEVERR_TIMEOUT);  // launched with the wrong cluster shape
       }
     } else {
       finish_partition<D>(a, r, b, g, part, nparts_b, tid, warp, lane, s_flag, s_last);
     }
-  }
-
-  // ---- cluster merge.  Every thread of every CTA reaches both barriers exactly once:
-  // no path above returns in cluster mode and every wait above is bounded.  The first
-  // barrier publishes each CTA's results to the cluster; after it, CTA `rank` merges
-  // heads rank, rank + n, ... (one warp each); the second keeps every CTA's shared
-  // memory alive until its peers have read it.
-  if (cluster) {
-    dev::cluster_sync();
-    const int n = (int)dev::cluster_nctarank();
-    const int rank = (int)dev::cluster_ctarank();
-    if (warp < kConsumerWarps) {
-      if (n == a.n_parts && n <= kMaxClusterParts) {
-        const int64_t head0 = (int64_t)b * a.num_q_heads + g * a.group;
-        for (int h = rank + n * warp; h < a.group; h += n * kConsumerWarps)
-          cluster_merge_head<D>(a.out + (head0 + h) * D, base + kPubOffset<D>, h, n, lane);
-      } else if (tid == 0 && rank == 0) {
-        raise_error(PKV_DEVERR_TIMEOUT);  // launched with the wrong cluster shape
-      }
-    }
-    dev::cluster_sync();
   }
 
   // ---- a timed-out wait leaves copies possibly in flight: wait for them (bounded)

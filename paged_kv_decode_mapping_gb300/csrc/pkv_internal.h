@@ -53,13 +53,26 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kMaxDevices = 64;
 
-// Stages of the TMA ring and the dynamic shared memory of one decode CTA.
+// Partitions one cluster merges (portable cluster size), and the slots of the area in
+// which a decode CTA receives its peers' results for the heads it merges: slot
+// u * ceil(G / n) + j holds source rank u's result for the CTA's j-th head, and
+// n * ceil(G / n) <= 14 for every cluster size n in [2, 8] and group G <= 8.
+constexpr int kMaxClusterParts = 8;
+constexpr int kRecvSlots = 16;
+
+// Stages of the TMA ring and the dynamic shared memory of one decode CTA: 1 KB of
+// alignment slack, the ring, its full/empty barriers, two flags and the merge barrier,
+// then the receive area (kRecvSlots rows of D floats, then kRecvSlots lse values).
 constexpr int split_stages(int d) { return d == 64 ? 4 : 3; }
+constexpr size_t split_ring_bytes(int d) { return (size_t)split_stages(d) * 2 * kChunk * d * 2; }
 constexpr size_t split_smem(int d) {
-  return 1024 + (size_t)split_stages(d) * 2 * kChunk * d * 2 + split_stages(d) * 16 + 16;
+  return 1024 + split_ring_bytes(d) + split_stages(d) * 16 + 16 + (size_t)kRecvSlots * (d + 1) * 4;
 }
-// CTAs of decode_kernel one SM holds (shared memory limited: 66 KB at D=64, 99 KB at D=128).
+// CTAs of decode_kernel one SM holds (shared memory limited: 70 KB at D=64, 105 KB at
+// D=128, of the 228 KB an SM shares out with 1 KB reserved per CTA).
 constexpr int split_occupancy(int d) { return d == 64 ? 3 : 2; }
+static_assert(3 * (split_smem(64) + 1024) <= 228 * 1024 && 2 * (split_smem(128) + 1024) <= 228 * 1024,
+              "decode CTAs per SM");
 
 // Guards the tensor-map cache, the SM-count cache and the per-device kernel attributes.
 std::mutex &attn_mutex();
@@ -226,7 +239,7 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
       : "memory");
 }
 
-// ---- thread-block clusters: rank, barrier, distributed shared memory reads
+// ---- thread-block clusters: rank, barrier, distributed shared memory stores
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -237,34 +250,46 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
   asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
   return r;
 }
-// Every thread of every CTA in the cluster: arrive (release), then wait (acquire).
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
 // The shared::cluster address of `addr` (a shared::cta address) in CTA `rank`.
 __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
-__device__ __forceinline__ float ld_dsmem(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
+// The cluster barrier in two halves: arrive without waiting (relaxed: a preceding
+// fence.mbarrier_init supplies the release of barrier initialisation), wait later.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
 }
-__device__ __forceinline__ float2 ld_dsmem_v2(uint32_t addr) {
-  float2 v;
-  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr)
-               : "memory");
-  return v;
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
 }
-__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
+// Stores v at shared::cluster address `addr` (in another CTA of the cluster, or this
+// one) and, once written, counts its 4 bytes off the transaction count of the mbarrier
+// at shared::cluster address `bar` in the same CTA (complete_tx releases at cluster
+// scope).  The sender needs nothing to stay alive: the value leaves from a register.
+__device__ __forceinline__ void st_async(uint32_t addr, float v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];"
+               ::"r"(addr), "f"(v), "r"(bar)
                : "memory");
-  return v;
+}
+// mbar_wait with acquire at cluster scope: what other CTAs of the cluster wrote to this
+// CTA's shared memory before completing the phase is visible after it returns true.
+// Same ~2 s limit.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((i & 255u) == 255u && globaltimer_ns() - t0 > 2000000000ull) return false;
+  }
 }
 
 // ---- 5th-generation tensor cores: TMEM, tcgen05.mma, shared-memory matrix descriptors
