@@ -638,14 +638,28 @@ __global__ void __launch_bounds__(kThreads, 2)
 // its launch, set-up and first-copy latency once, not once per partition.
 //
 // Order: longest first.  All full partitions come first (by partition index,
-// descending), then every sequence's last partition by its number of 64-key chunks,
-// descending; within a category, by sequence, then kv head.  Each CTA derives the same
+// descending), then every sequence's last partition by its size, descending; within a
+// category, by sequence, then kv head.  A single-partition sequence's size is its number
+// q of 64-key chunks.  A multi-partition sequence is merged by whichever of its
+// partitions finishes last: a store, a ticket and loads of the partials, about as much
+// latency as streaming two chunks, and pure delay near the end, where no other CTA's
+// streaming overlaps it.  So when the single-partition items alone fill one wave of CTAs
+// (T > 0, T the smallest chunk count at which they do), every multi-partition last
+// partition gets the largest size, Q + kMergeChunks: they follow the full partitions,
+// all merges happen while most of the work is still ahead, and the order ends with
+// single-partition items alone.  When they do not (T = 0; few, long sequences), moving
+// the merges up would put long single-partition items last instead, so a multi-partition
+// last partition only counts its merge: size q + kMergeChunks.  (Measured on batches of
+// 64 to 512 sequences: each rule is the faster one where it is used.)  Each CTA derives the same
 // order from the context lengths (histograms in shared memory), takes item blockIdx.x
-// first and then items gridDim.x + (a global counter).  No CTA waits for another; the
-// last CTA to finish resets the counter for the next call.
+// first and then items gridDim.x + (a global counter), each claimed when the current
+// item is two chunks from its last issue -- so the largest items left go to the CTAs
+// about to run dry (list scheduling).  No CTA waits for another; the last CTA to
+// finish resets the counter for the next call.
 
 constexpr int kMaxPersistSeqs = 1024;  // sequences per batch (a warp scans 32 x 32 of them)
-constexpr int kMaxCategories = 64;     // full-partition levels + last-partition chunk counts
+constexpr int kMaxCategories = 64;     // full-partition levels + last-partition sizes
+constexpr int kMergeChunks = 2;        // what a merge adds to a last partition's size
 
 // What the producer tells the consumers about the chunk in a stage.
 struct ItemDesc {
@@ -666,10 +680,11 @@ struct PersistSmem {
   static constexpr uint32_t q = STAGES * kStageBytes;
   static constexpr uint32_t desc = q + STAGES * kQSlot;
   static constexpr uint32_t bars = desc + STAGES * sizeof(ItemDesc);  // full[STAGES], empty[STAGES]
-  static constexpr uint32_t flags = bars + STAGES * 16;               // flag, last, issued
-  static constexpr uint32_t hist_nf = flags + 16;
-  static constexpr uint32_t hist_lc = hist_nf + kMaxCategories * 4;
-  static constexpr uint32_t off = hist_lc + kMaxCategories * 4;       // [kMaxCategories + 1]
+  static constexpr uint32_t flags = bars + STAGES * 16;               // flag, last, issued, T
+  static constexpr uint32_t hist_nf = flags + 16;                     // full partitions by nf
+  static constexpr uint32_t hist_lc = hist_nf + kMaxCategories * 4;   // single partitions by q
+  static constexpr uint32_t hist_ml = hist_lc + kMaxCategories * 4;   // multi-partition last, by q
+  static constexpr uint32_t off = hist_ml + kMaxCategories * 4;       // [kMaxCategories + 1]
   static constexpr uint32_t lt = off + (kMaxCategories + 4) * 4;      // u16 [kMaxPersistSeqs]
   static constexpr uint32_t nf = lt + kMaxPersistSeqs * 2;            // u8 [kMaxPersistSeqs]
   static constexpr uint32_t total = nf + kMaxPersistSeqs;
@@ -686,10 +701,12 @@ struct Item {
 // producer warp take part; the result is the same on every lane.
 //   s_off: exclusive prefix of the categories' item counts, s_off[ncat] = total;
 //   category c < R-1: full partition r = R-2-c of sequences with nf > r;
-//   category c >= R-1: last partition of sequences with ceil(lt / 64) = q = Q-(c-(R-1)).
+//   category c >= R-1: last partition of sequences whose size (q = ceil(lt / 64) if
+//                      nf = 0, else Q + kMergeChunks if T > 0, else q + kMergeChunks)
+//                      is Q + kMergeChunks - (c - (R-1)).
 __device__ __forceinline__ bool find_item(int k, const int *s_off, int ncat, int R, int P, int Hkv,
-                                          int num_seqs, const uint16_t *s_lt, const uint8_t *s_nf,
-                                          int lane, Item &it) {
+                                          int T, int num_seqs, const uint16_t *s_lt,
+                                          const uint8_t *s_nf, int lane, Item &it) {
   if (k >= s_off[ncat]) return false;
   // category: the last c with s_off[c] <= k (s_off is nondecreasing; that one is non-empty)
   const unsigned m0 = __ballot_sync(0xffffffffu, lane < ncat && s_off[lane] <= k);
@@ -699,33 +716,38 @@ __device__ __forceinline__ bool find_item(int k, const int *s_off, int ncat, int
   const int m = j / Hkv;
   it.g = j - m * Hkv;
   const bool full = cat < R - 1;
-  const int r = R - 2 - cat;                    // full: partition index
-  const int q = (P / kChunk) - (cat - (R - 1));  // last partition: its chunk count
+  const int r = R - 2 - cat;                                   // full: partition index
+  const int q = (P / kChunk) + kMergeChunks - (cat - (R - 1));  // last partition: its size
   // select the m-th sequence (ascending) of the category; lane w holds sequences [32w, 32w+32)
   unsigned bits = 0;
   if (32 * lane >= num_seqs) {
     // no sequences in this lane's word (the arrays are written up to num_seqs rounded to 32)
-  } else if (full) {
-    const uint4 *v = reinterpret_cast<const uint4 *>(s_nf + 32 * lane);
-    const uint4 w0 = v[0], w1 = v[1];
-    const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-    for (int t = 0; t < 32; ++t) bits |= (int)((wd[t >> 2] >> (8 * (t & 3))) & 0xffu) > r ? 1u << t : 0u;
   } else {
-    const uint4 *v = reinterpret_cast<const uint4 *>(s_lt + 32 * lane);
-    uint32_t wd[16];
+    const uint4 *vn = reinterpret_cast<const uint4 *>(s_nf + 32 * lane);
+    const uint4 n0 = vn[0], n1 = vn[1];
+    const uint32_t wn[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+    if (full) {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const uint4 x = v[u];
-      wd[4 * u] = x.x;
-      wd[4 * u + 1] = x.y;
-      wd[4 * u + 2] = x.z;
-      wd[4 * u + 3] = x.w;
-    }
+      for (int t = 0; t < 32; ++t) bits |= (int)((wn[t >> 2] >> (8 * (t & 3))) & 0xffu) > r ? 1u << t : 0u;
+    } else {
+      const uint4 *v = reinterpret_cast<const uint4 *>(s_lt + 32 * lane);
+      uint32_t wd[16];
 #pragma unroll
-    for (int t = 0; t < 32; ++t) {
-      const int lt = (int)((wd[t >> 1] >> (16 * (t & 1))) & 0xffffu);
-      bits |= (lt > 0 && (lt + kChunk - 1) / kChunk == q) ? 1u << t : 0u;
+      for (int u = 0; u < 4; ++u) {
+        const uint4 x = v[u];
+        wd[4 * u] = x.x;
+        wd[4 * u + 1] = x.y;
+        wd[4 * u + 2] = x.z;
+        wd[4 * u + 3] = x.w;
+      }
+#pragma unroll
+      for (int t = 0; t < 32; ++t) {
+        const int lt = (int)((wd[t >> 1] >> (16 * (t & 1))) & 0xffffu);
+        const int nf = (int)((wn[t >> 2] >> (8 * (t & 3))) & 0xffu);
+        const int qt = (lt + kChunk - 1) / kChunk;
+        const int size = nf == 0 ? qt : (T > 0 ? P / kChunk : qt) + kMergeChunks;
+        bits |= (lt > 0 && size == q) ? 1u << t : 0u;
+      }
     }
   }
   const int pc = __popc(bits);
@@ -774,21 +796,31 @@ __global__ void __launch_bounds__(kThreads, 2)
   volatile int *const s_flag = reinterpret_cast<volatile int *>(base_ptr + SL::flags);
   volatile int *const s_last = s_flag + 1;
   volatile int *const s_issued = s_flag + 2;
+  volatile int *const s_T = s_flag + 3;
   ItemDesc *const s_desc = reinterpret_cast<ItemDesc *>(base_ptr + SL::desc);
   int *const s_hist_nf = reinterpret_cast<int *>(base_ptr + SL::hist_nf);
   int *const s_hist_lc = reinterpret_cast<int *>(base_ptr + SL::hist_lc);
+  int *const s_hist_ml = reinterpret_cast<int *>(base_ptr + SL::hist_ml);
   int *const s_off = reinterpret_cast<int *>(base_ptr + SL::off);
   uint16_t *const s_lt = reinterpret_cast<uint16_t *>(base_ptr + SL::lt);
   uint8_t *const s_nf = base_ptr + SL::nf;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int P = a.partition_tokens, R = a.n_parts, Q = P / kChunk;
-  const int ncat = R - 1 + Q;
+  const int ncat = R - 1 + Q + kMergeChunks;
   const int Hkv = a.num_kv_heads;
   const int cap = (int)min((int64_t)a.max_blocks * a.block_size, (int64_t)a.max_context_len);
   const int bpad = (a.num_seqs + 31) & ~31;
 
-  // ---- set-up: barriers, and the order's histograms from the context lengths
+  // ---- set-up: barriers, and the order's histograms from the context lengths.  Every
+  // thread's lengths are loaded first, so their latencies overlap.
+  constexpr int kLensPerThread = (kMaxPersistSeqs + kThreads - 1) / kThreads;
+  int lens[kLensPerThread];
+#pragma unroll
+  for (int k = 0; k < kLensPerThread; ++k) {
+    const int bb = tid + k * kThreads;
+    lens[k] = bb < a.num_seqs ? __ldg(a.context_lens + bb) : 0;
+  }
   if (tid == 0) {
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) {
@@ -799,12 +831,15 @@ __global__ void __launch_bounds__(kThreads, 2)
     *s_issued = 0;
     dev::fence_mbar_init();
   }
-  for (int i = tid; i < 2 * kMaxCategories; i += kThreads) s_hist_nf[i] = 0;  // both histograms
+  for (int i = tid; i < 3 * kMaxCategories; i += kThreads) s_hist_nf[i] = 0;  // all three
   __syncthreads();
-  for (int bb = tid; bb < bpad; bb += kThreads) {
+#pragma unroll
+  for (int k = 0; k < kLensPerThread; ++k) {
+    const int bb = tid + k * kThreads;
+    if (bb >= bpad) break;
     int nf = 0, lt = 0;
     if (bb < a.num_seqs) {
-      int L = __ldg(a.context_lens + bb);
+      int L = lens[k];
       if (L < 0 || L > cap) {
         if (blockIdx.x == 0) raise_error(PKV_DEVERR_CONTEXT_LEN);
         L = L < 0 ? 0 : cap;
@@ -812,8 +847,13 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (L > 0) {
         nf = (L - 1) / P;
         lt = L - nf * P;
-        if (nf > 0) atomicAdd(s_hist_nf + nf, 1);
-        atomicAdd(s_hist_lc + (lt + kChunk - 1) / kChunk, 1);
+        const int q = (lt + kChunk - 1) / kChunk;
+        if (nf > 0) {
+          atomicAdd(s_hist_nf + nf, 1);
+          atomicAdd(s_hist_ml + q, 1);
+        } else {
+          atomicAdd(s_hist_lc + q, 1);
+        }
       } else if (bb % (int)gridDim.x == (int)blockIdx.x) {  // empty context: zero output
         uint2 *o = reinterpret_cast<uint2 *>(a.out + (int64_t)bb * a.num_q_heads * D);
         for (int i = 0; i < a.num_q_heads * D / 4; ++i) o[i] = make_uint2(0u, 0u);
@@ -823,18 +863,60 @@ __global__ void __launch_bounds__(kThreads, 2)
     s_lt[bb] = (uint16_t)lt;
   }
   __syncthreads();
-  if (tid == 0) {
-    int off = 0, suffix = 0, c = 0;
-    for (int r = R - 2; r >= 0; --r, ++c) {  // full partitions r: sequences with nf > r
-      suffix += s_hist_nf[r + 1];
-      s_off[c] = off;
-      off += suffix * Hkv;
+  if (warp == 0) {  // T, the item counts of the categories, then their exclusive prefix
+    int T = 0;
+    {  // single-partition items of at most q chunks, q = lane + 1 and lane + 33
+      int i0 = lane + 1 <= Q ? s_hist_lc[lane + 1] * Hkv : 0;
+      int i1 = lane + 33 <= Q ? s_hist_lc[lane + 33] * Hkv : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y0 = __shfl_up_sync(0xffffffffu, i0, o), y1 = __shfl_up_sync(0xffffffffu, i1, o);
+        if (lane >= o) {
+          i0 += y0;
+          i1 += y1;
+        }
+      }
+      i1 += __shfl_sync(0xffffffffu, i0, 31);
+      const unsigned b0 = __ballot_sync(0xffffffffu, lane + 1 <= Q && i0 >= (int)gridDim.x);
+      const unsigned b1 = __ballot_sync(0xffffffffu, lane + 33 <= Q && i1 >= (int)gridDim.x);
+      T = b0 ? __ffs(b0) : (b1 ? 32 + __ffs(b1) : 0);
     }
-    for (int q = Q; q >= 1; --q, ++c) {  // last partitions of q chunks
-      s_off[c] = off;
-      off += s_hist_lc[q] * Hkv;
+    int cnt[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int c = lane + 32 * hh;
+      int n = 0;
+      if (c < R - 1) {  // full partition r = R-2-c: sequences with nf > r
+        for (int x = R - 1 - c; x <= R - 1; ++x) n += s_hist_nf[x];
+      } else if (c < ncat) {  // last partitions of size sz
+        const int sz = Q + kMergeChunks - (c - (R - 1));
+        if (sz <= Q) n = s_hist_lc[sz];
+        if (T > 0) {  // every multi-partition last partition in the largest size
+          if (sz == Q + kMergeChunks)
+            for (int qm = 1; qm <= Q; ++qm) n += s_hist_ml[qm];
+        } else if (sz - kMergeChunks >= 1) {
+          n += s_hist_ml[sz - kMergeChunks];
+        }
+      }
+      cnt[hh] = n * Hkv;
     }
-    s_off[ncat] = off;
+    int i0 = cnt[0], i1 = cnt[1];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y0 = __shfl_up_sync(0xffffffffu, i0, o), y1 = __shfl_up_sync(0xffffffffu, i1, o);
+      if (lane >= o) {
+        i0 += y0;
+        i1 += y1;
+      }
+    }
+    const int t0 = __shfl_sync(0xffffffffu, i0, 31);
+    const int total = t0 + __shfl_sync(0xffffffffu, i1, 31);
+    if (lane < ncat) s_off[lane] = i0 - cnt[0];
+    if (lane + 32 < ncat) s_off[lane + 32] = t0 + i1 - cnt[1];
+    if (lane == 0) {
+      s_off[ncat] = total;
+      *s_T = T;
+    }
   }
   __syncthreads();
 
@@ -848,10 +930,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     int c = 0;  // chunks issued, over all items
     bool ok = true;
     Item it;
-    int k_next = 0;
-    bool have = find_item((int)blockIdx.x, s_off, ncat, R, P, Hkv, a.num_seqs, s_lt, s_nf, lane, it);
-    if (have && lane == 0) k_next = (int)gridDim.x + (int)atomicAdd(a.sched, 1u);
+    const int T = *s_T;
+    bool have = find_item((int)blockIdx.x, s_off, ncat, R, P, Hkv, T, a.num_seqs, s_lt, s_nf, lane, it);
     while (have) {
+      int k_next = 0;  // lane 0: the item after this one
       const int32_t *trow = a.block_tables + (int64_t)it.b * a.max_blocks;
       const int lb_last = (it.t_end - 1) >> a.log2_bs;
       int win = it.t_begin >> a.log2_bs;
@@ -868,6 +950,12 @@ __global__ void __launch_bounds__(kThreads, 2)
           ok = false;
           break;
         }
+        // The next item is claimed two chunks before this one's last issue, when this
+        // CTA is about to run out of work: CTAs that finish early take the larger items
+        // still left (the order is longest first), and the claim's latency hides behind
+        // the stages already queued.
+        if (lane == 0 && i == max(n_chunks - 2, 0))
+          k_next = (int)gridDim.x + (int)atomicAdd(a.sched, 1u);
         const int k0 = it.t_begin + i * kChunk;
         const int nk = min(kChunk, it.t_end - k0);
         const int nbox = (nk + rb - 1) / rb;
@@ -913,8 +1001,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       if (!ok) break;
       const int k = __shfl_sync(0xffffffffu, k_next, 0);
-      have = find_item(k, s_off, ncat, R, P, Hkv, a.num_seqs, s_lt, s_nf, lane, it);
-      if (have && lane == 0) k_next = (int)gridDim.x + (int)atomicAdd(a.sched, 1u);
+      have = find_item(k, s_off, ncat, R, P, Hkv, T, a.num_seqs, s_lt, s_nf, lane, it);
     }
     if (ok) {  // no item follows: a stop marker in the next stage
       const int s = c % STAGES;
@@ -1229,7 +1316,8 @@ bool use_persistent(int32_t num_seqs, int32_t hkv, int32_t d, int32_t max_len, i
   const int64_t R = ((int64_t)max_len + P - 1) / P;
   const int64_t Q = P / kChunk;
   return units >= (int64_t)sms * split_occupancy(d) && num_seqs <= kMaxPersistSeqs &&
-         P % kChunk == 0 && Q < kMaxCategories && R - 1 + Q <= kMaxCategories;
+         P % kChunk == 0 && Q + kMergeChunks < kMaxCategories &&
+         R - 1 + Q + kMergeChunks <= kMaxCategories;
 }
 
 template <int D>

@@ -240,7 +240,11 @@ def _lens(n, lo, hi, seed, extra=()):
 
 
 # Many (sequence, kv head) units -- at least one wave of CTAs -- take the persistent
-# kernel (at most 1024 sequences); the batch over 1024 takes the grid kernel.
+# kernel (at most 1024 sequences); the batch over 1024 takes the grid kernel.  The
+# kernel's work order has two forms: where the single-partition items fill a wave of
+# CTAs (456 at D=64, 304 at D=128 on 152 SMs), the last partitions of multi-partition
+# sequences follow the full partitions (the last two cases); otherwise they are sorted
+# in by size.
 PERSIST_CASES = [
     # D, BS, Hq, Hkv, lens
     (64, 16, 16, 4, _lens(120, 0, 3000, 1, (0, 1, 63, 64, 1024, 1025, 2048, 3000, 0))),
@@ -249,6 +253,8 @@ PERSIST_CASES = [
     (64, 256, 4, 4, _lens(116, 1, 2100, 4, (1024, 2048, 1))),
     (64, 16, 2, 1, _lens(1100, 1, 300, 5)),
     (64, 16, 8, 1, tuple(3000 if b == 17 else 0 for b in range(500))),
+    (64, 16, 8, 1, _lens(600, 1, 600, 6, tuple(range(1600, 5000, 120)) + (0, 1536, 1537))),
+    (128, 16, 16, 2, _lens(205, 1, 500, 7, (2000, 3100, 4700, 1537, 1536, 0))),
 ]
 
 
