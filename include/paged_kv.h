@@ -125,8 +125,9 @@ int paged_kv_write_rope(const pkv_bf16 *k, const pkv_bf16 *v, pkv_bf16 *q, int32
  * kv head) units, one CTA streams one partition and P is chosen so that the
  * partitions make about one wave of CTAs on this GPU.  With many units (at least
  * a wave of CTAs), a persistent wave of CTAs streams the partitions as work items,
- * longest first, and P = 1536 (1024 for batches over 1024 sequences, which take one
- * CTA per partition).  P is never below min(max_context_len, 512) rounded up to 64,
+ * longest first, and P = 1536 (1024 for batches over 1024 sequences).  Batches
+ * over 1024 sequences, or with contexts over 39 * 1536 = 59904 tokens, take one CTA
+ * per partition instead.  P is never below min(max_context_len, 512) rounded up to 64,
  * so short contexts stay whole.  0 for empty or unsupported sizes.  num_sms <= 0
  * queries the current device.  Pure host function.
  */
@@ -141,8 +142,10 @@ int32_t paged_decode_plan(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_
  *   PKV_PATH_CLUSTER: few units with 2..8 partitions each: the partitions of one
  *     (sequence, kv head) form a thread-block cluster and merge through distributed
  *     shared memory;
- *   PKV_PATH_PERSISTENT: many units (at least a wave of CTAs): a persistent wave of
- *     CTAs streams the partitions as work items, longest first.
+ *   PKV_PATH_PERSISTENT: many units (at least a wave of CTAs), at most 1024
+ *     sequences, contexts up to 59904 tokens: a persistent wave of CTAs streams the
+ *     partitions as work items, longest first, with the merges of multi-partition
+ *     sequences kept away from the end.
  * 0 for empty or unsupported sizes.  num_sms <= 0 queries the current device.  Pure
  * host function.
  */

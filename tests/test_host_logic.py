@@ -53,6 +53,10 @@ def test_path_follows_the_plan(B):
     assert P(2048, 8, 1, 64, 8192) == B.PATH_PARTITIONS       # more sequences than its tables hold
     assert P(400, 8, 1, 64, 4096) == B.PATH_PARTITIONS        # 400 units < 456 slots: whole
     assert P(200, 8, 1, 64, 4096) == B.PATH_CLUSTER           # 2 partitions each, 400 CTAs
+    # the persistent kernel's work order has at most 64 categories: R - 1 full-partition
+    # levels + 24 + 2 last-partition sizes at P = 1536, so contexts up to 39 * 1536
+    assert P(600, 8, 1, 64, 59904) == B.PATH_PERSISTENT
+    assert P(600, 8, 1, 64, 59905) == B.PATH_PARTITIONS
     assert P(0, 8, 1, 64, 4096) == 0
     assert P(2, 16, 1, 64, 4096) == 0                         # unsupported group
 
