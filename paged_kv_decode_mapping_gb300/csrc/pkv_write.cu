@@ -34,7 +34,11 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const uint4 *__restrict__
     const int64_t rem = i - tok * row_vecs;
     const int64_t h = rem / vecs_per_row;
     const int64_t e = rem - h * vecs_per_row;
+    // the row's vectors are loaded together with its slot (i < num_vecs: always in
+    // bounds), so the write pays one memory latency, not two in a row
     const int64_t slot = __ldg(slot_mapping + tok);
+    const uint4 kv = __ldg(k + i);
+    const uint4 vv = __ldg(v + i);
     if (slot < 0) continue;  // padding
     const int64_t blk = slot / block_size;
     const int64_t off = slot - blk * block_size;
@@ -43,8 +47,6 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const uint4 *__restrict__
       continue;
     }
     const int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * vecs_per_row + e;
-    const uint4 kv = __ldg(k + i);
-    const uint4 vv = __ldg(v + i);
     k_cache[dst] = kv;
     v_cache[dst] = vv;
   }
@@ -150,6 +152,7 @@ __global__ void __launch_bounds__(256) kv_write_rope_kernel(const RopeArgs a) {
       const int heads = is_q ? a.num_q_heads : a.num_kv_heads;
       const int64_t tok = row / heads;
       const int64_t pos = __ldg(a.positions + tok);
+      const int64_t slot = is_q ? 0 : __ldg(a.slot_mapping + tok);  // in flight with pos
       if (pos < 0 || pos >= a.max_position) {
         if (u == 0 && row % heads == 0) atomicOr(&g_write_errors, (unsigned)PKV_DEVERR_POSITION);
         continue;
@@ -159,7 +162,6 @@ __global__ void __launch_bounds__(256) kv_write_rope_kernel(const RopeArgs a) {
         uint4 *qrow = a.q + row * vpr;
         rope_unit(qrow, qrow, cs, u, a);
       } else {
-        const int64_t slot = __ldg(a.slot_mapping + tok);
         if (slot < 0) continue;
         const int64_t blk = slot / a.block_size, off = slot - blk * a.block_size;
         if (blk >= a.num_blocks) {
@@ -176,11 +178,12 @@ __global__ void __launch_bounds__(256) kv_write_rope_kernel(const RopeArgs a) {
       const int64_t e = j - row * vpr;
       const int64_t tok = row / a.num_kv_heads;
       const int64_t slot = __ldg(a.slot_mapping + tok);
+      const uint4 vv = __ldg(a.v + j);  // in flight with the slot
       if (slot < 0) continue;
       const int64_t blk = slot / a.block_size, off = slot - blk * a.block_size;
       if (blk >= a.num_blocks) continue;  // reported by the k rows
       const int64_t h = row - tok * a.num_kv_heads;
-      a.v_cache[((blk * a.num_kv_heads + h) * a.block_size + off) * vpr + e] = __ldg(a.v + j);
+      a.v_cache[((blk * a.num_kv_heads + h) * a.block_size + off) * vpr + e] = vv;
     }
   }
 }
