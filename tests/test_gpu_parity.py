@@ -255,6 +255,8 @@ PERSIST_CASES = [
     (64, 16, 8, 1, tuple(3000 if b == 17 else 0 for b in range(500))),
     (64, 16, 8, 1, _lens(600, 1, 600, 6, tuple(range(1600, 5000, 120)) + (0, 1536, 1537))),
     (128, 16, 16, 2, _lens(205, 1, 500, 7, (2000, 3100, 4700, 1537, 1536, 0))),
+    (64, 16, 32, 4, _lens(300, 1, 4000, 9)),       # many multi-partition sequences, T > 0
+    (128, 16, 24, 8, _lens(60, 1, 6000, 10)),      # ... and T = 0
 ]
 
 
