@@ -585,15 +585,17 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int rank = (int)dev::cluster_ctarank();
       if (n == a.n_parts && n <= kMaxClusterParts) {
         const int hpo = (a.group + n - 1) / n;  // heads each CTA merges, at most
-        for (int i = tid; i < a.group * D; i += kConsumers) {
-          const int h = i / D, d = i - h * D;
-          float M2, den;
-          const float val = cta_merge<D>(r, a.group, h, d, &M2, &den);
+        for (int i = tid; i < a.group * D / 2; i += kConsumers) {  // two dims per store
+          const int h = i / (D / 2), d = 2 * (i - h * (D / 2));
+          float M2, den, M2b, denb;
+          const float v0 = cta_merge<D>(r, a.group, h, d, &M2, &den);
+          const float v1 = cta_merge<D>(r, a.group, h, d + 1, &M2b, &denb);
           const bool live = den > 0.f;  // false (or NaN) when this range had no keys
           const int slot = rank * hpo + h / n;
           const uint32_t dst = dev::mapa(recv, (uint32_t)(h % n));
           const uint32_t dbar = dev::mapa(bar_merge, (uint32_t)(h % n));
-          dev::st_async(dst + (uint32_t)(slot * D + d) * 4u, live ? val : 0.f, dbar);
+          dev::st_async_v2(dst + (uint32_t)(slot * D + d) * 4u, live ? v0 : 0.f, live ? v1 : 0.f,
+                           dbar);
           if (d == 0)
             dev::st_async(dst + (uint32_t)(kRecvSlots * D + slot) * 4u,
                           live ? M2 + log2f(den) : -INFINITY, dbar);

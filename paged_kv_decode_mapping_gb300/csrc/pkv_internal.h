@@ -273,6 +273,12 @@ __device__ __forceinline__ void st_async(uint32_t addr, float v, uint32_t bar) {
                ::"r"(addr), "f"(v), "r"(bar)
                : "memory");
 }
+// The same for two floats at an 8-byte aligned `addr` (8 bytes counted).
+__device__ __forceinline__ void st_async_v2(uint32_t addr, float v0, float v1, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+               ::"r"(addr), "f"(v0), "f"(v1), "r"(bar)
+               : "memory");
+}
 // mbar_wait with acquire at cluster scope: what other CTAs of the cluster wrote to this
 // CTA's shared memory before completing the phase is visible after it returns true.
 // Same ~2 s limit.
