@@ -319,6 +319,8 @@ int paged_decode_combine(pkv_bf16 *out, const float *o_part, const float *lse_pa
  *  - Sizes whose plan needs more than PKV_NOALLOC_SCRATCH_BYTES of workspace
  *    (paged_decode_workspace_size) are rejected with PKV_ERR_WORKSPACE and a message;
  *    use paged_decode_attention with your own workspace for those.
+ *  - Every argument check of paged_decode_attention runs first: a refused call
+ *    returns its PKV_ERR_* code with nothing enqueued and the array untouched.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress) and caches it; make that first call outside any CUDA
  *    stream capture.

@@ -1577,6 +1577,20 @@ int decode_fused(pkv_bf16 *out, const pkv_bf16 *q, const pkv_bf16 *k_cache,
 }
 
 }  // namespace
+
+int check_decode_attention(const pkv_bf16 *out, const pkv_bf16 *q, const pkv_bf16 *k_cache,
+                           const pkv_bf16 *v_cache, const int32_t *block_tables,
+                           int32_t max_blocks_per_seq, const int32_t *context_lens,
+                           int32_t max_context_len, int32_t num_seqs, int32_t num_q_heads,
+                           const pkv_cache_desc *cache, size_t workspace_bytes, const char *fn) {
+  // Without a launch, decode_fused looks at the workspace pointer only to reject a NULL
+  // or misaligned one; this stands for the caller's aligned buffer and is never used.
+  void *const aligned_stand_in = reinterpret_cast<void *>(uintptr_t(256));
+  return decode_fused(const_cast<pkv_bf16 *>(out), q, k_cache, v_cache, block_tables,
+                      max_blocks_per_seq, context_lens, max_context_len, num_seqs, num_q_heads,
+                      cache, 1.f, aligned_stand_in, workspace_bytes, nullptr, false, false, fn);
+}
+
 }  // namespace pkv
 
 PKV_API int paged_decode_attention(pkv_bf16 *out, const pkv_bf16 *q, const pkv_bf16 *k_cache,

@@ -89,6 +89,15 @@ int check_decode(const void *q, const void *k_cache, const void *v_cache, const 
                  int32_t max_blocks, const int32_t *lens, int32_t max_len, int32_t num_seqs,
                  int32_t hq, const pkv_cache_desc *c, const char *fn);
 int ilog2(int x);  // smallest r with 2^r >= x
+// Every host check paged_decode_attention makes (shape, pointers, alignment, the
+// planned workspace against `workspace_bytes`), without enqueuing anything, for a caller
+// whose workspace is a fixed, 256-byte aligned buffer of `workspace_bytes`; `fn` names
+// the caller in the error message.
+int check_decode_attention(const pkv_bf16 *out, const pkv_bf16 *q, const pkv_bf16 *k_cache,
+                           const pkv_bf16 *v_cache, const int32_t *block_tables,
+                           int32_t max_blocks_per_seq, const int32_t *context_lens,
+                           int32_t max_context_len, int32_t num_seqs, int32_t num_q_heads,
+                           const pkv_cache_desc *cache, size_t workspace_bytes, const char *fn);
 
 // Device error words of the attention translation units (read + optional clear).
 cudaError_t read_decode_errors(uint32_t *flags, int clear);

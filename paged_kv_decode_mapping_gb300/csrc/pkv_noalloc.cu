@@ -61,31 +61,42 @@ PKV_API int paged_decode_attention_noalloc(pkv_bf16 *out, const pkv_bf16 *q,
                                            const pkv_cache_desc *cache, float scale,
                                            void *stream) {
   using namespace pkv;
-  if (!cache) return set_error(PKV_ERR_NULL, "paged_decode_attention_noalloc: cache descriptor is NULL");
+  static const char *const kFn = "paged_decode_attention_noalloc";
+  if (!cache) return set_error(PKV_ERR_NULL, "%s: cache descriptor is NULL", kFn);
   if (num_seqs < 0 || num_q_heads <= 0 || cache->num_kv_heads <= 0 || max_context_len < 0)
-    return set_error(PKV_ERR_SHAPE, "paged_decode_attention_noalloc: bad sizes");
+    return set_error(PKV_ERR_SHAPE, "%s: bad sizes", kFn);
   // The size the launcher's plan needs, checked before any device call.
   const size_t need = paged_decode_workspace_size(num_seqs, num_q_heads, cache->num_kv_heads,
                                                   cache->head_dim, max_context_len);
   if (need > kNoAllocScratchBytes)
     return set_error(PKV_ERR_WORKSPACE,
-                     "paged_decode_attention_noalloc: these sizes need %zu bytes of partition "
-                     "workspace, more than the library's fixed %zu-byte scratch; call "
-                     "paged_decode_attention with a workspace instead",
-                     need, kNoAllocScratchBytes);
+                     "%s: these sizes need %zu bytes of partition workspace, more than the "
+                     "library's fixed %zu-byte scratch; call paged_decode_attention with a "
+                     "workspace instead",
+                     kFn, need, kNoAllocScratchBytes);
+  // Every argument check of paged_decode_attention, before any device call: a call
+  // that is refused leaves nothing queued on the stream and never touches the array.
+  int rc = check_decode_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                  context_lens, max_context_len, num_seqs, num_q_heads, cache,
+                                  kNoAllocScratchBytes, kFn);
+  if (rc) return rc;
+  if (num_seqs == 0) {
+    clear_error();
+    return PKV_OK;
+  }
   // First call on this device: look up the array's device address (see the header).
   void *scratch = nullptr;
-  int rc = scratch_address(&scratch);
+  rc = scratch_address(&scratch);
   if (rc) return rc;
   // The decode keeps one completion counter per (sequence, kv head), then two work
   // scheduling words, at the start of its workspace; they must be zero when the kernel
   // starts.  A completed call leaves them zero, but clear them anyway so a call never
-  // depends on the previous one.
-  if (num_seqs > 0) {
-    const cudaError_t e = cudaMemsetAsync(scratch, 0, (size_t)num_seqs * cache->num_kv_heads * 4 + 8,
-                                          static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_error(e, "paged_decode_attention_noalloc: clear counters");
-  }
+  // depends on the previous one.  The plan was accepted above, so `need` covers them
+  // and lies within the array.
+  size_t clear = (size_t)num_seqs * cache->num_kv_heads * 4 + 8;
+  if (clear > need) clear = need;
+  const cudaError_t e = cudaMemsetAsync(scratch, 0, clear, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_error(e, "paged_decode_attention_noalloc: clear counters");
   return paged_decode_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                 context_lens, max_context_len, num_seqs, num_q_heads, cache,
                                 scale, scratch, kNoAllocScratchBytes, stream);

@@ -310,22 +310,39 @@ def pin_rope_zero_angle_is_identity(o):
     assert torch.equal(qr.view(torch.int16), q.view(torch.int16))
 
 
+def _rope_exact(x: torch.Tensor, cs: torch.Tensor, pos: torch.Tensor) -> torch.Tensor:
+    """Rotate-half pairs (i, i + D/2) of x [T, H, D] as the complex product
+    (x_i + i x_{i+D/2}) e^{i angle(pos, i)} in complex128, angle from the table cs."""
+    half = x.shape[-1] // 2
+    xd = x.double()
+    z = torch.complex(xd[..., :half], xd[..., half:])
+    c = cs.double()[pos][:, None, :half]
+    s = cs.double()[pos][:, None, half:]
+    zr = z * torch.complex(c, s)
+    return torch.cat([zr.real, zr.imag], dim=-1)
+
+
+def _within_bf16_rounding(y: torch.Tensor, exact: torch.Tensor, x: torch.Tensor) -> bool:
+    err = (y.double() - exact).abs()
+    return bool((err <= 2.0 ** -8 * exact.abs() + 1e-6 * (1 + x.double().abs())).all())
+
+
 def pin_rope_is_complex_rotation(o):
     """Each pair (x1, x2) becomes (x1 + i x2) * e^{i angle}, computed independently in
-    complex128; the oracle's fp32-then-bf16 result is within bf16 rounding of it."""
+    complex128; the oracle's fp32-then-bf16 result is within bf16 rounding of it.  Both
+    the query rotated in place and the keys as they land in the cache (each token at
+    its own nonzero position, every kv head), since the cache must hold keys rotated at
+    their absolute positions."""
     k, v, q, kc = _rope_case(T=6, D=32)
     cs = rope_table(50, 32).float()
-    pos = torch.tensor([0, 1, 7, 13, 31, 49], dtype=torch.int64)
-    kr, _, qr = o.kv_write_rope(k, v, torch.full((6,), -1, dtype=torch.int64), pos, cs, kc, kc, q=q)
-    for x, y in ((q, qr),):
-        xd = x.double()
-        z = torch.complex(xd[..., :16], xd[..., 16:])
-        c = cs.double()[pos][:, None, :16]
-        s = cs.double()[pos][:, None, 16:]
-        zr = z * torch.complex(c, s)
-        exact = torch.cat([zr.real, zr.imag], dim=-1)
-        err = (y.double() - exact).abs()
-        assert bool((err <= 2.0 ** -8 * exact.abs() + 1e-6 * (1 + xd.abs())).all()), err.max()
+    pos = torch.tensor([3, 1, 7, 13, 31, 49], dtype=torch.int64)
+    slots = torch.tensor([5, 0, 15, 8, 2, 11], dtype=torch.int64)  # in a 4-block x 4-slot pool
+    kc_out, vc_out, qr = o.kv_write_rope(k, v, slots, pos, cs, kc, kc, q=q)
+    assert _within_bf16_rounding(qr, _rope_exact(q, cs, pos), q), "q"
+    kr = torch.stack([kc_out[int(sl) // 4, :, int(sl) % 4, :] for sl in slots])  # [T, Hkv, D]
+    vr = torch.stack([vc_out[int(sl) // 4, :, int(sl) % 4, :] for sl in slots])
+    assert _within_bf16_rounding(kr, _rope_exact(k, cs, pos), k), "k in the cache"
+    assert torch.equal(vr.view(torch.int16), v.view(torch.int16)), "v is copied, not rotated"
 
 
 def pin_rope_pairing_permutation(o):
@@ -343,19 +360,29 @@ def pin_rope_pairing_permutation(o):
 
 
 def pin_rope_relative_position(o):
-    """<R(m) q, R(n) k> depends only on m - n (up to bf16 rounding of the rotated vectors)."""
+    """<R(m) q, R(n) k> depends only on m - n (up to bf16 rounding of the rotated vectors):
+    q rotated in place at m, k rotated through the write at n and read back from the
+    cache slot it was written to."""
     k, v, q, kc = _rope_case(T=1, Hkv=1, Hq=1, D=64, seed=4)
     cs = rope_table(200, 64).float()
     none = torch.full((1,), -1, dtype=torch.int64)
+    slot = torch.tensor([6], dtype=torch.int64)
 
-    def rot(x, p):
-        _, _, y = o.kv_write_rope(k, v, none, torch.tensor([p]), cs, kc[:, :1], kc[:, :1], q=x)
+    def rot_q(p):
+        _, _, y = o.kv_write_rope(k, v, none, torch.tensor([p]), cs, kc[:, :1], kc[:, :1], q=q)
         return y.double().flatten()
 
-    base = float(rot(q, 40) @ rot(k.reshape(1, 1, 64), 25))
+    def rot_k(p):
+        kc1, _, _ = o.kv_write_rope(k, v, slot, torch.tensor([p]), cs, kc[:, :1], kc[:, :1])
+        return kc1[1, 0, 2].double()  # slot 6 = block 1, offset 2
+
+    base = float(rot_q(40) @ rot_k(25))
+    assert abs(base - float(q.double().flatten() @ k.double().flatten())) > 1e-3  # rotation matters
     for d in (0, 17, 100, 150):
-        other = float(rot(q, 40 + d) @ rot(k.reshape(1, 1, 64), 25 + d))
+        other = float(rot_q(40 + d) @ rot_k(25 + d))
         assert abs(other - base) < 0.05 * (1 + abs(base)), (d, other, base)
+    # and a different offset m - n gives a different product
+    assert abs(float(rot_q(40) @ rot_k(29)) - base) > 1e-3
 
 
 def pin_rope_partial_rotary(o):

@@ -148,3 +148,26 @@ def test_empty_batch_is_a_no_op(B):
     d = _desc(B)
     assert lib.paged_decode_attention(None, None, None, None, None, 8, None, 0, 0, 8,
                                       ctypes.byref(d), 0.1, None, 0, None) == 0
+
+
+def test_noalloc_refuses_bad_arguments_before_any_device_work(B):
+    """The allocation-free decode runs every host check before it touches its fixed
+    scratch array.  Shapes the launcher cannot plan (workspace size 0) used to slip past
+    the size check into a clear of num_seqs * num_kv_heads counters; with 65535 x 256
+    of them that clear alone would be 64 MiB, twice the array.  Each must come back
+    with an error on the host (no GPU here: any device work would fail differently)."""
+    lib = B.lib()
+
+    def call(desc, hq, n=65535, max_len=64, max_blocks=4, out=FAKE, q=FAKE):
+        return lib.paged_decode_attention_noalloc(out, q, FAKE, FAKE, FAKE, max_blocks, FAKE,
+                                                  max_len, n, hq, ctypes.byref(desc), 0.1, None)
+
+    assert B.paged_decode_workspace_size(65535, 256, 256, 96, 64) == 0
+    assert call(_desc(B, hkv=256, d=96), 256) == -3 and "head_dim" in B.pkv_last_error()
+    assert call(_desc(B, hkv=16), 256) == -3 and "group" in B.pkv_last_error()   # group 16
+    assert call(_desc(B, hkv=3), 256) == -2                                        # 256 % 3
+    assert call(_desc(B, hkv=8), 64, n=70000) in (-3, -4)                          # > 65535 sequences
+    assert call(_desc(B, hkv=2), 8, n=2, out=None) == -1
+    assert call(_desc(B, hkv=2), 8, n=2, q=ctypes.c_void_p((1 << 20) + 4)) == -5
+    assert call(_desc(B, hkv=2), 8, n=2, max_len=100) == -2                       # over the table
+    assert call(_desc(B, hkv=2), 8, n=0, out=None, q=None) == 0                   # nothing to do

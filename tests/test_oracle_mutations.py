@@ -46,6 +46,13 @@ MUTATIONS = {
                                   "attend_range(out + row, &lse, qd, Kd, Vd, 0, pos, head_dim, scale, s);"),
     "prefill_position_from_chunk_start": ("const int32_t pos = len - n + i;",
                                           "const int32_t pos = i;"),
+    "rope_k_at_position_zero": ("rope_row(krot + o, k + o, cs, head_dim, rotary_dim, neox_style);",
+                                "rope_row(krot + o, k + o, cos_sin, head_dim, rotary_dim, neox_style);"),
+    "rope_k_unrotated": ("rope_row(krot + o, k + o, cs, head_dim, rotary_dim, neox_style);",
+                         "rope_row(krot + o, k + o, cs, head_dim, 0, neox_style);"),
+    "rope_k_row_of_head_zero": (
+        "rope_row(krot + o, k + o, cs, head_dim, rotary_dim, neox_style);",
+        "rope_row(krot + o, k + i * num_kv_heads * (int64_t)head_dim, cs, head_dim, rotary_dim, neox_style);"),
     "q_row_of_wrong_head": (
         "qd[d] = oracle_bf16_to_double(q[((int64_t)b * num_q_heads + h) * head_dim + d]);",
         "qd[d] = oracle_bf16_to_double(q[((int64_t)b * num_q_heads + (h ^ 1)) * head_dim + d]);"),

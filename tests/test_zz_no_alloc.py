@@ -92,3 +92,66 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(B):
     rc = B.lib().paged_decode_attention_noalloc(fake, fake, fake, fake, fake, L // BS, fake, L, Bn,
                                                 Hq, ctypes.byref(d), 0.1, None)
     assert rc == -4 and "scratch" in B.pkv_last_error()
+
+
+def _cudart():
+    # the CUDA runtime libpkv.so is linked against (already loaded, found by its soname)
+    for name in ("libcudart.so.13", "libcudart.so"):
+        try:
+            return ctypes.CDLL(name)
+        except OSError:
+            continue
+    pytest.skip("libcudart not loadable by name")
+
+
+def _captured_nodes(rt, stream, fn) -> int:
+    """Runs fn() while `stream` is being captured into a CUDA graph (relaxed mode) and
+    returns how many nodes the graph got.  Nothing captured is ever launched."""
+    assert rt.cudaStreamBeginCapture(ctypes.c_void_p(stream.cuda_stream), 2) == 0
+    try:
+        fn()
+    finally:
+        graph = ctypes.c_void_p()
+        assert rt.cudaStreamEndCapture(ctypes.c_void_p(stream.cuda_stream), ctypes.byref(graph)) == 0
+    n = ctypes.c_size_t(0)
+    assert rt.cudaGraphGetNodes(graph, None, ctypes.byref(n)) == 0
+    assert rt.cudaGraphDestroy(graph) == 0
+    return int(n.value)
+
+
+def test_noalloc_refused_calls_enqueue_nothing(B):
+    """Arguments the launcher cannot plan (head_dim 96, a query group over 8) with
+    65535 x 256 (sequence, kv head) units -- enough counters that clearing them would
+    overrun the fixed array twice over -- are refused before anything reaches the
+    stream: captured on a side stream, the refused calls add no node to the graph,
+    while an accepted call adds its clear and its kernel."""
+    rt = _cudart()
+    w = W.small_workload(B=2, Hq=8, Hkv=2, D=64, BS=16, lens=(900, 40), seed=44, write="none")
+    g = {k: (v.cuda() if isinstance(v, torch.Tensor) else v)
+         for k, v in W.make_inputs(w).items()}
+    out = torch.empty_like(g["q"])
+    assert _noalloc(B, out, g) == 0  # first call on this device: set-up outside capture
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    fake = ctypes.c_void_p(1 << 20)
+
+    def refused():
+        for hkv, d in ((256, 96), (16, 64)):
+            desc = B.pkv_cache_desc(16, 16, hkv, d)
+            rc = B.lib().paged_decode_attention_noalloc(fake, fake, fake, fake, fake, 4, fake, 64,
+                                                        65535, 256, ctypes.byref(desc), 0.1,
+                                                        ctypes.c_void_p(s.cuda_stream))
+            assert rc == -3, (hkv, d, rc)
+
+    def accepted():
+        d = B.cache_desc(g["k_cache"])
+        rc = B.lib().paged_decode_attention_noalloc(
+            out.data_ptr(), g["q"].data_ptr(), g["k_cache"].data_ptr(), g["v_cache"].data_ptr(),
+            g["block_tables"].data_ptr(), g["block_tables"].shape[1], g["context_lens"].data_ptr(),
+            g["max_context_len"], 2, 8, ctypes.byref(d), g["scale"], ctypes.c_void_p(s.cuda_stream))
+        assert rc == 0, B.pkv_last_error()
+
+    assert _captured_nodes(rt, s, refused) == 0
+    assert _captured_nodes(rt, s, accepted) >= 2
+    torch.cuda.synchronize()
+    assert B.pkv_device_errors(clear=True) == 0
