@@ -1,6 +1,6 @@
 """Benchmark of one paged-KV decode step on GB300: slot write + decode attention.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 2]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 3]
 
 A step is one pass of the whole hot path over one batch of synthetic input, through
 paged_decode_step: the slot-mapping KV write of the step's new tokens, then decode
@@ -8,9 +8,12 @@ attention (launched as a programmatic dependent of the write) as the
 launcher plans it (one kernel: one CTA per partition; split sequences are merged by
 their last partition).
 
-Default workload: decode B=16, context 2048, 32 query / 8 kv heads, head_dim 64,
-bf16, block_size 16, block tables drawn from a shuffled pool of 2560 blocks, 16
-new tokens written per step.
+Default workload: the largest single-GPU step, a decode batch of 64 sequences with
+ragged contexts uniform in [128, 4096], 24 query / 8 kv heads, head_dim 128, bf16,
+block_size 16, block tables drawn from a shuffled pool of 1.25x the blocks in use,
+64 new tokens written per step (about 554 MB of K/V read per step).  The other
+workloads (--workload 1..5) are the batch-1 / batch-16 / continuous-batching /
+long-context shapes of the same path.
 
 Timing (ours): inputs are resident in HBM; the pool is replicated R times so that
 the copies together exceed 3x the L2 size, and step i uses copy i mod R (so every
@@ -274,7 +277,8 @@ def config_dict(w, inp, args, world: int) -> dict:
             "head_dim": w.D, "block_size": w.BS, "context": f"{w.lens}:{int(inp['context_lens'].min())}"
             f"..{int(inp['context_lens'].max())}", "pool_blocks": inp["num_blocks"],
             "new_tokens_per_step": int(inp["slot_mapping"].numel()), "seed": w.seed,
-            "l2": "rotating pool copies > 3x L2 between steps", "parallelism": f"replicas x{world}"}
+            "l2": "rotating pool copies > 3x L2 between steps", "parallelism": f"replicas x{world}",
+            "consumer": args.consumer}
 
 
 # ----------------------------------------------------------------------------- ours
@@ -363,8 +367,36 @@ def run_ours(args, w) -> None:
 
     clocks = ClockSampler(local)
     t_step = timed(*g_step)
-    clk = clocks.stop()
+    clk_timed = clocks.stop()
     t_dec = timed(*g_dec)
+
+    # Clock record: the timed region above can be far shorter than nvidia-smi's 100 ms
+    # sampling period, so the same step graph is also replayed back to back for a window
+    # of about 1.5 s (outside the timed region) while the clocks are sampled; its own
+    # step time is reported beside the clocks as a cross-check of the timed number.
+    def clock_window(full, seconds=1.5):
+        sampler = ClockSampler(local)
+        time.sleep(0.25)  # let nvidia-smi start before the load
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 0
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            while time.perf_counter() - t0 < seconds:
+                for _ in range(20):
+                    full.replay()
+                reps += 20
+                stream.synchronize()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        c = sampler.stop()
+        c["window_s"] = round(time.perf_counter() - t0, 3)
+        c["window_us_per_step"] = e0.elapsed_time(e1) * 1e3 / (reps * R)
+        c["timed_region_samples"] = clk_timed.get("samples", 0)
+        c["timed_region_reasons"] = clk_timed.get("reasons", [])
+        return c
+
+    clk = clock_window(g_step[0])
 
     # spread of the step time: 200 replays of the R-step graph, each timed by its own
     # events on the stream (outside the timed region above)
@@ -448,6 +480,40 @@ def run_ours(args, w) -> None:
     t_e2e_eager = time_e2e(e2e_body)
     e2e_value = reduce_sum(nb["step"], world, device) / t_e2e / 1e9
 
+    # Where the end-to-end time goes: the device time of the two copies (each measured
+    # as 20 copies in one graph, back to back), the device time of the step (the timed
+    # region above), the step alone replayed and synchronised per step (no copies), and
+    # the rest -- graph launch, host synchronise and the gaps between -- as the remainder.
+    def copies_us(fn, n=20) -> float:
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            for _ in range(n):
+                fn()
+        with torch.cuda.stream(stream):
+            gr.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(10):
+                gr.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / (10 * n)
+
+    h2d_us = copies_us(lambda: stage_d.copy_(stage_h, non_blocking=True))
+    d2h_us = copies_us(lambda: out_h.copy_(out, non_blocking=True))
+    step_graphs = []
+    for r in range(R):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            step(r)
+        step_graphs.append(gr)
+    t_step_sync = time_e2e(lambda r: step_graphs[r].replay())
+    breakdown = {"h2d_us": h2d_us, "step_us": us_step, "d2h_us": d2h_us,
+                 "launch_sync_us": t_e2e * 1e6 - (h2d_us + us_step + d2h_us),
+                 "step_alone_replayed_and_synchronised_us": t_step_sync * 1e6}
+
     peaks = measured_peaks()
     peak = peaks.get("hbm_gbs")
     peak_src = "measured" if peak else "fallback"
@@ -484,7 +550,7 @@ def run_ours(args, w) -> None:
                 "d2h_bytes_per_step": d2h, "us_per_step": t_e2e * 1e6,
                 "how": "one pinned H2D copy of the step's inputs + paged_decode_step + D2H of "
                        "out, one CUDA graph replayed and synchronised per step",
-                "eager_us_per_step": t_e2e_eager * 1e6},
+                "eager_us_per_step": t_e2e_eager * 1e6, "breakdown": breakdown},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
@@ -558,6 +624,22 @@ def run_kernel(args, w) -> None:
         unit, per = "GB/s", nbytes / 1e9
         bound, peak = "hbm", peaks.get("hbm_gbs") or 6800.0
         metric = "decode step with RoPE (rotary write + fused decode) GB/s"
+    elif args.kernel == "split":
+        nb = algorithmic_bytes(inp)
+        P = args.partition
+        n = math.ceil(inp["max_context_len"] / P)
+        qd = inp["q"].to(device)
+        o_part = torch.empty(Bn, Hq, n, D, device=device)
+        lse = torch.empty(Bn, Hq, n, device=device)
+        out = torch.empty_like(qd)
+
+        def fn(r):
+            B.paged_decode_split(o_part, lse, qd, kcs[r], vcs[r], bt, cl, inp["max_context_len"],
+                                 inp["scale"], P)
+            B.paged_decode_combine(out, o_part, lse, cl, inp["max_context_len"], P)
+        unit, per = "GB/s", nb["decode_kernel"] / 1e9
+        bound, peak = "hbm", peaks.get("hbm_gbs") or 6800.0
+        metric = f"decode attention as paged_decode_split (P={P}) + paged_decode_combine GB/s"
     else:  # rope_write
         T = Bn
         kn = torch.randn(T, Hkv, D, generator=gen).to(torch.bfloat16).to(device)
@@ -607,7 +689,7 @@ def run_kernel(args, w) -> None:
                  "steps": reps * R, "higher_is_better": True,
                  "roofline": {"bound": bound, "achieved": value, "peak": peak, "unit": unit,
                               "frac": value / peak, "traffic": None},
-                 "gpu_launches": (2 if args.kernel == "rope_step" else 1) * reps * R,
+                 "gpu_launches": (2 if args.kernel in ("rope_step", "split") else 1) * reps * R,
                  "clocks": clk})
     print(json.dumps(line), flush=True)
 
@@ -618,14 +700,24 @@ def main():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", type=int, default=2, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--workload", type=int, default=3, choices=sorted(W.WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for the cpu_baseline object (0: skip)")
-    ap.add_argument("--kernel", choices=["step", "prefill", "rope_write", "rope_step"], default="step",
-                    help="step: the decode step (the benchmark line); others time one kernel")
+    ap.add_argument("--kernel", choices=["step", "prefill", "rope_write", "rope_step", "split"],
+                    default="step",
+                    help="step: the decode step (the benchmark line); others time one kernel; "
+                         "split: paged_decode_split + paged_decode_combine at --partition")
     ap.add_argument("--chunk", type=int, default=512, help="prefill: query tokens per sequence")
+    ap.add_argument("--consumer", choices=["tensor", "fma"], default="tensor",
+                    help="arithmetic of the partition decode kernel's consumer warps")
+    ap.add_argument("--partition", type=int, default=1024,
+                    help="split: partition size in tokens (a multiple of 64)")
     args = ap.parse_args()
     w = W.WORKLOADS[args.workload]
+    if args.consumer != "tensor":
+        from paged_kv_decode_mapping_gb300 import binding as B
+
+        B.pkv_set_decode_consumer(B.CONSUMER_FMA)
     if args.kernel != "step":
         run_kernel(args, w)
     elif args.impl == "reference":

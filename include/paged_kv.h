@@ -154,6 +154,25 @@ int32_t paged_decode_path(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_
                           int32_t head_dim, int32_t max_context_len, int32_t num_sms);
 
 /*
+ * pkv_set_decode_consumer -- the arithmetic of the consumer warps of the partition
+ * decode kernel, process-wide (every later launch on any stream or device).  Both
+ * forms take bf16 inputs and accumulate exact bf16 products in fp32 ("llm-stack",
+ * Attention kernel); they differ only in the units that do it:
+ *   PKV_CONSUMER_TENSOR (default): the group's scores and P.V as mma.sync tiles
+ *     (16 keys x 8 heads), P entering P.V as a bf16 hi + lo pair;
+ *   PKV_CONSUMER_FMA: fp32 FMAs on the CUDA cores (mixed bf16 x bf16 + fp32 FMAs for
+ *     the scores, P in fp32 for P.V), with warp shuffles to combine and spread values.
+ * It applies to the PKV_PATH_PARTITIONS and PKV_PATH_CLUSTER arrangements and to
+ * paged_decode_split; the persistent arrangement always uses the tensor form.  The
+ * CUDA-core form is kept so that the two can be measured against each other on the
+ * same shapes; the default is the tensor form.  Returns the previous form, or
+ * PKV_ERR_UNSUPPORTED for an unknown one.  Host function; not synchronised with
+ * launches already queued.
+ */
+enum { PKV_CONSUMER_TENSOR = 0, PKV_CONSUMER_FMA = 1 };
+int32_t pkv_set_decode_consumer(int32_t consumer);
+
+/*
  * paged_decode_workspace_size -- bytes of workspace paged_decode_attention needs for
  * these sizes on the current device: a completion counter per (sequence, kv head),
  * then the partition results of paged_decode_split's layout for P =

@@ -68,7 +68,7 @@ class Oracle:
                                            i32, i32, i32]
         L.oracle_kv_write_rope.restype = ctypes.c_int
         L.oracle_prefill_attention.argtypes = [P, P, P, P, P, i32, P, P, i32, i32, i32, i64, i32,
-                                               i32, dbl]
+                                               i32, dbl, i32]
         L.oracle_prefill_attention.restype = ctypes.c_int
         self._L = L
 
@@ -164,7 +164,7 @@ class Oracle:
         return torch.from_numpy(out)
 
     def prefill(self, q, k_cache, v_cache, block_tables, context_lens, query_start,
-                scale: float) -> torch.Tensor:
+                scale: float, num_threads: int = 0) -> torch.Tensor:
         """fp64 causal attention of each sequence's last n_b tokens (packed q [Nq, Hq, D])."""
         Nq, Hq, D = q.shape
         NB, Hkv, BS, _ = k_cache.shape
@@ -175,7 +175,8 @@ class Oracle:
         out = np.zeros((Nq, Hq, D), dtype=np.float64)
         rc = self._L.oracle_prefill_attention(self._p(out), self._p(qa), self._p(ka), self._p(va),
                                               self._p(bt), bt.shape[1], self._p(cl), self._p(qs),
-                                              len(cl), Hq, Hkv, NB, BS, D, float(scale))
+                                              len(cl), Hq, Hkv, NB, BS, D, float(scale),
+                                              num_threads)
         self._check(rc, "prefill")
         return torch.from_numpy(out)
 

@@ -408,45 +408,62 @@ int oracle_kv_write_rope(const uint16_t *k, const uint16_t *v, uint16_t *q, int3
  * tokens, of which the last n_b = query_start[b+1] - query_start[b] are this chunk's
  * queries; query i of the chunk sits at position p = L_b - n_b + i and attends to keys
  * t <= p (causal).  q and out are packed [num_queries][num_q_heads][head_dim] with
- * sequence b's queries at rows query_start[b] .. query_start[b+1]-1.  fp64. */
+ * sequence b's queries at rows query_start[b] .. query_start[b+1]-1.  fp64.
+ * The (sequence, kv head) pairs are independent and are shared out over threads
+ * (OpenMP; num_threads <= 0: all); each pair's arithmetic is the same either way. */
 int oracle_prefill_attention(double *out, const uint16_t *q, const uint16_t *k_cache,
                              const uint16_t *v_cache, const int32_t *block_tables,
                              int32_t max_blocks_per_seq, const int32_t *context_lens,
                              const int32_t *query_start, int32_t num_seqs, int32_t num_q_heads,
                              int32_t num_kv_heads, int64_t num_blocks, int32_t block_size,
-                             int32_t head_dim, double scale) {
+                             int32_t head_dim, double scale, int32_t num_threads) {
   int rc = check_decode_args(context_lens, num_seqs, num_q_heads, num_kv_heads, num_blocks,
                              block_size, head_dim, max_blocks_per_seq);
   if (rc) return rc;
-  const int32_t group = num_q_heads / num_kv_heads;
   for (int32_t b = 0; b < num_seqs; ++b) {
+    const int32_t n = query_start[b + 1] - query_start[b];
+    if (n < 0 || n > context_lens[b]) return ORACLE_ERR_LEN;
+  }
+  const int32_t group = num_q_heads / num_kv_heads;
+  const int64_t pairs = (int64_t)num_seqs * num_kv_heads;
+  int err = ORACLE_OK;
+#ifdef _OPENMP
+  if (num_threads <= 0) num_threads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads)
+#endif
+  for (int64_t pg = 0; pg < pairs; ++pg) {
+    const int32_t b = (int32_t)(pg / num_kv_heads), g = (int32_t)(pg % num_kv_heads);
     const int32_t len = context_lens[b];
     const int32_t n = query_start[b + 1] - query_start[b];
-    if (n < 0 || n > len) return ORACLE_ERR_LEN;
     double *Kd = (double *)malloc(sizeof(double) * ((size_t)len * head_dim + 1));
     double *Vd = (double *)malloc(sizeof(double) * ((size_t)len * head_dim + 1));
     double *s = (double *)malloc(sizeof(double) * ((size_t)len + 1));
     double *qd = (double *)malloc(sizeof(double) * (size_t)head_dim);
-    if (!Kd || !Vd || !s || !qd) rc = ORACLE_ERR_NOMEM;
-    for (int32_t g = 0; g < num_kv_heads && !rc; ++g) {
-      rc = gather_dense(Kd, Vd, k_cache, v_cache, block_tables + (int64_t)b * max_blocks_per_seq,
-                        len, num_blocks, num_kv_heads, block_size, head_dim, g);
-      for (int32_t i = 0; i < n && !rc; ++i) {
-        const int32_t pos = len - n + i;
-        for (int32_t j = 0; j < group; ++j) {
-          const int32_t h = g * group + j;
-          const int64_t row = ((int64_t)(query_start[b] + i) * num_q_heads + h) * head_dim;
-          for (int32_t d = 0; d < head_dim; ++d) qd[d] = oracle_bf16_to_double(q[row + d]);
-          double lse;
-          attend_range(out + row, &lse, qd, Kd, Vd, 0, pos + 1, head_dim, scale, s);
-        }
+    int prc = ORACLE_OK;
+    if (!Kd || !Vd || !s || !qd) prc = ORACLE_ERR_NOMEM;
+    if (!prc)
+      prc = gather_dense(Kd, Vd, k_cache, v_cache, block_tables + (int64_t)b * max_blocks_per_seq,
+                         len, num_blocks, num_kv_heads, block_size, head_dim, g);
+    for (int32_t i = 0; i < n && !prc; ++i) {
+      const int32_t pos = len - n + i;
+      for (int32_t j = 0; j < group; ++j) {
+        const int32_t h = g * group + j;
+        const int64_t row = ((int64_t)(query_start[b] + i) * num_q_heads + h) * head_dim;
+        for (int32_t d = 0; d < head_dim; ++d) qd[d] = oracle_bf16_to_double(q[row + d]);
+        double lse;
+        attend_range(out + row, &lse, qd, Kd, Vd, 0, pos + 1, head_dim, scale, s);
       }
     }
     free(Kd);
     free(Vd);
     free(s);
     free(qd);
-    if (rc) return rc;
+    if (prc) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+      err = prc;
+    }
   }
-  return ORACLE_OK;
+  return err;
 }

@@ -56,6 +56,8 @@ _lib.paged_decode_plan.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
 _lib.paged_decode_plan.restype = _i32
 _lib.paged_decode_path.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
 _lib.paged_decode_path.restype = _i32
+_lib.pkv_set_decode_consumer.argtypes = [_i32]
+_lib.pkv_set_decode_consumer.restype = _i32
 _lib.paged_decode_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32]
 _lib.paged_decode_workspace_size.restype = _sz
 _lib.paged_decode_split_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32]
@@ -185,6 +187,16 @@ def paged_kv_write_rope(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Te
 
 
 PATH_PARTITIONS, PATH_CLUSTER, PATH_PERSISTENT = 1, 2, 3
+CONSUMER_TENSOR, CONSUMER_FMA = 0, 1
+
+
+def pkv_set_decode_consumer(consumer: int) -> int:
+    """Selects the consumer warps' arithmetic of the partition decode kernel (CONSUMER_*);
+    returns the previous one."""
+    rc = int(_lib.pkv_set_decode_consumer(consumer))
+    if rc < 0:
+        _check(rc, "pkv_set_decode_consumer")
+    return rc
 
 
 def paged_decode_path(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,

@@ -38,6 +38,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "attn_device.cuh"
@@ -137,6 +138,137 @@ __device__ __forceinline__ void warp_tile(WarpAcc<D> &acc, const uint32_t (&qb)[
   }
 }
 
+// ---------------------------------------------------------------------------
+// The same per-stage work on the CUDA cores (the comparison form of the consumer
+// warps; pkv_set_decode_consumer selects it for decode_kernel).  bf16 products are
+// exact in fp32, so both forms accumulate the same products in fp32.
+//  * QK: lane l takes key 16*warp + (l & 15) and half (l >> 4) of the dims; for each
+//    16-byte chunk of its K row it issues mixed-precision FMAs (bf16 x bf16 + fp32,
+//    fma.rn.f32.bf16) against the group's query rows, read from shared memory
+//    (all lanes of a half read the same address: a broadcast).  The two halves are
+//    added with one shuffle per head.
+//  * softmax: as the tensor form (base 2, warp-shuffle maxima over the 16 keys); each
+//    lane keeps (m, l) for every head, l as its own key's partial sum.
+//  * PV: lane l owns dims l*D/32 .. +D/32 of every head; for each valid key it loads
+//    those V elements, widens them to fp32 and takes each head's weight from the lane
+//    that holds it (shuffle).
+template <int D>
+struct WarpAccF {
+  float o[kMaxGroup][D / 32];   // O: head h, dims lane*(D/32) + v
+  float m[kMaxGroup], l[kMaxGroup];
+};
+
+template <int D>
+__device__ __forceinline__ void accf_reset(WarpAccF<D> &a) {
+#pragma unroll
+  for (int h = 0; h < kMaxGroup; ++h) {
+#pragma unroll
+    for (int v = 0; v < D / 32; ++v) a.o[h][v] = 0.f;
+    a.m[h] = -INFINITY;
+    a.l[h] = 0.f;
+  }
+}
+
+// c + a.lo * b.lo + a.hi * b.hi for bf16 pairs a, b: two mixed-precision FMAs.
+__device__ __forceinline__ float fma_bf16x2(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t.reg .f32 t;\n\t"
+      "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.bf16 t, al, bl, %3;\n\tfma.rn.f32.bf16 %0, ah, bh, t;\n\t}"
+      : "=f"(d)
+      : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+// qs: shared address of the group's query rows [G][D] bf16.
+template <int D>
+__device__ __forceinline__ void warp_tile_fma(WarpAccF<D> &acc, uint32_t qs, int G, uint32_t kb,
+                                              uint32_t vb, int warp, int lane, int nvalid,
+                                              float scale_log2) {
+  constexpr int VPL = D / 32;  // dims per lane in PV
+  constexpr int CH = D / 16;   // 16-byte chunks in half a row
+  const int kk = lane & 15, hf = lane >> 4;
+  const int key = 16 * warp + kk;
+  float s[kMaxGroup];
+#pragma unroll
+  for (int h = 0; h < kMaxGroup; ++h) s[h] = 0.f;
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    const int dch = hf * CH + c;
+    const uint4 kv = lds128(kb + tile_off(key, dch));
+#pragma unroll
+    for (int h = 0; h < kMaxGroup; ++h) {
+      if (h < G) {
+        const uint4 qv = lds128(qs + (uint32_t)(h * D + dch * 8) * 2u);
+        float t = fma_bf16x2(kv.x, qv.x, s[h]);
+        t = fma_bf16x2(kv.y, qv.y, t);
+        t = fma_bf16x2(kv.z, qv.z, t);
+        s[h] = fma_bf16x2(kv.w, qv.w, t);
+      }
+    }
+  }
+  const bool valid = kk < nvalid;
+  float p[kMaxGroup];
+#pragma unroll
+  for (int h = 0; h < kMaxGroup; ++h) {
+    if (h < G) {
+      float sh = s[h] + __shfl_xor_sync(0xffffffffu, s[h], 16);
+      sh = valid ? sh * scale_log2 : -INFINITY;
+      float mx = sh;
+#pragma unroll
+      for (int x = 1; x < 16; x <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, x));
+      const float mn = fmaxf(acc.m[h], mx);
+      const float al = dev::ex2(acc.m[h] - mn);
+      p[h] = dev::ex2(sh - mn);
+      acc.l[h] = acc.l[h] * al + (hf == 0 ? p[h] : 0.f);
+      acc.m[h] = mn;
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) acc.o[h][v] *= al;
+    } else {
+      p[h] = 0.f;
+    }
+  }
+  // PV over the valid keys (rows past the range are never read: 0 * NaN would poison O)
+  const int d0 = lane * VPL;
+  const uint32_t voff = (uint32_t)((d0 & 7) * 2);
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    if (t < nvalid) {
+      const uint32_t va = vb + tile_off(16 * warp + t, d0 >> 3) + voff;
+      float vf[VPL];
+      if constexpr (VPL == 2) {
+        uint32_t w;
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w) : "r"(va));
+        vf[0] = dev::bf16lo_to_f32(w);
+        vf[1] = dev::bf16hi_to_f32(w);
+      } else {
+        uint32_t w0, w1;
+        asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(w0), "=r"(w1) : "r"(va));
+        vf[0] = dev::bf16lo_to_f32(w0);
+        vf[1] = dev::bf16hi_to_f32(w0);
+        vf[2] = dev::bf16lo_to_f32(w1);
+        vf[3] = dev::bf16hi_to_f32(w1);
+      }
+#pragma unroll
+      for (int h = 0; h < kMaxGroup; ++h) {
+        if (h < G) {
+          const float ph = __shfl_sync(0xffffffffu, p[h], t);
+#pragma unroll
+          for (int v = 0; v < VPL; ++v) acc.o[h][v] = fmaf(ph, vf[v], acc.o[h][v]);
+        }
+      }
+    }
+  }
+}
+
 // Receive slots the largest case needs: n * ceil(G / n) over cluster sizes n >= 2 and
 // groups G <= kMaxGroup.
 constexpr int recv_slots_needed() {
@@ -180,6 +312,28 @@ __device__ __forceinline__ void warp_stash(WarpAcc<D> &acc, const MergeArea &r, 
     if (h1 < G) {
       r.o[(warp * G + h1) * D + d] = acc.o[mt][1];
       r.o[(warp * G + h1) * D + d + 8] = acc.o[mt][3];
+    }
+  }
+}
+
+// warp_stash for the CUDA-core form: the 16 key lanes' partial sums reduced per head,
+// and the warp's (m, l, O) for heads < G written in the same merge-area layout.
+template <int D>
+__device__ __forceinline__ void warp_stash_fma(WarpAccF<D> &acc, const MergeArea &r, int G,
+                                               int warp, int lane) {
+  constexpr int VPL = D / 32;
+#pragma unroll
+  for (int h = 0; h < kMaxGroup; ++h) {
+    float l = acc.l[h];
+#pragma unroll
+    for (int x = 1; x < 32; x <<= 1) l += __shfl_xor_sync(0xffffffffu, l, x);
+    if (lane == 0) {
+      r.m[warp * kMaxGroup + h] = acc.m[h];
+      r.l[warp * kMaxGroup + h] = l;
+    }
+    if (h < G) {
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) r.o[(warp * G + h) * D + lane * VPL + v] = acc.o[h][v];
     }
   }
 }
@@ -400,7 +554,7 @@ __device__ __forceinline__ void finish_partition(const DecodeArgs &a, const Merg
   }
 }
 
-template <int D, int STAGES>
+template <int D, int STAGES, bool kFma>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const DecodeArgs a) {
@@ -416,7 +570,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t bar_empty = bar_full + STAGES * 8;
   volatile int *const s_flag =
       reinterpret_cast<volatile int *>(base_ptr + STAGES * kStageBytes + STAGES * 16);
-  volatile int *const s_last = s_flag + 1;
+  volatile int *const s_last = s_flag + 1;  // ticket merge: this partition merges
+  volatile int *const s_merge_timeout = s_last;  // cluster merge: its wait gave up
   // Cluster merge: a barrier whose phase completes when every CTA of the cluster has
   // pushed its results here, and the area they land in (rows of D floats, then the lse).
   const uint32_t bar_merge = bar_full + STAGES * 16 + 8;
@@ -424,6 +579,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   const float *const recv_o =
       reinterpret_cast<const float *>(base_ptr + STAGES * kStageBytes + STAGES * 16 + 16);
   const float *const recv_l = recv_o + kRecvSlots * D;
+  // the group's query rows (bf16 [G][D]) for the CUDA-core form of the consumers
+  const uint32_t q_area = recv + (uint32_t)(kRecvSlots * (D + 1) * 4);
 
   // grid: x = partition (fastest), y = kv head, z = sequence
   const int part = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -434,19 +591,26 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int win0 = (part * a.partition_tokens) >> a.log2_bs;
   int tb0 = 0;
   if (warp == kConsumerWarps && win0 + lane < a.max_blocks) tb0 = __ldg(trow + win0 + lane);
-  // consumer warps: the group's query rows as mma B fragments, also loaded up front
+  // consumer warps: the group's query rows as mma B fragments (tensor form) or in
+  // shared memory (CUDA-core form; published by the set-up barrier below), loaded up front
   uint32_t qb[KS][2];
   if (warp < kConsumerWarps) {
     // In a step whose first kernel rotates q in place, q is read only after that grid.
     if (a.q_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int gid = lane >> 2, tig = lane & 3;
-    const bool hv = gid < a.group;
-    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-        a.q + ((int64_t)b * a.num_q_heads + g * a.group + (hv ? gid : 0)) * D);
+    const uint16_t *qg = a.q + ((int64_t)b * a.num_q_heads + g * a.group) * D;
+    if constexpr (kFma) {
+      if (tid < a.group * D / 8)
+        *reinterpret_cast<uint4 *>(base_ptr + (q_area - base) + tid * 16) =
+            __ldcg(reinterpret_cast<const uint4 *>(qg) + tid);
+    } else {
+      const int gid = lane >> 2, tig = lane & 3;
+      const bool hv = gid < a.group;
+      const uint32_t *qrow = reinterpret_cast<const uint32_t *>(qg + (hv ? gid : 0) * D);
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      qb[ks][0] = hv ? __ldcg(qrow + 8 * ks + tig) : 0u;
-      qb[ks][1] = hv ? __ldcg(qrow + 8 * ks + 4 + tig) : 0u;
+      for (int ks = 0; ks < KS; ++ks) {
+        qb[ks][0] = hv ? __ldcg(qrow + 8 * ks + tig) : 0u;
+        qb[ks][1] = hv ? __ldcg(qrow + 8 * ks + 4 + tig) : 0u;
+      }
     }
   }
 
@@ -483,11 +647,13 @@ __global__ void __launch_bounds__(kThreads, 2)
       dev::mbar_arrive_expect_tx(bar_merge, (uint32_t)(n * owned * (D + 1) * 4));
     }
     *s_flag = 0;
+    *s_last = 0;
     dev::fence_mbar_init();
   }
   __syncthreads();
   // Every thread arrives on the cluster barrier now and waits on it before its first
   // access to another CTA's shared memory: by then every merge barrier is initialised.
+  // (Its next phase is the closing handshake at the end of the kernel.)
   if (cluster) dev::cluster_arrive_relaxed();
 
   if (warp == kConsumerWarps) {
@@ -541,8 +707,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (cluster) dev::cluster_wait();
   } else {
     // ----------------------------------------------------------- consumer warps
-    WarpAcc<D> acc;
-    acc_reset(acc);
+    WarpAcc<D> acc;    // tensor form
+    WarpAccF<D> accf;  // CUDA-core form
+    if constexpr (kFma)
+      accf_reset(accf);
+    else
+      acc_reset(acc);
     for (int c = 0; c < n_chunks; ++c) {
       const int s = c % STAGES;
       if (!__all_sync(0xffffffffu, dev::mbar_wait(bar_full + 8 * s, (c / STAGES) & 1))) {
@@ -556,7 +726,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int nvalid = min(16, t_end - key0);
       if (nvalid > 0) {
         const uint32_t kb = base + s * kStageBytes;
-        warp_tile<D>(acc, qb, kb, kb + kTileBytes, warp, lane, nvalid, a.scale_log2);
+        if constexpr (kFma)
+          warp_tile_fma<D>(accf, q_area, a.group, kb, kb + kTileBytes, warp, lane, nvalid,
+                           a.scale_log2);
+        else
+          warp_tile<D>(acc, qb, kb, kb + kTileBytes, warp, lane, nvalid, a.scale_log2);
       }
       __syncwarp();
       if (lane == 0) dev::mbar_arrive(bar_empty + 8 * s);
@@ -567,7 +741,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     r.o = reinterpret_cast<float *>(base_ptr);
     r.m = r.o + kConsumerWarps * a.group * D;
     r.l = r.m + kConsumerWarps * kMaxGroup;
-    warp_stash<D>(acc, r, a.group, warp, lane);
+    if constexpr (kFma)
+      warp_stash_fma<D>(accf, r, a.group, warp, lane);
+    else
+      warp_stash<D>(acc, r, a.group, warp, lane);
     consumer_bar();
     const int nparts_b = (L + a.partition_tokens - 1) / a.partition_tokens;  // non-empty ones
     if (cluster) {
@@ -577,9 +754,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       // arrival at set-up armed for all n * (heads owned) * (D + 1) * 4 bytes.  The
       // phase completes when the last byte has landed: the owner then merges from its
       // own shared memory, which nobody touches again, so no CTA waits for its peers
-      // to finish reading and there is no closing cluster barrier.  Every wait on the
-      // way to the pushes is bounded, so they all come; if the merge barrier still
-      // times out, the CTA records the error and skips the merge.
+      // to finish reading.  Every wait on the way to the pushes is bounded, so they all
+      // come; if the merge barrier still times out, the CTA records the error, skips the
+      // merge and, before it exits, waits until no peer can still be storing into it
+      // (the closing handshake at the end of the kernel).
       dev::cluster_wait();
       const int n = (int)dev::cluster_nctarank();
       const int rank = (int)dev::cluster_ctarank();
@@ -609,6 +787,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
         } else if (lane == 0) {
           raise_error(PKV_DEVERR_TIMEOUT);
+          *s_merge_timeout = 1;
         }
       } else if (tid == 0 && rank == 0) {
         raise_error(PKV_DEVERR_TIMEOUT);  // launched with the wrong cluster shape
@@ -624,6 +803,21 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int s = 0; s < STAGES; ++s) {
       const int c_last = s + ((n_chunks - 1 - s) / STAGES) * STAGES;  // last chunk on stage s
       if (c_last >= 0 && c_last < n_chunks) (void)dev::mbar_wait(bar_full + 8 * s, (c_last / STAGES) & 1);
+    }
+  }
+  // ---- closing handshake of the cluster merge.  Every thread of every CTA arrives
+  // here, after all of its pushes were issued, and normally leaves at once: a CTA
+  // whose merge barrier completed has received every byte aimed at it, so no store
+  // can still be on its way in.  A CTA whose merge wait gave up instead waits for the
+  // whole cluster to arrive -- every peer thread gets here through bounded waits only,
+  // so this wait ends -- and then once more (bounded) on its merge barrier, whose
+  // phase completes when the last of those already-issued stores has landed.  Only
+  // then does it exit, so no peer's store can target a CTA that has left.
+  if (cluster) {
+    dev::cluster_arrive_relaxed();
+    if (*s_merge_timeout) {
+      dev::cluster_wait();
+      if (tid == 0) (void)dev::mbar_wait_cluster(bar_merge, 0);
     }
   }
 }
@@ -1160,8 +1354,10 @@ cudaError_t read_decode_errors(uint32_t *flags, int clear) { return read_tu_erro
 
 namespace {
 
-bool g_split_attr[kMaxDevices][2];    // dynamic smem attribute of decode_kernel set
+bool g_split_attr[kMaxDevices][2][2];  // dynamic smem attribute of decode_kernel set [D][form]
 bool g_persist_attr[kMaxDevices][2];  // ... of decode_persistent_kernel
+// Arithmetic of decode_kernel's consumer warps (PKV_CONSUMER_*), process-wide.
+std::atomic<int> g_consumer{PKV_CONSUMER_TENSOR};
 
 // Partition size for paged_decode_attention.  Few (sequence, kv head) units: cut each
 // into as many partitions as make about one wave of CTAs, so every CTA streams a long
@@ -1225,6 +1421,9 @@ int launch_split(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_c
                  cudaStream_t stream, bool programmatic = false, int cluster = 0,
                  bool q_wait = false) {
   CUtensorMap tmk, tmv;
+  const bool fma = g_consumer.load(std::memory_order_relaxed) == PKV_CONSUMER_FMA;
+  void (*const kern)(const CUtensorMap, const CUtensorMap, const DecodeArgs) =
+      fma ? decode_kernel<D, split_stages(D), true> : decode_kernel<D, split_stages(D), false>;
   {
     std::lock_guard<std::mutex> lk(attn_mutex());
     int rc = maps_for(k_cache, v_cache, c, &tmk, &tmv);
@@ -1232,15 +1431,13 @@ int launch_split(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_c
     int dev = 0;
     if ((rc = current_device(&dev))) return rc;
     const int vi = D == 64 ? 0 : 1;
-    if (!g_split_attr[dev][vi]) {
-      cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, split_stages(D)>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (!g_split_attr[dev][vi][fma ? 1 : 0]) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)split_smem(D));
       if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute");
-      e = cudaFuncSetAttribute(decode_kernel<D, split_stages(D)>,
-                               cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
       if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(carveout)");
-      g_split_attr[dev][vi] = true;
+      g_split_attr[dev][vi][fma ? 1 : 0] = true;
     }
   }
   DecodeArgs a;
@@ -1270,7 +1467,7 @@ int launch_split(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_c
   dim3 grid((unsigned)a.n_parts, (unsigned)c.num_kv_heads, (unsigned)num_seqs);
   cudaError_t e;
   if (!programmatic && cluster <= 1) {
-    decode_kernel<D, split_stages(D)><<<grid, kThreads, split_smem(D), stream>>>(tmk, tmv, a);
+    kern<<<grid, kThreads, split_smem(D), stream>>>(tmk, tmv, a);
     e = cudaGetLastError();
   } else {
     cudaLaunchConfig_t cfg = {};
@@ -1294,7 +1491,7 @@ int launch_split(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_c
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    e = cudaLaunchKernelEx(&cfg, decode_kernel<D, split_stages(D)>, tmk, tmv, a);
+    e = cudaLaunchKernelEx(&cfg, kern, tmk, tmv, a);
   }
   if (e != cudaSuccess) return cuda_error(e, "decode_kernel launch");
   return PKV_OK;
@@ -1435,6 +1632,13 @@ PKV_API int32_t paged_decode_plan(int32_t num_seqs, int32_t num_q_heads, int32_t
       max_context_len <= 0)
     return 0;
   return plan_partition(num_seqs, num_kv_heads, head_dim, max_context_len, sms_or_default(num_sms));
+}
+
+PKV_API int32_t pkv_set_decode_consumer(int32_t consumer) {
+  if (consumer != PKV_CONSUMER_TENSOR && consumer != PKV_CONSUMER_FMA)
+    return set_error(PKV_ERR_UNSUPPORTED, "pkv_set_decode_consumer: unknown form %d", consumer);
+  clear_error();
+  return g_consumer.exchange(consumer);
 }
 
 PKV_API int32_t paged_decode_path(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,

@@ -62,11 +62,13 @@ constexpr int kRecvSlots = 16;
 
 // Stages of the TMA ring and the dynamic shared memory of one decode CTA: 1 KB of
 // alignment slack, the ring, its full/empty barriers, two flags and the merge barrier,
-// then the receive area (kRecvSlots rows of D floats, then kRecvSlots lse values).
+// the receive area (kRecvSlots rows of D floats, then kRecvSlots lse values), then the
+// group's query rows as bf16 (read there by the CUDA-core form of the consumer warps).
 constexpr int split_stages(int d) { return d == 64 ? 4 : 3; }
 constexpr size_t split_ring_bytes(int d) { return (size_t)split_stages(d) * 2 * kChunk * d * 2; }
 constexpr size_t split_smem(int d) {
-  return 1024 + split_ring_bytes(d) + split_stages(d) * 16 + 16 + (size_t)kRecvSlots * (d + 1) * 4;
+  return 1024 + split_ring_bytes(d) + split_stages(d) * 16 + 16 + (size_t)kRecvSlots * (d + 1) * 4 +
+         (size_t)kMaxGroup * d * 2;
 }
 // CTAs of decode_kernel one SM holds (shared memory limited: 70 KB at D=64, 105 KB at
 // D=128, of the 228 KB an SM shares out with 1 KB reserved per CTA).

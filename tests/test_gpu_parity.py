@@ -1,11 +1,12 @@
 """CUDA path vs the CPU oracle, through the C ABI.
 
 Bar: the KV write is bit-exact (the whole pool is compared, so no other byte may
-change); attention is within |gpu - oracle| <= 1e-2 + 2^-8 |oracle| elementwise.
-The 1e-2 absolute bound is the stated target; the 2^-8 |oracle| term is the bf16
-output's own half-ulp, which only exceeds 1e-2 where |out| > 2.56 (a bf16 value
-can be no closer than that to the fp64 result).  Attention inputs carry NaN in
-every slot no sequence owns, so reading one shows up.
+change); attention is within |gpu - oracle| <= 1e-2 elementwise wherever
+|oracle| <= 2.56, and within 1e-2 + 2^-8 |oracle| elsewhere.  The 1e-2 absolute
+bound is the stated target; the 2^-8 |oracle| term is the bf16 output's own
+half-ulp, which only exceeds 1e-2 where |out| > 2.56 (a bf16 value can be no
+closer than that to the fp64 result).  Attention inputs carry NaN in every slot no
+sequence owns, so reading one shows up.
 """
 
 import dataclasses
@@ -39,12 +40,20 @@ def dev(inp):
     return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
 
 
+ABS_ONLY_BELOW = 2.56  # |oracle| at which the bf16 half-ulp term reaches 1e-2
+
+
 def check_attention(got: torch.Tensor, ref: torch.Tensor, tag: str) -> float:
     got = got.cpu().double()
     assert torch.isfinite(got).all(), f"{tag}: non-finite output"
     err = (got - ref).abs()
-    bad = err > ATOL + RTOL * ref.abs()
-    assert not bool(bad.any()), f"{tag}: {int(bad.sum())} outputs out of tolerance, max |diff| {err.max():.3e}"
+    # every element: the absolute target where the output is small enough for a bf16
+    # value to reach it, the target plus the output's own half-ulp elsewhere
+    bound = torch.where(ref.abs() <= ABS_ONLY_BELOW, torch.full_like(ref, ATOL),
+                        ATOL + RTOL * ref.abs())
+    bad = err > bound
+    assert not bool(bad.any()), (f"{tag}: {int(bad.sum())} outputs out of tolerance, max |diff| "
+                                 f"{err.max():.3e}")
     return float(err.max())
 
 
@@ -75,8 +84,7 @@ def test_workload_step_matches_oracle(B, oracle, wid):
     # KV write: every byte of both pools
     assert torch.equal(g["k_cache"].cpu().view(torch.int16), kc_ref.view(torch.int16))
     assert torch.equal(g["v_cache"].cpu().view(torch.int16), vc_ref.view(torch.int16))
-    e = check_attention(out, ref, w.name)
-    assert e <= ATOL or ref.abs().max() > 2.56, f"{w.name}: max |diff| {e}"
+    check_attention(out, ref, w.name)
 
 
 @pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
@@ -796,11 +804,11 @@ def test_prefill_wide_scores_and_full_tiles(B, oracle, D, BS, Hq, Hkv):
 
 
 @pytest.mark.parametrize("wid", [2, 3, 4, 5])
-def test_workload_prefill_sampled(B, oracle, wid):
+def test_workload_prefill_every_row(B, oracle, wid):
     """Prefill of the last min(L, 512) tokens of every sequence at the workload's full size
-    (the configuration bench.py --kernel prefill times).  Sampled against the oracle: the
-    last 8 query rows of four sequences; the oracle runs just those 8 queries, which sit at
-    the same positions."""
+    (the configuration bench.py --kernel prefill times), every query row of every head
+    against the oracle (threads over (sequence, kv head) pairs): the causal diagonal of
+    every 128-row tile, the ragged last tiles and the ragged last key blocks included."""
     import itertools
     w = W.WORKLOADS[wid]
     inp = W.make_inputs(w, poison=True)
@@ -818,17 +826,13 @@ def test_workload_prefill_sampled(B, oracle, wid):
     torch.cuda.synchronize()
     assert_no_device_errors(B)
     got = out.cpu()
-    assert torch.isfinite(got.float()).all(), "a query row was not written"
-    for b in sorted({0, Bn // 3, (2 * Bn) // 3, Bn - 1}):
-        n = min(8, int(chunks[b]))
-        rows = slice(int(qs[b + 1]) - n, int(qs[b + 1]))
-        ref = oracle.prefill(q[rows], inp["k_cache"], inp["v_cache"], inp["block_tables"][b:b + 1],
-                             inp["context_lens"][b:b + 1],
-                             torch.tensor([0, n], dtype=torch.int32), inp["scale"])
-        check_attention(got[rows], ref, f"{w.name} sequence {b}")
+    del g, out
+    ref = oracle.prefill(q, inp["k_cache"], inp["v_cache"], inp["block_tables"],
+                         inp["context_lens"], qs, inp["scale"])
+    check_attention(got, ref, f"{w.name} prefill, all {int(qs[-1])} query rows")
 
 
-@pytest.mark.parametrize("wid", [2, 4])
+@pytest.mark.parametrize("wid", [2, 3, 4, 5])
 def test_workload_decode_step_rope(B, oracle, wid):
     """paged_decode_step_rope at the workload's full size (bench.py --kernel rope_step):
     q and both caches bit for bit, every output within tolerance."""
@@ -894,3 +898,64 @@ def test_prefill_single_token_chunks_equal_decode(B, oracle):
                         inp["context_lens"], inp["scale"])
     check_attention(out, ref, "prefill n=1")
     check_attention(dec, ref, "decode")
+
+
+# ------------------------------------------------- CUDA-core form of the consumer warps
+@pytest.fixture
+def fma_consumer(B):
+    prev = B.pkv_set_decode_consumer(B.CONSUMER_FMA)
+    yield
+    B.pkv_set_decode_consumer(prev)
+
+
+@pytest.mark.parametrize("D,BS,Hq,Hkv", [(64, 16, 8, 2), (128, 16, 24, 8), (64, 32, 32, 4),
+                                         (128, 32, 16, 2), (64, 16, 4, 4), (128, 8, 8, 8)])
+def test_fma_consumer_small_cases(B, oracle, fma_consumer, D, BS, Hq, Hkv):
+    """The CUDA-core consumer (fp32 FMAs, shuffles) against the oracle: the launcher's
+    plan (cluster or partition path), then explicit partitions through split + combine;
+    ragged lengths, partial 16-key groups, G from 1 to 8."""
+    lens = (1, 15, 16, 17, 63, 64, 65, 130, 700, 1025)
+    w = W.small_workload(B=len(lens), Hq=Hq, Hkv=Hkv, D=D, BS=BS, lens=lens, seed=7 * D + BS + Hq)
+    inp = W.make_inputs(w, poison=True)
+    assert B.paged_decode_path(w.B, Hq, Hkv, D, inp["max_context_len"]) in (B.PATH_CLUSTER,
+                                                                            B.PATH_PARTITIONS)
+    g = dev(inp)
+    out = step(B, g)
+    ref, kc_ref, vc_ref = oracle.step(inp)
+    check_attention(out, ref, f"fma consumer D={D} BS={BS} G={Hq // Hkv}")
+    for P in (64, 320):
+        n = math.ceil(inp["max_context_len"] / P)
+        o_part = torch.empty(w.B, Hq, n, D, device="cuda")
+        lse = torch.empty(w.B, Hq, n, device="cuda")
+        B.paged_decode_split(o_part, lse, g["q"], g["k_cache"], g["v_cache"], g["block_tables"],
+                             g["context_lens"], inp["max_context_len"], inp["scale"], P)
+        o2 = torch.empty_like(g["q"])
+        B.paged_decode_combine(o2, o_part, lse, g["context_lens"], inp["max_context_len"], P)
+        check_attention(o2, ref, f"fma consumer P={P} D={D} G={Hq // Hkv}")
+    assert_no_device_errors(B)
+
+
+@pytest.mark.parametrize("wid,P", [(1, 0), (2, 0), (5, 0), (3, 1024), (4, 1024)])
+def test_fma_consumer_workloads(B, oracle, fma_consumer, wid, P):
+    """Full workloads with the CUDA-core consumer, in the configuration bench.py times it:
+    the fused step on the partition kernel's paths (workloads 1, 2, 5), and split +
+    combine at P = 1024 where the fused step takes the persistent kernel (3, 4)."""
+    w = W.WORKLOADS[wid]
+    inp = W.make_inputs(w, poison=True)
+    g = dev(inp)
+    ref, kc_ref, vc_ref = oracle.step(inp)
+    if P == 0:
+        out = step(B, g)
+    else:
+        B.paged_kv_write(g["k_new"], g["v_new"], g["slot_mapping"], g["k_cache"], g["v_cache"])
+        Bn, Hq, D = inp["q"].shape
+        n = math.ceil(inp["max_context_len"] / P)
+        o_part = torch.empty(Bn, Hq, n, D, device="cuda")
+        lse = torch.empty(Bn, Hq, n, device="cuda")
+        B.paged_decode_split(o_part, lse, g["q"], g["k_cache"], g["v_cache"], g["block_tables"],
+                             g["context_lens"], inp["max_context_len"], inp["scale"], P)
+        out = torch.empty_like(g["q"])
+        B.paged_decode_combine(out, o_part, lse, g["context_lens"], inp["max_context_len"], P)
+    torch.cuda.synchronize()
+    assert_no_device_errors(B)
+    check_attention(out, ref, f"{w.name} (fma consumer)")
