@@ -7,6 +7,25 @@
 #include <mutex>
 
 #include "attn_device.cuh"
+#include "pkv_exp2.cuh"
+
+// Of the 16 column pairs of each 32-column chunk of a score row, how many take their
+// exponentials on the FMA pipe (exp2_fma) rather than the special-function unit.
+#ifndef PKV_PREFILL_POLY_PAIRS
+#define PKV_PREFILL_POLY_PAIRS 0
+#endif
+// Row maxima with three-input max instructions (1) or two-input ones (0).
+#ifndef PKV_PREFILL_MAX3
+#define PKV_PREFILL_MAX3 1
+#endif
+// Scaled, max-subtracted scores two at a time with packed fp32 FMAs (1) or one at a time (0).
+#ifndef PKV_PREFILL_FMA2
+#define PKV_PREFILL_FMA2 1
+#endif
+// Row sums of the bf16 weights with mixed-precision adds (1) or widen-then-add (0).
+#ifndef PKV_PREFILL_SUM_MIXED
+#define PKV_PREFILL_SUM_MIXED 1
+#endif
 
 namespace pkv {
 
@@ -110,6 +129,213 @@ __device__ __forceinline__ void tc_load_block(const CUtensorMap *tm, uint32_t ds
     }
   }
   __syncwarp();
+}
+
+// ---------------------------------------------------------------------------
+// The softmax warps' work on one 128-column block of a score row in TMEM (one thread =
+// one row = one TMEM lane).  TMEM is read in 32-column chunks with the next chunk's load
+// in flight while the current one is processed.
+
+// Waits for this thread's TMEM loads; the 32 registers the last one fills are tied to
+// the wait, so that nothing reads them before it.
+__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&x)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(x[0]), "+r"(x[1]), "+r"(x[2]), "+r"(x[3]), "+r"(x[4]), "+r"(x[5]),
+                 "+r"(x[6]), "+r"(x[7]), "+r"(x[8]), "+r"(x[9]), "+r"(x[10]), "+r"(x[11]),
+                 "+r"(x[12]), "+r"(x[13]), "+r"(x[14]), "+r"(x[15]), "+r"(x[16]), "+r"(x[17]),
+                 "+r"(x[18]), "+r"(x[19]), "+r"(x[20]), "+r"(x[21]), "+r"(x[22]), "+r"(x[23]),
+                 "+r"(x[24]), "+r"(x[25]), "+r"(x[26]), "+r"(x[27]), "+r"(x[28]), "+r"(x[29]),
+                 "+r"(x[30]), "+r"(x[31])
+               :
+               : "memory");
+}
+
+// c + lo(x) + hi(x) for a bf16 pair x: two mixed-precision adds (bf16 + fp32).
+__device__ __forceinline__ float add_bf16x2(uint32_t x, float c) {
+  float d;
+  asm("{\n\t.reg .b16 lo, hi;\n\t.reg .f32 t;\n\t"
+      "mov.b32 {lo, hi}, %1;\n\t"
+      "add.rn.f32.bf16 t, lo, %2;\n\tadd.rn.f32.bf16 %0, hi, t;\n\t}"
+      : "=f"(d)
+      : "r"(x), "f"(c));
+  return d;
+}
+
+// (x0, x1) * s + c, both lanes rounded once (fused), in one packed instruction.
+__device__ __forceinline__ void fma_f32x2(float x0, float x1, float s, float c, float &d0,
+                                          float &d1) {
+  asm("{\n\t.reg .b64 x, sc, cc, d;\n\t"
+      "mov.b64 x, {%2, %3};\n\tmov.b64 sc, {%4, %4};\n\tmov.b64 cc, {%5, %5};\n\t"
+      "fma.rn.f32x2 d, x, sc, cc;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(x0), "f"(x1), "f"(s), "f"(c));
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Pass 1: the row's maximum scaled score over the block's columns c <= lim (all of them
+// when `whole`).  With a positive scale, the max of the raw scores scaled once equals
+// the max of the scaled scores (rounding is monotonic).
+__device__ __forceinline__ float row_block_max(uint32_t sb, int lim, bool whole, bool pos_scale,
+                                               float scale_log2) {
+  float mx[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
+  const float sc = pos_scale ? 1.f : scale_log2;
+  uint32_t xa[32], xb[32];
+  dev::tmem_ld32(sb, xa);
+  tmem_wait_ld_regs(xa);
+#pragma unroll
+  for (int ch = 0; ch < kTcKeys / 32; ++ch) {
+    uint32_t(&cur)[32] = (ch & 1) ? xb : xa;
+    uint32_t(&nxt)[32] = (ch & 1) ? xa : xb;
+    if (ch + 1 < kTcKeys / 32) dev::tmem_ld32(sb + (ch + 1) * 32, nxt);
+    const int lc = lim - ch * 32;
+    if (whole && pos_scale) {
+#if PKV_PREFILL_MAX3
+#pragma unroll
+      for (int i = 0; i < 32; i += 2)
+        mx[(i >> 1) & 7] = fmax3(mx[(i >> 1) & 7], __uint_as_float(cur[i]), __uint_as_float(cur[i + 1]));
+#else
+#pragma unroll
+      for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(cur[i]));
+#endif
+    } else if (whole) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(cur[i]) * sc);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        mx[i & 7] = fmaxf(mx[i & 7], i <= lc ? __uint_as_float(cur[i]) * sc : -INFINITY);
+    }
+    if (ch + 1 < kTcKeys / 32) tmem_wait_ld_regs(nxt);
+  }
+  float bmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+  return pos_scale ? bmax * scale_log2 : bmax;
+}
+
+// Pass 2: P = exp2(S * scale - m_ref) for the block's columns c <= lim (0 past it),
+// rounded to bf16 and stored into row r of the P buffer at shared offset `prow`
+// (K-major, 128-byte swizzle: two 64-column sub-tiles `sub` bytes apart); returns the
+// sum of the rounded values, which is what the tensor cores multiply.  The first
+// PKV_PREFILL_POLY_PAIRS column pairs of each 32-column chunk take exp2_fma.
+__device__ __forceinline__ float row_block_exp(uint32_t sb, uint8_t *bp, uint32_t prow,
+                                               uint32_t sub, int r, int lim, bool whole,
+                                               float scale_log2, float m_ref) {
+  float ls[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) ls[u] = 0.f;
+  uint32_t xa[32], xb[32];
+  dev::tmem_ld32(sb, xa);
+  tmem_wait_ld_regs(xa);
+#pragma unroll
+  for (int ch = 0; ch < kTcKeys / 32; ++ch) {
+    uint32_t(&cur)[32] = (ch & 1) ? xb : xa;
+    uint32_t(&nxt)[32] = (ch & 1) ? xa : xb;
+    if (ch + 1 < kTcKeys / 32) dev::tmem_ld32(sb + (ch + 1) * 32, nxt);
+    const int lc = whole ? 32 : lim - ch * 32;
+    uint32_t pk[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+#if PKV_PREFILL_FMA2
+      float a0, a1;
+      fma_f32x2(__uint_as_float(cur[2 * e]), __uint_as_float(cur[2 * e + 1]), scale_log2, -m_ref,
+                a0, a1);
+#else
+      const float a0 = fmaf(__uint_as_float(cur[2 * e]), scale_log2, -m_ref);
+      const float a1 = fmaf(__uint_as_float(cur[2 * e + 1]), scale_log2, -m_ref);
+#endif
+      float p0, p1;
+      if (e < PKV_PREFILL_POLY_PAIRS) {
+        p0 = dev::exp2_fma(a0);
+        p1 = dev::exp2_fma(a1);
+      } else {
+        p0 = dev::ex2(a0);
+        p1 = dev::ex2(a1);
+      }
+      if (!whole) {
+        p0 = 2 * e <= lc ? p0 : 0.f;
+        p1 = 2 * e + 1 <= lc ? p1 : 0.f;
+      }
+      pk[e] = dev::pack_bf16x2(p0, p1);
+      // sum what the tensor cores multiply: with a stale reference max the largest P is
+      // not a power of two, and only this keeps the weights a convex combination
+#if PKV_PREFILL_SUM_MIXED
+      ls[e & 7] = add_bf16x2(pk[e], ls[e & 7]);
+#else
+      ls[(2 * e) & 7] += dev::bf16lo_to_f32(pk[e]);
+      ls[(2 * e + 1) & 7] += dev::bf16hi_to_f32(pk[e]);
+#endif
+    }
+    const uint32_t dst = prow + (ch >> 1) * sub;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c16 = (ch & 1) * 4 + u;
+      *reinterpret_cast<uint4 *>(bp + dst + ((c16 ^ (r & 7)) << 4)) =
+          make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+    }
+    if (ch + 1 < kTcKeys / 32) tmem_wait_ld_regs(nxt);
+  }
+  return ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+}
+
+// ---------------------------------------------------------------------------
+// Tensor-core issue.  A tcgen05.mma returns to the issuing thread only once the tensor
+// core has taken it, about as long as it then runs (~65 cycles for M=128, N<=128, K=16),
+// so any work the thread does between two of them leaves the tensor core idle.  The MMA
+// thread therefore builds every descriptor before a sequence and issues four at a time
+// from one straight-line block: the first accumulates per `acc_first`, the others always.
+
+// Adds a byte offset (a multiple of 16) to a shared-memory descriptor's start address.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) {
+  return desc + (uint64_t)(bytes >> 4);
+}
+
+__device__ __forceinline__ void umma4(uint32_t d_tmem, uint64_t a0, uint64_t a1, uint64_t a2,
+                                      uint64_t a3, uint64_t b0, uint64_t b1, uint64_t b2,
+                                      uint64_t b3, uint32_t idesc, uint32_t acc_first) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %10, 0;\n\tsetp.eq.u32 q, 1, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %9, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %6, %9, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %9, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %9, q;\n\t}" ::"r"(d_tmem),
+      "l"(a0), "l"(a1), "l"(a2), "l"(a3), "l"(b0), "l"(b1), "l"(b2), "l"(b3), "r"(idesc),
+      "r"(acc_first)
+      : "memory");
+}
+
+// S = Q . K^T over D: D/16 MMAs of K = 16.  q, k: descriptors of the K-major, 128-byte
+// swizzled tiles (64-dim sub-tiles `sub` bytes apart).
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q, uint64_t k, uint32_t sub,
+                                         uint32_t idesc) {
+#pragma unroll
+  for (int g4 = 0; g4 < D / 64; ++g4) {
+    const uint32_t o = g4 * sub;
+    umma4(d_tmem, desc_add(q, o), desc_add(q, o + 32), desc_add(q, o + 64), desc_add(q, o + 96),
+          desc_add(k, o), desc_add(k, o + 32), desc_add(k, o + 64), desc_add(k, o + 96), idesc,
+          g4 > 0 ? 1u : 0u);
+  }
+}
+
+// O (+)= P . V over a block of kTcKeys keys: kTcKeys/16 MMAs of K = 16.  p: descriptor of
+// the K-major P buffer (64-key sub-tiles `sub` bytes apart); v: descriptor of the
+// MN-major V tile (16 keys = 2048 bytes apart).
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint64_t p, uint64_t v, uint32_t sub,
+                                         uint32_t idesc, uint32_t acc_first) {
+#pragma unroll
+  for (int g4 = 0; g4 < kTcKeys / 64; ++g4) {
+    const uint32_t o = g4 * sub, vo = g4 * 4 * 2048u;
+    umma4(d_tmem, desc_add(p, o), desc_add(p, o + 32), desc_add(p, o + 64), desc_add(p, o + 96),
+          desc_add(v, vo), desc_add(v, vo + 2048), desc_add(v, vo + 4096), desc_add(v, vo + 6144),
+          idesc, g4 > 0 ? 1u : acc_first);
+  }
 }
 
 template <int D>
@@ -225,19 +451,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       constexpr uint32_t id_s = dev::idesc_bf16_f32(kTcRows, kTcKeys, 0);
       constexpr uint32_t id_o = dev::idesc_bf16_f32(kTcRows, D, 1);
+      // descriptors of the Q tile, K stage 0, V stage 0 and P buffer 0 (the others are
+      // whole tiles / buffers further on)
+      const uint64_t dq = dev::smem_desc(base + SL::q, 16, 1024);
+      const uint64_t dk0 = dev::smem_desc(base + SL::k, 16, 1024);
+      const uint64_t dv0 = dev::smem_desc(base + SL::v, SL::kSub, 1024);
+      const uint64_t dp0 = dev::smem_desc(base + SL::p, 16, 1024);
       bool ok = fail(dev::mbar_wait(q_ready, 0));
       auto issue_s = [&](int j) {
         const int s = j % KS;
         if (!fail(dev::mbar_wait(k_full(s), (j / KS) & 1))) return false;
         if (j >= 2 && !fail(dev::mbar_wait(s_free(j & 1), ((j >> 1) - 1) & 1))) return false;
         dev::tc_fence_after();
-        const uint32_t kt = base + SL::k + s * SL::kTile;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * SL::kSub + (ks & 3) * 32;
-          dev::umma_bf16(tmem + 128u * (j & 1), dev::smem_desc(base + SL::q + off, 16, 1024),
-                         dev::smem_desc(kt + off, 16, 1024), id_s, ks > 0 ? 1u : 0u);
-        }
+        issue_qk<D>(tmem + 128u * (j & 1), dq, desc_add(dk0, s * SL::kTile), SL::kSub, id_s);
         dev::umma_commit(s_full(j & 1));
         dev::umma_commit(k_empty(s));
         return true;
@@ -249,15 +475,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!(ok = fail(dev::mbar_wait(p_full(j & 1), (j >> 1) & 1)))) break;
         if (!(ok = fail(dev::mbar_wait(v_full(s), (j / KS) & 1)))) break;
         dev::tc_fence_after();
-        const uint32_t vt = base + SL::v + s * SL::kTile;
-        const uint32_t pb = base + SL::p + (j & 1) * SL::kP;
-#pragma unroll
-        for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-          const uint32_t poff = (kk >> 2) * SL::kSub + (kk & 3) * 32;
-          dev::umma_bf16(tmem + 256u, dev::smem_desc(pb + poff, 16, 1024),
-                         dev::smem_desc(vt + kk * 2048u, SL::kSub, 1024), id_o,
-                         (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        issue_pv(tmem + 256u, desc_add(dp0, (j & 1) * SL::kP), desc_add(dv0, s * SL::kTile),
+                 SL::kSub, id_o, j > 0 ? 1u : 0u);
         dev::umma_commit(pv_done(j & 1));
         dev::umma_commit(v_empty(s));
       }
@@ -298,34 +517,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // S row of this block: four chunks of 32 columns, read from TMEM in each pass
       const uint32_t sbase = tmem + lane_base + 128u * (j & 1);
       const bool whole = __all_sync(0xffffffffu, lim >= kTcKeys - 1);  // no column masked
-      // pass 1: the block's row max (eight independent chains)
-      float mx[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
-#pragma unroll 1
-      for (int ch = 0; ch < kTcKeys / 32; ++ch) {
-        uint32_t x[32];
-        dev::tmem_ld32(sbase + ch * 32, x);
-        dev::tmem_wait_ld();
-        const int lc = lim - ch * 32;
-        // with a positive scale the max of the raw scores, scaled once, is the max of
-        // the scaled scores (rounding is monotonic)
-        const float sc = pos_scale ? 1.f : a.scale_log2;
-        if (whole && pos_scale) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(x[i]));
-        } else if (whole) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(x[i]) * sc);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            mx[i & 7] = fmaxf(mx[i & 7], i <= lc ? __uint_as_float(x[i]) * sc : -INFINITY);
-        }
-      }
-      float bmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      if (pos_scale) bmax *= a.scale_log2;
+      // pass 1: the block's row max
+      const float bmax = row_block_max(sbase, lim, whole, pos_scale, a.scale_log2);
       if (j > 0) {
         const bool need = bmax > m_ref + kTcRescale;
         if (__any_sync(0xffffffffu, need)) {  // O moves: wait until the previous P.V is in
@@ -356,40 +549,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                       dev::mbar_wait(pv_done(j & 1), ((j - 2) >> 1) & 1))))
         break;
       // pass 2: P = exp2(S - m_ref) as bf16 into shared memory, and its row sum
-      float ls[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) ls[u] = 0.f;
-      const uint32_t prow = SL::p + (j & 1) * SL::kP + r * 128;
-#pragma unroll 1
-      for (int ch = 0; ch < kTcKeys / 32; ++ch) {
-        uint32_t x[32];
-        dev::tmem_ld32(sbase + ch * 32, x);
-        dev::tmem_wait_ld();
-        const int lc = whole ? 32 : lim - ch * 32;
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float p0 = dev::ex2(fmaf(__uint_as_float(x[2 * e]), a.scale_log2, -m_ref));
-          float p1 = dev::ex2(fmaf(__uint_as_float(x[2 * e + 1]), a.scale_log2, -m_ref));
-          if (!whole) {
-            p0 = 2 * e <= lc ? p0 : 0.f;
-            p1 = 2 * e + 1 <= lc ? p1 : 0.f;
-          }
-          pk[e] = dev::pack_bf16x2(p0, p1);
-          // sum what the tensor cores multiply: with a stale reference max the largest
-          // P is not a power of two, and only this keeps the weights a convex combination
-          ls[(2 * e) & 7] += dev::bf16lo_to_f32(pk[e]);
-          ls[(2 * e + 1) & 7] += dev::bf16hi_to_f32(pk[e]);
-        }
-        const uint32_t dst = prow + (ch >> 1) * SL::kSub;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int c16 = (ch & 1) * 4 + u;
-          *reinterpret_cast<uint4 *>(bp + dst + ((c16 ^ (r & 7)) << 4)) =
-              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-        }
-      }
-      lsum += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      lsum += row_block_exp(sbase, bp, SL::p + (j & 1) * SL::kP + r * 128, SL::kSub, r, lim, whole,
+                            a.scale_log2, m_ref);
       // S read: the MMA warp may refill this buffer
       dev::tc_fence_before();
       __syncwarp();
@@ -614,15 +775,13 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
         dev::tc_fence_after();
         return true;
       };
+      const uint64_t dq0 = dev::smem_desc(base + SL::q, 16, 1024);
+      const uint64_t dk0 = dev::smem_desc(base + SL::k, 16, 1024);
+      const uint64_t dv0 = dev::smem_desc(base + SL::v, SL::kSub, 1024);
+      const uint64_t dp0 = dev::smem_desc(base + SL::p, 16, 1024);
       auto issue_s = [&](int t, int j) {
-        const uint32_t kt = base + SL::k + (j % KSK) * SL::kTile;
-        const uint32_t qt = base + SL::q + t * SL::kTile;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * SL::kSub + (ks & 3) * 32;
-          dev::umma_bf16(tmem + 128u * t, dev::smem_desc(qt + off, 16, 1024),
-                         dev::smem_desc(kt + off, 16, 1024), id_s, ks > 0 ? 1u : 0u);
-        }
+        issue_qk<D>(tmem + 128u * t, desc_add(dq0, t * SL::kTile),
+                    desc_add(dk0, (j % KSK) * SL::kTile), SL::kSub, id_s);
         dev::umma_commit(s_full(t));
         // K_j is free once the last tile that reads it has its S
         if (t == 1 || j >= nblk_of(1)) dev::umma_commit(k_empty(j % KSK));
@@ -647,15 +806,8 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
             v_seen = true;
             dev::tc_fence_after();
           }
-          const uint32_t vt = base + SL::v + (j % KSV) * SL::kTile;
-          const uint32_t pb = base + SL::p + t * SL::kP;
-#pragma unroll
-          for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-            const uint32_t poff = (kk >> 2) * SL::kSub + (kk & 3) * 32;
-            dev::umma_bf16(tmem + 256u + (uint32_t)(D * t), dev::smem_desc(pb + poff, 16, 1024),
-                           dev::smem_desc(vt + kk * 2048u, SL::kSub, 1024), id_o,
-                           (j > 0 || kk > 0) ? 1u : 0u);
-          }
+          issue_pv(tmem + 256u + (uint32_t)(D * t), desc_add(dp0, t * SL::kP),
+                   desc_add(dv0, (j % KSV) * SL::kTile), SL::kSub, id_o, j > 0 ? 1u : 0u);
           dev::umma_commit(pv_done(t));
         }
         if (ok) dev::umma_commit(v_empty(j % KSV));
@@ -699,33 +851,7 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
       if (!(ok = __all_sync(0xffffffffu, dev::mbar_wait(s_full(t), j & 1)))) break;
       dev::tc_fence_after();
       const bool whole = __all_sync(0xffffffffu, lim >= kTcKeys - 1);
-      float mx[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
-#pragma unroll 1
-      for (int ch = 0; ch < kTcKeys / 32; ++ch) {
-        uint32_t x[32];
-        dev::tmem_ld32(sb + ch * 32, x);
-        dev::tmem_wait_ld();
-        const int lc = lim - ch * 32;
-        // with a positive scale the max of the raw scores, scaled once, is the max of
-        // the scaled scores (rounding is monotonic)
-        const float sc = pos_scale ? 1.f : a.scale_log2;
-        if (whole && pos_scale) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(x[i]));
-        } else if (whole) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(x[i]) * sc);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            mx[i & 7] = fmaxf(mx[i & 7], i <= lc ? __uint_as_float(x[i]) * sc : -INFINITY);
-        }
-      }
-      float bmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      if (pos_scale) bmax *= a.scale_log2;
+      const float bmax = row_block_max(sb, lim, whole, pos_scale, a.scale_log2);
       // O_t is stable and the P buffer free once PV_t(j-1) has completed
       if (j > 0 && !(ok = __all_sync(0xffffffffu, dev::mbar_wait(pv_done(t), (j - 1) & 1)))) break;
       if (j > 0) {
@@ -749,38 +875,8 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
       } else {
         m_ref = bmax;
       }
-      float ls[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) ls[u] = 0.f;
-      const uint32_t prow = SL::p + t * SL::kP + r * 128;
-#pragma unroll 1
-      for (int ch = 0; ch < kTcKeys / 32; ++ch) {
-        uint32_t x[32];
-        dev::tmem_ld32(sb + ch * 32, x);
-        dev::tmem_wait_ld();
-        const int lc = whole ? 32 : lim - ch * 32;
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float p0 = dev::ex2(fmaf(__uint_as_float(x[2 * e]), a.scale_log2, -m_ref));
-          float p1 = dev::ex2(fmaf(__uint_as_float(x[2 * e + 1]), a.scale_log2, -m_ref));
-          if (!whole) {
-            p0 = 2 * e <= lc ? p0 : 0.f;
-            p1 = 2 * e + 1 <= lc ? p1 : 0.f;
-          }
-          pk[e] = dev::pack_bf16x2(p0, p1);
-          ls[(2 * e) & 7] += dev::bf16lo_to_f32(pk[e]);
-          ls[(2 * e + 1) & 7] += dev::bf16hi_to_f32(pk[e]);
-        }
-        const uint32_t dst = prow + (ch >> 1) * SL::kSub;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int c16 = (ch & 1) * 4 + u;
-          *reinterpret_cast<uint4 *>(bp + dst + ((c16 ^ (r & 7)) << 4)) =
-              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-        }
-      }
-      lsum += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      lsum += row_block_exp(sb, bp, SL::p + t * SL::kP + r * 128, SL::kSub, r, lim, whole,
+                            a.scale_log2, m_ref);
       const int nk = min(kTcKeys, t_end - k0);  // keys the CTA staged in this block
       if (nk < kTcKeys) {  // the CTA's last block: V rows past its keys are stale or unowned
         const int s = j % KSV;
