@@ -177,24 +177,26 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
-// Pass 1: the row's maximum scaled score over the block's columns c <= lim (all of them
-// when `whole`).  With a positive scale, the max of the raw scores scaled once equals
-// the max of the scaled scores (rounding is monotonic).
-__device__ __forceinline__ float row_block_max(uint32_t sb, int lim, bool whole, bool pos_scale,
-                                               float scale_log2) {
+// Pass 1: the row's maximum scaled score over the columns c <= lim (all of them when
+// `whole`) of NCH 32-column chunks starting at chunk ch0.  With a positive scale, the
+// max of the raw scores scaled once equals the max of the scaled scores (rounding is
+// monotonic).
+template <int NCH>
+__device__ __forceinline__ float row_block_max(uint32_t sb, int ch0, int lim, bool whole,
+                                               bool pos_scale, float scale_log2) {
   float mx[8];
 #pragma unroll
   for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
   const float sc = pos_scale ? 1.f : scale_log2;
   uint32_t xa[32], xb[32];
-  dev::tmem_ld32(sb, xa);
+  dev::tmem_ld32(sb + ch0 * 32, xa);
   tmem_wait_ld_regs(xa);
 #pragma unroll
-  for (int ch = 0; ch < kTcKeys / 32; ++ch) {
+  for (int ch = 0; ch < NCH; ++ch) {
     uint32_t(&cur)[32] = (ch & 1) ? xb : xa;
     uint32_t(&nxt)[32] = (ch & 1) ? xa : xb;
-    if (ch + 1 < kTcKeys / 32) dev::tmem_ld32(sb + (ch + 1) * 32, nxt);
-    const int lc = lim - ch * 32;
+    if (ch + 1 < NCH) dev::tmem_ld32(sb + (ch0 + ch + 1) * 32, nxt);
+    const int lc = lim - (ch0 + ch) * 32;
     if (whole && pos_scale) {
 #if PKV_PREFILL_MAX3
 #pragma unroll
@@ -212,33 +214,36 @@ __device__ __forceinline__ float row_block_max(uint32_t sb, int lim, bool whole,
       for (int i = 0; i < 32; ++i)
         mx[i & 7] = fmaxf(mx[i & 7], i <= lc ? __uint_as_float(cur[i]) * sc : -INFINITY);
     }
-    if (ch + 1 < kTcKeys / 32) tmem_wait_ld_regs(nxt);
+    if (ch + 1 < NCH) tmem_wait_ld_regs(nxt);
   }
   float bmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                      fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
   return pos_scale ? bmax * scale_log2 : bmax;
 }
 
-// Pass 2: P = exp2(S * scale - m_ref) for the block's columns c <= lim (0 past it),
-// rounded to bf16 and stored into row r of the P buffer at shared offset `prow`
-// (K-major, 128-byte swizzle: two 64-column sub-tiles `sub` bytes apart); returns the
-// sum of the rounded values, which is what the tensor cores multiply.  The first
-// PKV_PREFILL_POLY_PAIRS column pairs of each 32-column chunk take exp2_fma.
-__device__ __forceinline__ float row_block_exp(uint32_t sb, uint8_t *bp, uint32_t prow,
+// Pass 2: P = exp2(S * scale - m_ref) for the columns c <= lim (0 past it) of NCH
+// 32-column chunks starting at chunk ch0, rounded to bf16 and stored into row r of the
+// P buffer at shared offset `prow` (K-major, 128-byte swizzle: two 64-column sub-tiles
+// `sub` bytes apart); returns the sum of the rounded values, which is what the tensor
+// cores multiply.  The first PKV_PREFILL_POLY_PAIRS column pairs of each chunk take
+// exp2_fma.
+template <int NCH>
+__device__ __forceinline__ float row_block_exp(uint32_t sb, int ch0, uint8_t *bp, uint32_t prow,
                                                uint32_t sub, int r, int lim, bool whole,
                                                float scale_log2, float m_ref) {
   float ls[8];
 #pragma unroll
   for (int u = 0; u < 8; ++u) ls[u] = 0.f;
   uint32_t xa[32], xb[32];
-  dev::tmem_ld32(sb, xa);
+  dev::tmem_ld32(sb + ch0 * 32, xa);
   tmem_wait_ld_regs(xa);
 #pragma unroll
-  for (int ch = 0; ch < kTcKeys / 32; ++ch) {
+  for (int ch = 0; ch < NCH; ++ch) {
     uint32_t(&cur)[32] = (ch & 1) ? xb : xa;
     uint32_t(&nxt)[32] = (ch & 1) ? xa : xb;
-    if (ch + 1 < kTcKeys / 32) dev::tmem_ld32(sb + (ch + 1) * 32, nxt);
-    const int lc = whole ? 32 : lim - ch * 32;
+    if (ch + 1 < NCH) dev::tmem_ld32(sb + (ch0 + ch + 1) * 32, nxt);
+    const int cha = ch0 + ch;  // absolute chunk
+    const int lc = whole ? 32 : lim - cha * 32;
     uint32_t pk[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
@@ -272,17 +277,114 @@ __device__ __forceinline__ float row_block_exp(uint32_t sb, uint8_t *bp, uint32_
       ls[(2 * e + 1) & 7] += dev::bf16hi_to_f32(pk[e]);
 #endif
     }
-    const uint32_t dst = prow + (ch >> 1) * sub;
+    const uint32_t dst = prow + (cha >> 1) * sub;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int c16 = (ch & 1) * 4 + u;
+      const int c16 = (cha & 1) * 4 + u;
       *reinterpret_cast<uint4 *>(bp + dst + ((c16 ^ (r & 7)) << 4)) =
           make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
     }
-    if (ch + 1 < kTcKeys / 32) tmem_wait_ld_regs(nxt);
+    if (ch + 1 < NCH) tmem_wait_ld_regs(nxt);
   }
   return ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
 }
+
+// The same two passes from one read of the row's chunks into registers (TMEM is read
+// once per block instead of twice).
+template <int NCH>
+__device__ __forceinline__ void row_block_load(uint32_t sb, int ch0, uint32_t (&x)[NCH * 32]) {
+#pragma unroll
+  for (int ch = 0; ch < NCH; ++ch) {
+    uint32_t(&c)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[ch * 32]);
+    dev::tmem_ld32(sb + (ch0 + ch) * 32, c);
+  }
+#pragma unroll
+  for (int ch = 0; ch < NCH; ++ch) {
+    uint32_t(&c)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[ch * 32]);
+    if (ch == 0)
+      tmem_wait_ld_regs(c);  // one wait covers every load above
+    else
+      asm volatile("" : "+r"(c[0]), "+r"(c[1]), "+r"(c[2]), "+r"(c[3]), "+r"(c[4]), "+r"(c[5]),
+                   "+r"(c[6]), "+r"(c[7]), "+r"(c[8]), "+r"(c[9]), "+r"(c[10]), "+r"(c[11]),
+                   "+r"(c[12]), "+r"(c[13]), "+r"(c[14]), "+r"(c[15]), "+r"(c[16]), "+r"(c[17]),
+                   "+r"(c[18]), "+r"(c[19]), "+r"(c[20]), "+r"(c[21]), "+r"(c[22]), "+r"(c[23]),
+                   "+r"(c[24]), "+r"(c[25]), "+r"(c[26]), "+r"(c[27]), "+r"(c[28]), "+r"(c[29]),
+                   "+r"(c[30]), "+r"(c[31]));
+  }
+}
+
+template <int NCH>
+__device__ __forceinline__ float row_regs_max(const uint32_t (&x)[NCH * 32], int ch0, int lim,
+                                              bool whole, bool pos_scale, float scale_log2) {
+  float mx[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
+  const float sc = pos_scale ? 1.f : scale_log2;
+  if (whole && pos_scale) {
+#pragma unroll
+    for (int i = 0; i < NCH * 32; i += 2)
+      mx[(i >> 1) & 7] = fmax3(mx[(i >> 1) & 7], __uint_as_float(x[i]), __uint_as_float(x[i + 1]));
+  } else if (whole) {
+#pragma unroll
+    for (int i = 0; i < NCH * 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(x[i]) * sc);
+  } else {
+    const int lc = lim - ch0 * 32;
+#pragma unroll
+    for (int i = 0; i < NCH * 32; ++i)
+      mx[i & 7] = fmaxf(mx[i & 7], i <= lc ? __uint_as_float(x[i]) * sc : -INFINITY);
+  }
+  const float bmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                           fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+  return pos_scale ? bmax * scale_log2 : bmax;
+}
+
+template <int NCH>
+__device__ __forceinline__ float row_regs_exp(const uint32_t (&x)[NCH * 32], int ch0, uint8_t *bp,
+                                              uint32_t prow, uint32_t sub, int r, int lim,
+                                              bool whole, float scale_log2, float m_ref) {
+  float ls[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) ls[u] = 0.f;
+#pragma unroll
+  for (int ch = 0; ch < NCH; ++ch) {
+    const int cha = ch0 + ch;
+    const int lc = whole ? 32 : lim - cha * 32;
+    uint32_t pk[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      float a0, a1;
+      fma_f32x2(__uint_as_float(x[ch * 32 + 2 * e]), __uint_as_float(x[ch * 32 + 2 * e + 1]),
+                scale_log2, -m_ref, a0, a1);
+      float p0 = dev::ex2(a0), p1 = dev::ex2(a1);
+      if (!whole) {
+        p0 = 2 * e <= lc ? p0 : 0.f;
+        p1 = 2 * e + 1 <= lc ? p1 : 0.f;
+      }
+      pk[e] = dev::pack_bf16x2(p0, p1);
+      ls[e & 7] = add_bf16x2(pk[e], ls[e & 7]);
+    }
+    const uint32_t dst = prow + (cha >> 1) * sub;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c16 = (cha & 1) * 4 + u;
+      *reinterpret_cast<uint4 *>(bp + dst + ((c16 ^ (r & 7)) << 4)) =
+          make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+    }
+  }
+  return ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+}
+
+// Whether the softmax reads a row's block from TMEM once into registers (1) or in each
+// of the two passes (0), by head_dim: once at 128 (measured 7% faster), twice at 64,
+// where the extra live registers cost more than the second read.
+#ifndef PKV_PREFILL_ROW_ONCE128
+#define PKV_PREFILL_ROW_ONCE128 1
+#endif
+#ifndef PKV_PREFILL_ROW_ONCE64
+#define PKV_PREFILL_ROW_ONCE64 0
+#endif
+template <int D>
+__host__ __device__ constexpr bool row_once() { return D == 128 ? PKV_PREFILL_ROW_ONCE128 != 0 : PKV_PREFILL_ROW_ONCE64 != 0; }
 
 // ---------------------------------------------------------------------------
 // Tensor-core issue.  A tcgen05.mma returns to the issuing thread only once the tensor
@@ -518,7 +620,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t sbase = tmem + lane_base + 128u * (j & 1);
       const bool whole = __all_sync(0xffffffffu, lim >= kTcKeys - 1);  // no column masked
       // pass 1: the block's row max
-      const float bmax = row_block_max(sbase, lim, whole, pos_scale, a.scale_log2);
+      uint32_t xrow[row_once<D>() ? kTcKeys : 1];
+      float bmax;
+      if constexpr (row_once<D>()) {
+        row_block_load<kTcKeys / 32>(sbase, 0, xrow);
+        bmax = row_regs_max<kTcKeys / 32>(xrow, 0, lim, whole, pos_scale, a.scale_log2);
+      } else {
+        bmax = row_block_max<kTcKeys / 32>(sbase, 0, lim, whole, pos_scale, a.scale_log2);
+      }
       if (j > 0) {
         const bool need = bmax > m_ref + kTcRescale;
         if (__any_sync(0xffffffffu, need)) {  // O moves: wait until the previous P.V is in
@@ -549,8 +658,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                       dev::mbar_wait(pv_done(j & 1), ((j - 2) >> 1) & 1))))
         break;
       // pass 2: P = exp2(S - m_ref) as bf16 into shared memory, and its row sum
-      lsum += row_block_exp(sbase, bp, SL::p + (j & 1) * SL::kP + r * 128, SL::kSub, r, lim, whole,
-                            a.scale_log2, m_ref);
+      if constexpr (row_once<D>())
+        lsum += row_regs_exp<kTcKeys / 32>(xrow, 0, bp, SL::p + (j & 1) * SL::kP + r * 128, SL::kSub,
+                                           r, lim, whole, a.scale_log2, m_ref);
+      else
+        lsum += row_block_exp<kTcKeys / 32>(sbase, 0, bp, SL::p + (j & 1) * SL::kP + r * 128,
+                                            SL::kSub, r, lim, whole, a.scale_log2, m_ref);
       // S read: the MMA warp may refill this buffer
       dev::tc_fence_before();
       __syncwarp();
@@ -625,9 +738,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // PV_t(j) runs; it waits for PV_t(j) (pv_done) before it rescales O_t or overwrites P_t.
 // Row arithmetic (positions, masking, lazy rescale, bf16 row sums) is the one-tile
 // kernel's.  head_dim 64: K and V rings of 3; head_dim 128: K ring of 2, V ring of 1.
-constexpr int kTc2Threads = 320;  // softmax warpgroups 0 and 1, producer warp 8, MMA warp 9
+// H softmax threads per query row: with H = 2, two warps share each 32-row lane quadrant,
+// one taking the first 64 columns of every key block, the other the last 64; their row
+// maxima and row sums are combined through shared memory.  Warps 0 .. 8H-1 are the two
+// tiles' softmax warps (tile t: warps 8H/2 t .. ), then the producer and MMA warps.
+template <int H>
+constexpr int tc2_threads() { return 32 * (8 * H + 2); }
 
-template <int D>
+template <int D, int H>
 struct Tc2Smem {
   static constexpr int KSK = D == 64 ? 3 : 2;        // stages of the K ring
   static constexpr int KSV = D == 64 ? 3 : 1;        // stages of the V ring
@@ -638,19 +756,27 @@ struct Tc2Smem {
   static constexpr uint32_t q = v + KSV * kTile;     // two Q tiles
   static constexpr uint32_t p = q + 2 * kTile;       // two P buffers [2][128 rows][128 B]
   static constexpr uint32_t kP = 2 * kSub;
-  static constexpr uint32_t bars = p + 2 * kP;
-  static constexpr int kBars = 2 * KSK + 2 * KSV + 8;
+  // H = 2: the halves' row values, [2 buffers][2 tiles][2 halves][128 rows] fp32
+  static constexpr uint32_t xchg = p + 2 * kP;
+  static constexpr uint32_t bars = xchg + (H == 2 ? 2 * 2 * 2 * kTcRows * 4 : 0);
+  // the rings, s_full/p_full/pv_done per tile, q_ready, mma_done, and with H = 2 one
+  // barrier per (tile, lane quadrant) where the two halves of its rows meet
+  static constexpr int kBars = 2 * KSK + 2 * KSV + 8 + (H == 2 ? 8 : 0);
   static constexpr uint32_t tslot = bars + kBars * 8;
   static constexpr uint32_t flag = tslot + 8;
   static constexpr uint32_t total = flag + 8;
 };
 
-template <int D>
-__global__ void __launch_bounds__(kTc2Threads, 1)
+template <int D, int H>
+__global__ void __launch_bounds__(tc2_threads<H>(), 1)
     prefill_tc2_kernel(const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, const PrefillArgs a) {
-  using SL = Tc2Smem<D>;
+  using SL = Tc2Smem<D, H>;
   constexpr int KSK = SL::KSK, KSV = SL::KSV;
+  constexpr int kSoftWarps = 8 * H;        // softmax warps of both tiles
+  constexpr int kTileWarps = 4 * H;        // softmax warps of one tile
+  constexpr int kProducer = kSoftWarps, kMma = kSoftWarps + 1;
+  constexpr int NCH = kTcKeys / 32 / H;    // 32-column chunks of a block per thread
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = dev::smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -666,6 +792,7 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
   auto pv_done = [&](int t) { return bars + 8u * (R4 + 4 + t); };
   const uint32_t q_ready = bars + 8u * (R4 + 6);
   const uint32_t mma_done = bars + 8u * (R4 + 7);
+  auto pair_bar = [&](int t, int wq) { return bars + 8u * (R4 + 8 + 4 * t + wq); };
   volatile uint32_t *const s_tmem = reinterpret_cast<volatile uint32_t *>(bp + SL::tslot);
   volatile int *const s_flag = reinterpret_cast<volatile int *>(bp + SL::flag);
 
@@ -709,7 +836,10 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
     for (int i = 0; i < SL::kBars; ++i) {
       const uint32_t bar = bars + 8u * i;
       const bool per_warp = bar == p_full(0) || bar == p_full(1);
-      dev::mbar_init(bar, per_warp ? 4u : (bar == q_ready ? 8u : 1u));
+      const bool pair = i >= R4 + 8;  // every thread of the two halves' warps arrives
+      dev::mbar_init(bar, pair ? 64u
+                               : per_warp ? (uint32_t)kTileWarps
+                                          : (bar == q_ready ? (uint32_t)kSoftWarps : 1u));
     }
     *s_flag = 0;
     dev::fence_mbar_init();
@@ -729,7 +859,7 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
   };
   int k_issued = 0, v_issued = 0;
 
-  if (warp == 8) {
+  if (warp == kProducer) {
     // ------------------------------------------------------------- producer warp
     const uint64_t policy = dev::policy_evict_last();
     const int32_t *trow = a.block_tables + (int64_t)b * a.max_blocks;
@@ -761,7 +891,7 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
         v_issued = jv + 1;
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == kMma) {
     // ------------------------------------------------- tensor-core issue (one thread)
     if (lane == 0) {
       constexpr uint32_t id_s = dev::idesc_bf16_f32(kTcRows, kTcKeys, 0);
@@ -815,23 +945,45 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
       dev::umma_commit(mma_done);
     }
   } else {
-    // ------------------------------------------------- softmax warpgroup t, row = lane
-    const int t = warp >> 2;
-    const int r = 32 * (warp & 3) + lane;
+    // ------------------------- softmax warps of tile t: row r, half hc of each block
+    const int t = warp / kTileWarps;
+    const int wq = warp & 3;                       // TMEM lane quadrant of this warp
+    const int hc = (warp % kTileWarps) >> 2;       // which H-th of the columns
+    const int r = 32 * wq + lane;
     const int gr = row0 + t * kTcRows + r;
     const bool valid = gr < rows;
     const int last_row_t = min(row0 + t * kTcRows + kTcRows, rows) - 1;
     const int qi = valid ? gr / G : (last_row_t >= 0 ? last_row_t / G : 0);
     const int h = valid ? gr - (gr / G) * G : 0;
     const int pos = L - n + qi;
-    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
     const uint32_t sb = tmem + lane_base + 128u * t;
     const uint32_t ob = tmem + lane_base + 256u + (uint32_t)(D * t);
-    {  // this tile's query rows (zeros past the end)
+    // The two halves of a row exchange a value through shared memory: use k writes
+    // buffer k & 1 and arrives on the pair's barrier (every thread of both warps), whose
+    // phase k then publishes both values.  A half is at most one phase ahead of the
+    // other, so it never overwrites a buffer its partner has yet to read.  The wait is
+    // bounded; if it gives up, the row keeps its own value and the error is raised.
+    float *const xchg = reinterpret_cast<float *>(bp + SL::xchg);  // [buf][t][half][row]
+    auto other_half = [&](float v, int use, bool &good) -> float {
+      if constexpr (H == 2) {
+        xchg[(((use & 1) * 2 + t) * 2 + hc) * kTcRows + r] = v;
+        dev::mbar_arrive(pair_bar(t, wq));
+        if (!__all_sync(0xffffffffu, dev::mbar_wait(pair_bar(t, wq), use & 1))) {
+          good = false;
+          return v;
+        }
+        return xchg[(((use & 1) * 2 + t) * 2 + (hc ^ 1)) * kTcRows + r];
+      } else {
+        return v;
+      }
+    };
+    {  // this tile's query rows (zeros past the end): chunks [hc D/8/H, (hc+1) D/8/H)
       const uint4 *src = reinterpret_cast<const uint4 *>(
           a.q + ((int64_t)(q0 + qi) * a.num_q_heads + g * G + h) * D);
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
+      for (int cc = 0; cc < D / 8 / H; ++cc) {
+        const int c = hc * (D / 8 / H) + cc;
         const uint4 v = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
         *reinterpret_cast<uint4 *>(bp + SL::q + t * SL::kTile + (c >> 3) * SL::kSub + r * 128 +
                                    (((c & 7) ^ (r & 7)) << 4)) = v;
@@ -850,17 +1002,27 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
       const int lim = min(pos, te - 1) - k0;
       if (!(ok = __all_sync(0xffffffffu, dev::mbar_wait(s_full(t), j & 1)))) break;
       dev::tc_fence_after();
+      // the same for both halves of a row: its rows and the block are the same
       const bool whole = __all_sync(0xffffffffu, lim >= kTcKeys - 1);
-      const float bmax = row_block_max(sb, lim, whole, pos_scale, a.scale_log2);
+      uint32_t xrow[row_once<D>() ? NCH * 32 : 1];
+      float hmax;
+      if constexpr (row_once<D>()) {
+        row_block_load<NCH>(sb, hc * NCH, xrow);
+        hmax = row_regs_max<NCH>(xrow, hc * NCH, lim, whole, pos_scale, a.scale_log2);
+      } else {
+        hmax = row_block_max<NCH>(sb, hc * NCH, lim, whole, pos_scale, a.scale_log2);
+      }
+      const float bmax = fmaxf(hmax, other_half(hmax, j, ok));
+      if (!ok) break;
       // O_t is stable and the P buffer free once PV_t(j-1) has completed
       if (j > 0 && !(ok = __all_sync(0xffffffffu, dev::mbar_wait(pv_done(t), (j - 1) & 1)))) break;
       if (j > 0) {
         const bool need = bmax > m_ref + kTcRescale;
-        if (__any_sync(0xffffffffu, need)) {
+        if (__any_sync(0xffffffffu, need)) {  // each half rescales its D/H columns of O
           const float m_new = fmaxf(m_ref, bmax);
           const float f = need ? dev::ex2(m_ref - m_new) : 1.f;
 #pragma unroll 1
-          for (int ch = 0; ch < D / 32; ++ch) {
+          for (int ch = hc * (D / 32 / H); ch < (hc + 1) * (D / 32 / H); ++ch) {
             uint32_t o[32];
             dev::tmem_ld32(ob + ch * 32, o);
             dev::tmem_wait_ld();
@@ -875,14 +1037,18 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
       } else {
         m_ref = bmax;
       }
-      lsum += row_block_exp(sb, bp, SL::p + t * SL::kP + r * 128, SL::kSub, r, lim, whole,
-                            a.scale_log2, m_ref);
+      if constexpr (row_once<D>())
+        lsum += row_regs_exp<NCH>(xrow, hc * NCH, bp, SL::p + t * SL::kP + r * 128, SL::kSub, r,
+                                  lim, whole, a.scale_log2, m_ref);
+      else
+        lsum += row_block_exp<NCH>(sb, hc * NCH, bp, SL::p + t * SL::kP + r * 128, SL::kSub, r,
+                                   lim, whole, a.scale_log2, m_ref);
       const int nk = min(kTcKeys, t_end - k0);  // keys the CTA staged in this block
       if (nk < kTcKeys) {  // the CTA's last block: V rows past its keys are stale or unowned
         const int s = j % KSV;
         if (!(ok = __all_sync(0xffffffffu, dev::mbar_wait(v_full(s), (j / KSV) & 1)))) break;
         const uint32_t vt = SL::v + s * SL::kTile;
-        for (int idx = r; idx < (kTcKeys - nk) * (D / 8); idx += kTcRows) {
+        for (int idx = hc * kTcRows + r; idx < (kTcKeys - nk) * (D / 8); idx += H * kTcRows) {
           const int row = nk + idx / (D / 8), c = idx % (D / 8);
           *reinterpret_cast<uint4 *>(bp + vt + (c >> 3) * SL::kSub + row * 128 +
                                      (((c & 7) ^ (row & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
@@ -894,13 +1060,16 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
       if (lane == 0) dev::mbar_arrive(p_full(t));
     }
     if (!ok && lane == 0) fail(false);
+    // the row sum: both halves' parts (exchange number nb of the pair)
+    float ltot = lsum;
+    if (H == 2 && ok) ltot = lsum + other_half(lsum, nb, ok);
     if (ok && nb > 0 && __all_sync(0xffffffffu, dev::mbar_wait(pv_done(t), (nb - 1) & 1))) {
       dev::tc_fence_after();
-      const float inv = 1.f / lsum;
+      const float inv = 1.f / ltot;
       uint4 *dst = reinterpret_cast<uint4 *>(
           a.out + ((int64_t)(q0 + qi) * a.num_q_heads + g * G + h) * D);
 #pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
+      for (int ch = hc * (D / 32 / H); ch < (hc + 1) * (D / 32 / H); ++ch) {
         uint32_t o[32];
         dev::tmem_ld32(ob + ch * 32, o);
         dev::tmem_wait_ld();
@@ -922,7 +1091,7 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
   }
 
   if (tid == 0) (void)dev::mbar_wait(mma_done, 0);
-  if (warp == 8 && lane == 0 && *s_flag) {
+  if (warp == kProducer && lane == 0 && *s_flag) {
     for (int s = 0; s < KSK; ++s) {
       const int kl = s + ((k_issued - 1 - s) / KSK) * KSK;
       if (kl >= 0 && kl < k_issued) (void)dev::mbar_wait(k_full(s), (kl / KSK) & 1);
@@ -942,8 +1111,15 @@ cudaError_t read_prefill_errors(uint32_t *flags, int clear) { return read_tu_err
 
 constexpr size_t tc_smem(int d) { return 1024 + (d == 64 ? TcSmem<64>::total : TcSmem<128>::total); }
 static_assert(tc_smem(64) <= 227 * 1024 && tc_smem(128) <= 227 * 1024, "prefill tile fits a CTA");
+// Softmax threads per query row of the two-tile kernel, by head_dim.  Two at head_dim 64
+// (where the softmax bounds the kernel) measured within a few percent of one (+3.5% on a
+// 256-sequence batch, -1% on 16 long sequences), so one is kept at both.
+#ifndef PKV_PREFILL_HALVES64
+#define PKV_PREFILL_HALVES64 1
+#endif
+constexpr int tc2_halves(int d) { return d == 64 ? PKV_PREFILL_HALVES64 : 1; }
 constexpr size_t tc2_smem(int d) {
-  return 1024 + (d == 64 ? Tc2Smem<64>::total : Tc2Smem<128>::total);
+  return 1024 + (d == 64 ? Tc2Smem<64, tc2_halves(64)>::total : Tc2Smem<128, tc2_halves(128)>::total);
 }
 static_assert(tc2_smem(64) <= 227 * 1024 && tc2_smem(128) <= 227 * 1024,
               "two prefill tiles fit a CTA");
@@ -999,10 +1175,10 @@ PKV_API int paged_prefill_attention(pkv_bf16 *out, const pkv_bf16 *q, const pkv_
     if (!g_prefill_attr[dev][vi]) {
       cudaError_t e;
       if (two)
-        e = D == 64 ? cudaFuncSetAttribute(prefill_tc2_kernel<64>,
+        e = D == 64 ? cudaFuncSetAttribute(prefill_tc2_kernel<64, tc2_halves(64)>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)tc2_smem(64))
-                    : cudaFuncSetAttribute(prefill_tc2_kernel<128>,
+                    : cudaFuncSetAttribute(prefill_tc2_kernel<128, tc2_halves(128)>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)tc2_smem(128));
       else
@@ -1035,9 +1211,9 @@ PKV_API int paged_prefill_attention(pkv_bf16 *out, const pkv_bf16 *q, const pkv_
   dim3 grid((unsigned)tiles, (unsigned)cache->num_kv_heads, (unsigned)num_seqs);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (two && D == 64)
-    prefill_tc2_kernel<64><<<grid, kTc2Threads, tc2_smem(64), s>>>(tmk, tmv, a);
+    prefill_tc2_kernel<64, tc2_halves(64)><<<grid, tc2_threads<tc2_halves(64)>(), tc2_smem(64), s>>>(tmk, tmv, a);
   else if (two)
-    prefill_tc2_kernel<128><<<grid, kTc2Threads, tc2_smem(128), s>>>(tmk, tmv, a);
+    prefill_tc2_kernel<128, tc2_halves(128)><<<grid, tc2_threads<tc2_halves(128)>(), tc2_smem(128), s>>>(tmk, tmv, a);
   else if (D == 64)
     prefill_tc_kernel<64><<<grid, kTcThreads, tc_smem(64), s>>>(tmk, tmv, a);
   else
