@@ -22,6 +22,12 @@
 #ifndef PKV_PREFILL_FMA2
 #define PKV_PREFILL_FMA2 1
 #endif
+// Row sums of the two-tile kernel at head_dim 64 formed by the tensor core (a column of
+// ones appended to V) instead of by the softmax threads.
+#ifndef PKV_PREFILL_SUM_MMA64
+#define PKV_PREFILL_SUM_MMA64 1
+#endif
+
 // Row sums of the bf16 weights with mixed-precision adds (1) or widen-then-add (0).
 #ifndef PKV_PREFILL_SUM_MIXED
 #define PKV_PREFILL_SUM_MIXED 1
@@ -177,6 +183,16 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
+// One 32-bit TMEM column of this thread's lane (load: complete with a wait).
+__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
+  uint32_t x;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(x) : "r"(taddr));
+  return x;
+}
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t x) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(x) : "memory");
+}
+
 // Pass 1: the row's maximum scaled score over the columns c <= lim (all of them when
 // `whole`) of NCH 32-column chunks starting at chunk ch0.  With a positive scale, the
 // max of the raw scores scaled once equals the max of the scaled scores (rounding is
@@ -227,7 +243,7 @@ __device__ __forceinline__ float row_block_max(uint32_t sb, int ch0, int lim, bo
 // `sub` bytes apart); returns the sum of the rounded values, which is what the tensor
 // cores multiply.  The first PKV_PREFILL_POLY_PAIRS column pairs of each chunk take
 // exp2_fma.
-template <int NCH>
+template <int NCH, bool kSum = true>
 __device__ __forceinline__ float row_block_exp(uint32_t sb, int ch0, uint8_t *bp, uint32_t prow,
                                                uint32_t sub, int r, int lim, bool whole,
                                                float scale_log2, float m_ref) {
@@ -270,12 +286,14 @@ __device__ __forceinline__ float row_block_exp(uint32_t sb, int ch0, uint8_t *bp
       pk[e] = dev::pack_bf16x2(p0, p1);
       // sum what the tensor cores multiply: with a stale reference max the largest P is
       // not a power of two, and only this keeps the weights a convex combination
+      if constexpr (kSum) {
 #if PKV_PREFILL_SUM_MIXED
-      ls[e & 7] = add_bf16x2(pk[e], ls[e & 7]);
+        ls[e & 7] = add_bf16x2(pk[e], ls[e & 7]);
 #else
-      ls[(2 * e) & 7] += dev::bf16lo_to_f32(pk[e]);
-      ls[(2 * e + 1) & 7] += dev::bf16hi_to_f32(pk[e]);
+        ls[(2 * e) & 7] += dev::bf16lo_to_f32(pk[e]);
+        ls[(2 * e + 1) & 7] += dev::bf16hi_to_f32(pk[e]);
 #endif
+      }
     }
     const uint32_t dst = prow + (cha >> 1) * sub;
 #pragma unroll
@@ -743,7 +761,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // maxima and row sums are combined through shared memory.  Warps 0 .. 8H-1 are the two
 // tiles' softmax warps (tile t: warps 8H/2 t .. ), then the producer and MMA warps.
 template <int H>
-constexpr int tc2_threads() { return 32 * (8 * H + 2); }
+__host__ __device__ constexpr int tc2_threads() { return 32 * (8 * H + 2); }
 
 template <int D, int H>
 struct Tc2Smem {
@@ -758,7 +776,11 @@ struct Tc2Smem {
   static constexpr uint32_t kP = 2 * kSub;
   // H = 2: the halves' row values, [2 buffers][2 tiles][2 halves][128 rows] fp32
   static constexpr uint32_t xchg = p + 2 * kP;
-  static constexpr uint32_t bars = xchg + (H == 2 ? 2 * 2 * 2 * kTcRows * 4 : 0);
+  // kOnes: a [128 keys][64] bf16 tile of ones, read by P.V as 16 extra B columns, so that
+  // the tensor core also forms each row's sum of the bf16 weights (in O's extra columns)
+  static constexpr bool kOnes = D == 64 && H == 1 && PKV_PREFILL_SUM_MMA64 != 0;
+  static constexpr uint32_t ones = (xchg + (H == 2 ? 2 * 2 * 2 * kTcRows * 4 : 0) + 1023u) & ~1023u;
+  static constexpr uint32_t bars = ones + (kOnes ? kSub : 0);
   // the rings, s_full/p_full/pv_done per tile, q_ready, mma_done, and with H = 2 one
   // barrier per (tile, lane quadrant) where the two halves of its rows meet
   static constexpr int kBars = 2 * KSK + 2 * KSV + 8 + (H == 2 ? 8 : 0);
@@ -777,6 +799,8 @@ __global__ void __launch_bounds__(tc2_threads<H>(), 1)
   constexpr int kTileWarps = 4 * H;        // softmax warps of one tile
   constexpr int kProducer = kSoftWarps, kMma = kSoftWarps + 1;
   constexpr int NCH = kTcKeys / 32 / H;    // 32-column chunks of a block per thread
+  constexpr bool kOnes = SL::kOnes;        // row sums from the tensor core
+  constexpr int kON = D + (kOnes ? 16 : 0);  // O columns per tile (then the row sums)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = dev::smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -844,11 +868,17 @@ __global__ void __launch_bounds__(tc2_threads<H>(), 1)
     *s_flag = 0;
     dev::fence_mbar_init();
   }
+  if constexpr (kOnes) {  // bf16 1.0 everywhere; read by the tensor cores (async proxy)
+    for (int i = tid; i < (int)(SL::kSub / 16); i += tc2_threads<H>())
+      *reinterpret_cast<uint4 *>(bp + SL::ones + i * 16) =
+          make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    dev::fence_proxy_async_smem();
+  }
   if (warp == 0) dev::tmem_alloc(base + SL::tslot, 512);
   dev::tc_fence_before();
   __syncthreads();
   dev::tc_fence_after();
-  const uint32_t tmem = *s_tmem;  // S of tile t at column 128 t, O of tile t at 256 + D t
+  const uint32_t tmem = *s_tmem;  // S of tile t at column 128 t, O of tile t at 256 + kON t
 
   auto fail = [&](bool ok) {
     if (!ok) {
@@ -895,7 +925,7 @@ __global__ void __launch_bounds__(tc2_threads<H>(), 1)
     // ------------------------------------------------- tensor-core issue (one thread)
     if (lane == 0) {
       constexpr uint32_t id_s = dev::idesc_bf16_f32(kTcRows, kTcKeys, 0);
-      constexpr uint32_t id_o = dev::idesc_bf16_f32(kTcRows, D, 1);
+      constexpr uint32_t id_o = dev::idesc_bf16_f32(kTcRows, kON, 1);
       bool ok = fail(dev::mbar_wait(q_ready, 0));
       int k_waited = 0;  // K blocks whose k_full this thread has seen
       auto need_k = [&](int j) {
@@ -907,7 +937,12 @@ __global__ void __launch_bounds__(tc2_threads<H>(), 1)
       };
       const uint64_t dq0 = dev::smem_desc(base + SL::q, 16, 1024);
       const uint64_t dk0 = dev::smem_desc(base + SL::k, 16, 1024);
-      const uint64_t dv0 = dev::smem_desc(base + SL::v, SL::kSub, 1024);
+      // V stage s as the MN-major B operand: the next 64 columns are V's other half
+      // (head_dim 128) or, with kOnes, the tile of ones, `lbo` bytes further on
+      auto dv = [&](int s) {
+        const uint32_t vs = SL::v + s * SL::kTile;
+        return dev::smem_desc(base + vs, kOnes ? SL::ones - vs : SL::kSub, 1024);
+      };
       const uint64_t dp0 = dev::smem_desc(base + SL::p, 16, 1024);
       auto issue_s = [&](int t, int j) {
         issue_qk<D>(tmem + 128u * t, desc_add(dq0, t * SL::kTile),
@@ -936,8 +971,8 @@ __global__ void __launch_bounds__(tc2_threads<H>(), 1)
             v_seen = true;
             dev::tc_fence_after();
           }
-          issue_pv(tmem + 256u + (uint32_t)(D * t), desc_add(dp0, t * SL::kP),
-                   desc_add(dv0, (j % KSV) * SL::kTile), SL::kSub, id_o, j > 0 ? 1u : 0u);
+          issue_pv(tmem + 256u + (uint32_t)(kON * t), desc_add(dp0, t * SL::kP), dv(j % KSV),
+                   SL::kSub, id_o, j > 0 ? 1u : 0u);
           dev::umma_commit(pv_done(t));
         }
         if (ok) dev::umma_commit(v_empty(j % KSV));
@@ -958,7 +993,7 @@ __global__ void __launch_bounds__(tc2_threads<H>(), 1)
     const int pos = L - n + qi;
     const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
     const uint32_t sb = tmem + lane_base + 128u * t;
-    const uint32_t ob = tmem + lane_base + 256u + (uint32_t)(D * t);
+    const uint32_t ob = tmem + lane_base + 256u + (uint32_t)(kON * t);
     // The two halves of a row exchange a value through shared memory: use k writes
     // buffer k & 1 and arrives on the pair's barrier (every thread of both warps), whose
     // phase k then publishes both values.  A half is at most one phase ahead of the
@@ -1030,6 +1065,11 @@ __global__ void __launch_bounds__(tc2_threads<H>(), 1)
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
             dev::tmem_st32(ob + ch * 32, o);
           }
+          if constexpr (kOnes) {  // the row sum in O's column D
+            const uint32_t sm = tmem_ld1(ob + D);
+            dev::tmem_wait_ld();
+            tmem_st1(ob + D, __float_as_uint(__uint_as_float(sm) * f));
+          }
           dev::tmem_wait_st();
           lsum *= f;
           if (need) m_ref = m_new;
@@ -1041,8 +1081,8 @@ __global__ void __launch_bounds__(tc2_threads<H>(), 1)
         lsum += row_regs_exp<NCH>(xrow, hc * NCH, bp, SL::p + t * SL::kP + r * 128, SL::kSub, r,
                                   lim, whole, a.scale_log2, m_ref);
       else
-        lsum += row_block_exp<NCH>(sb, hc * NCH, bp, SL::p + t * SL::kP + r * 128, SL::kSub, r,
-                                   lim, whole, a.scale_log2, m_ref);
+        lsum += row_block_exp<NCH, !kOnes>(sb, hc * NCH, bp, SL::p + t * SL::kP + r * 128, SL::kSub,
+                                           r, lim, whole, a.scale_log2, m_ref);
       const int nk = min(kTcKeys, t_end - k0);  // keys the CTA staged in this block
       if (nk < kTcKeys) {  // the CTA's last block: V rows past its keys are stale or unowned
         const int s = j % KSV;
@@ -1065,6 +1105,10 @@ __global__ void __launch_bounds__(tc2_threads<H>(), 1)
     if (H == 2 && ok) ltot = lsum + other_half(lsum, nb, ok);
     if (ok && nb > 0 && __all_sync(0xffffffffu, dev::mbar_wait(pv_done(t), (nb - 1) & 1))) {
       dev::tc_fence_after();
+      if constexpr (kOnes) {
+        ltot = __uint_as_float(tmem_ld1(ob + D));
+        dev::tmem_wait_ld();
+      }
       const float inv = 1.f / ltot;
       uint4 *dst = reinterpret_cast<uint4 *>(
           a.out + ((int64_t)(q0 + qi) * a.num_q_heads + g * G + h) * D);
