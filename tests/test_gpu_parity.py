@@ -43,13 +43,14 @@ def dev(inp):
 ABS_ONLY_BELOW = 2.56  # |oracle| at which the bf16 half-ulp term reaches 1e-2
 
 
-def check_attention(got: torch.Tensor, ref: torch.Tensor, tag: str) -> float:
+def check_attention(got: torch.Tensor, ref: torch.Tensor, tag: str,
+                    abs_only_below: float = ABS_ONLY_BELOW) -> float:
     got = got.cpu().double()
     assert torch.isfinite(got).all(), f"{tag}: non-finite output"
     err = (got - ref).abs()
     # every element: the absolute target where the output is small enough for a bf16
     # value to reach it, the target plus the output's own half-ulp elsewhere
-    bound = torch.where(ref.abs() <= ABS_ONLY_BELOW, torch.full_like(ref, ATOL),
+    bound = torch.where(ref.abs() <= abs_only_below, torch.full_like(ref, ATOL),
                         ATOL + RTOL * ref.abs())
     bad = err > bound
     assert not bool(bad.any()), (f"{tag}: {int(bad.sum())} outputs out of tolerance, max |diff| "
@@ -858,10 +859,14 @@ def test_workload_decode_step_rope(B, oracle, wid):
 
 
 @pytest.mark.parametrize("D,BS", [(64, 16), (128, 32)])
-def test_prefill_two_tiles_ragged(B, oracle, D, BS):
+@pytest.mark.parametrize("wide", [False, True])
+def test_prefill_two_tiles_ragged(B, oracle, D, BS, wide):
     """Enough (sequence, kv head) units (40 x 8 = 320 >= two waves on 152 SMs) that the
     launcher gives each CTA two 128-row query tiles: ragged lengths, chunk sizes from one
-    token to the whole sequence, tiles whose second half is empty."""
+    token to the whole sequence, tiles whose second half is empty.  With `wide`, scale 1
+    spreads the scores so that rows' maxima jump between key blocks and the rescale of O
+    in TMEM runs (at head_dim 64 it also rescales the row-sum column that the tensor core
+    accumulates)."""
     import itertools
     gen = torch.Generator().manual_seed(90 + D)
     lens = [int(x) for x in torch.randint(1, 261, (40,), generator=gen)]
@@ -871,14 +876,21 @@ def test_prefill_two_tiles_ragged(B, oracle, D, BS):
     inp = W.make_inputs(w, poison=True)
     qs = torch.tensor([0] + list(itertools.accumulate(chunks)), dtype=torch.int32)
     q = torch.randn(int(qs[-1]), 16, D, generator=gen).to(torch.bfloat16)
+    scale = 1.0 if wide else inp["scale"]
     ref = oracle.prefill(q, inp["k_cache"], inp["v_cache"], inp["block_tables"], inp["context_lens"],
-                         qs, inp["scale"])
+                         qs, scale)
     g = dev(inp)
     out = torch.full((int(qs[-1]), 16, D), float("nan"), dtype=torch.bfloat16, device="cuda")
     B.paged_prefill_attention(out, q.cuda(), g["k_cache"], g["v_cache"], g["block_tables"],
                               g["context_lens"], inp["max_context_len"], qs.cuda(), max(chunks),
-                              inp["scale"])
-    check_attention(out, ref, f"two-tile prefill D={D} BS={BS}")
+                              scale)
+    # At scale 1 the scores spread over tens of units (base 2), the lazy reference max is
+    # often stale by up to 2^8, and each weight enters P.V as one bf16 value (2^-9
+    # relative).  Those weights' rounding then adds up to another 2^-9 |out| on top of the
+    # output's own bf16 half-ulp, so here the 2^-8 |oracle| term applies to every element
+    # (measured at head_dim 128: 2 of 5.5 M outputs between 1e-2 and 1.6e-2).
+    check_attention(out, ref, f"two-tile prefill D={D} BS={BS} scale={scale}",
+                    abs_only_below=0.0 if wide else ABS_ONLY_BELOW)
     assert_no_device_errors(B)
 
 
