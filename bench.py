@@ -31,6 +31,12 @@ inputs copied from pinned host memory and the output read back each step;
 graph per step (the eager time is reported beside it).
 
 `--impl reference` times that oracle as the reference arm (rank 0 only).
+
+Other modes, each printing one JSON line of its own: `--kernel prefill | rope_write |
+rope_step` time those entry points on the workload's shapes; `--kernel split
+--partition P` times paged_decode_split + paged_decode_combine at a fixed partition
+size; `--consumer fma` switches the partition decode kernel's consumer warps to their
+CUDA-core form (pkv_set_decode_consumer) for comparison with the default tensor form.
 """
 
 from __future__ import annotations
