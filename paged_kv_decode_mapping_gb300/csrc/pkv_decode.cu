@@ -877,7 +877,8 @@ struct PersistSmem {
   static constexpr uint32_t desc = q + STAGES * kQSlot;
   static constexpr uint32_t bars = desc + STAGES * sizeof(ItemDesc);  // full[STAGES], empty[STAGES]
   static constexpr uint32_t flags = bars + STAGES * 16;               // flag, last, issued, T
-  static constexpr uint32_t hist_nf = flags + 16;                     // full partitions by nf
+  static constexpr uint32_t ord = flags + 16;                         // order-ready barrier, ex0
+  static constexpr uint32_t hist_nf = ord + 16;                       // full partitions by nf
   static constexpr uint32_t hist_lc = hist_nf + kMaxCategories * 4;   // single partitions by q
   static constexpr uint32_t hist_ml = hist_lc + kMaxCategories * 4;   // multi-partition last, by q
   static constexpr uint32_t off = hist_ml + kMaxCategories * 4;       // [kMaxCategories + 1]
@@ -901,7 +902,7 @@ struct Item {
 //                      nf = 0, else Q + kMergeChunks if T > 0, else q + kMergeChunks)
 //                      is Q + kMergeChunks - (c - (R-1)).
 __device__ __forceinline__ bool find_item(int k, const int *s_off, int ncat, int R, int P, int Hkv,
-                                          int T, int num_seqs, const uint16_t *s_lt,
+                                          int T, int num_seqs, int Ex, const uint16_t *s_lt,
                                           const uint8_t *s_nf, int lane, Item &it) {
   if (k >= s_off[ncat]) return false;
   // category: the last c with s_off[c] <= k (s_off is nondecreasing; that one is non-empty)
@@ -914,7 +915,12 @@ __device__ __forceinline__ bool find_item(int k, const int *s_off, int ncat, int
   const bool full = cat < R - 1;
   const int r = R - 2 - cat;                                   // full: partition index
   const int q = (P / kChunk) + kMergeChunks - (cat - (R - 1));  // last partition: its size
-  // select the m-th sequence (ascending) of the category; lane w holds sequences [32w, 32w+32)
+  // select the m-th sequence (ascending) of the category; lane w holds sequences [32w, 32w+32).
+  // Partition 0 of sequences b < Ex is not in the order (those are the provisional first
+  // items): excluded from the full level r = 0 and, for single-partition sequences, from
+  // the last-partition categories.
+  const int rem = Ex - 32 * lane;
+  const unsigned exmask = rem >= 32 ? 0xffffffffu : (rem > 0 ? (1u << rem) - 1u : 0u);
   unsigned bits = 0;
   if (32 * lane >= num_seqs) {
     // no sequences in this lane's word (the arrays are written up to num_seqs rounded to 32)
@@ -925,6 +931,7 @@ __device__ __forceinline__ bool find_item(int k, const int *s_off, int ncat, int
     if (full) {
 #pragma unroll
       for (int t = 0; t < 32; ++t) bits |= (int)((wn[t >> 2] >> (8 * (t & 3))) & 0xffu) > r ? 1u << t : 0u;
+      if (r == 0) bits &= ~exmask;
     } else {
       const uint4 *v = reinterpret_cast<const uint4 *>(s_lt + 32 * lane);
       uint32_t wd[16];
@@ -942,7 +949,8 @@ __device__ __forceinline__ bool find_item(int k, const int *s_off, int ncat, int
         const int nf = (int)((wn[t >> 2] >> (8 * (t & 3))) & 0xffu);
         const int qt = (lt + kChunk - 1) / kChunk;
         const int size = nf == 0 ? qt : (T > 0 ? P / kChunk : qt) + kMergeChunks;
-        bits |= (lt > 0 && size == q) ? 1u << t : 0u;
+        const bool excluded = nf == 0 && ((exmask >> t) & 1u);
+        bits |= (lt > 0 && size == q && !excluded) ? 1u << t : 0u;
       }
     }
   }
@@ -1007,15 +1015,23 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int Hkv = a.num_kv_heads;
   const int cap = (int)min((int64_t)a.max_blocks * a.block_size, (int64_t)a.max_context_len);
   const int bpad = (a.num_seqs + 31) & ~31;
+  // Provisional first items: CTA c < Ex * Hkv starts at once on partition 0 of unit c
+  // (sequence c / Hkv, kv head c % Hkv) instead of waiting for the order, whose set-up
+  // (every context length, histograms, the category scan) then runs on the consumer
+  // warps while the first stages are in flight.  The order holds every other item.
+  const int Ex = (int)gridDim.x / Hkv;  // sequences whose partition 0 is taken this way
+  const uint32_t bar_order = base + SL::ord;  // phase 0: the order's tables are written
+  volatile int *const s_ex0 = reinterpret_cast<volatile int *>(base_ptr + SL::ord + 8);
 
-  // ---- set-up: barriers, and the order's histograms from the context lengths.  Every
-  // thread's lengths are loaded first, so their latencies overlap.
-  constexpr int kLensPerThread = (kMaxPersistSeqs + kThreads - 1) / kThreads;
+  // ---- set-up: barriers; the consumer warps load every context length at once
+  constexpr int kLensPerThread = (kMaxPersistSeqs + kConsumers - 1) / kConsumers;
   int lens[kLensPerThread];
+  if (warp < kConsumerWarps) {
 #pragma unroll
-  for (int k = 0; k < kLensPerThread; ++k) {
-    const int bb = tid + k * kThreads;
-    lens[k] = bb < a.num_seqs ? __ldg(a.context_lens + bb) : 0;
+    for (int k = 0; k < kLensPerThread; ++k) {
+      const int bb = tid + k * kConsumers;
+      lens[k] = bb < a.num_seqs ? __ldg(a.context_lens + bb) : 0;
+    }
   }
   if (tid == 0) {
 #pragma unroll
@@ -1023,42 +1039,49 @@ __global__ void __launch_bounds__(kThreads, 2)
       dev::mbar_init(bar_full + 8 * s, 1);
       dev::mbar_init(bar_empty + 8 * s, kConsumerWarps);
     }
+    dev::mbar_init(bar_order, 32);  // every lane of warp 0, after the scan
     *s_flag = 0;
     *s_issued = 0;
+    *s_ex0 = 0;
     dev::fence_mbar_init();
   }
   for (int i = tid; i < 3 * kMaxCategories; i += kThreads) s_hist_nf[i] = 0;  // all three
   __syncthreads();
+
+  if (warp < kConsumerWarps) {
+    // ---- the order's histograms (consumer warps), then its category scan (warp 0)
 #pragma unroll
-  for (int k = 0; k < kLensPerThread; ++k) {
-    const int bb = tid + k * kThreads;
-    if (bb >= bpad) break;
-    int nf = 0, lt = 0;
-    if (bb < a.num_seqs) {
-      int L = lens[k];
-      if (L < 0 || L > cap) {
-        if (blockIdx.x == 0) raise_error(PKV_DEVERR_CONTEXT_LEN);
-        L = L < 0 ? 0 : cap;
-      }
-      if (L > 0) {
-        nf = (L - 1) / P;
-        lt = L - nf * P;
-        const int q = (lt + kChunk - 1) / kChunk;
-        if (nf > 0) {
-          atomicAdd(s_hist_nf + nf, 1);
-          atomicAdd(s_hist_ml + q, 1);
-        } else {
-          atomicAdd(s_hist_lc + q, 1);
+    for (int k = 0; k < kLensPerThread; ++k) {
+      const int bb = tid + k * kConsumers;
+      if (bb >= bpad) break;
+      int nf = 0, lt = 0;
+      if (bb < a.num_seqs) {
+        int L = lens[k];
+        if (L < 0 || L > cap) {
+          if (blockIdx.x == 0) raise_error(PKV_DEVERR_CONTEXT_LEN);
+          L = L < 0 ? 0 : cap;
         }
-      } else if (bb % (int)gridDim.x == (int)blockIdx.x) {  // empty context: zero output
-        uint2 *o = reinterpret_cast<uint2 *>(a.out + (int64_t)bb * a.num_q_heads * D);
-        for (int i = 0; i < a.num_q_heads * D / 4; ++i) o[i] = make_uint2(0u, 0u);
+        if (L > 0) {
+          nf = (L - 1) / P;
+          lt = L - nf * P;
+          const int q = (lt + kChunk - 1) / kChunk;
+          if (nf > 0) {
+            atomicAdd(s_hist_nf + nf, 1);
+            atomicAdd(s_hist_ml + q, 1);
+            if (bb < Ex) atomicAdd(const_cast<int *>(s_ex0), 1);  // its partition 0 is provisional
+          } else if (bb >= Ex) {
+            atomicAdd(s_hist_lc + q, 1);
+          }
+        } else if (bb % (int)gridDim.x == (int)blockIdx.x) {  // empty context: zero output
+          uint2 *o = reinterpret_cast<uint2 *>(a.out + (int64_t)bb * a.num_q_heads * D);
+          for (int i = 0; i < a.num_q_heads * D / 4; ++i) o[i] = make_uint2(0u, 0u);
+        }
       }
+      s_nf[bb] = (uint8_t)nf;
+      s_lt[bb] = (uint16_t)lt;
     }
-    s_nf[bb] = (uint8_t)nf;
-    s_lt[bb] = (uint16_t)lt;
+    consumer_bar();
   }
-  __syncthreads();
   if (warp == 0) {  // T, the item counts of the categories, then their exclusive prefix
     int T = 0;
     {  // single-partition items of at most q chunks, q = lane + 1 and lane + 33
@@ -1084,6 +1107,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       int n = 0;
       if (c < R - 1) {  // full partition r = R-2-c: sequences with nf > r
         for (int x = R - 1 - c; x <= R - 1; ++x) n += s_hist_nf[x];
+        if (c == R - 2) n -= *s_ex0;  // r = 0 of sequences b < Ex: provisional
       } else if (c < ncat) {  // last partitions of size sz
         const int sz = Q + kMergeChunks - (c - (R - 1));
         if (sz <= Q) n = s_hist_lc[sz];
@@ -1113,8 +1137,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       s_off[ncat] = total;
       *s_T = T;
     }
+    dev::mbar_arrive(bar_order);  // releases this lane's writes; phase 0 after all 32
   }
-  __syncthreads();
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------- producer warp
@@ -1122,18 +1146,62 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int rb = a.box_rows;
     const uint32_t box_bytes = (uint32_t)rb * 128u;
     const uint32_t q_bytes = (uint32_t)a.group * D * 2u;
+    // The provisional first item (partition 0 of unit blockIdx.x, for CTAs below Ex * Hkv
+    // whose sequence is not empty), and the first 32 entries of its table row; neither
+    // needs the order.
+    Item it;
+    bool have = false, pre = false;
+    int tb_pre = 0;
+    if ((int)blockIdx.x < Ex * Hkv) {
+      const int b0 = (int)blockIdx.x / Hkv;
+      int L0 = __ldg(a.context_lens + b0);
+      tb_pre = lane < a.max_blocks ? __ldg(a.block_tables + (int64_t)b0 * a.max_blocks + lane) : 0;
+      if (L0 > cap) L0 = cap;  // out-of-range lengths are flagged by the histogram pass
+      if (L0 > 0) {
+        const int nf0 = (L0 - 1) / P;
+        it.b = b0;
+        it.g = (int)blockIdx.x - b0 * Hkv;
+        it.t_begin = 0;
+        it.t_end = nf0 > 0 ? P : L0;
+        it.np = nf0 + 1;
+        have = pre = true;
+      }
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");  // see decode_kernel
     int c = 0;  // chunks issued, over all items
     bool ok = true;
-    Item it;
-    const int T = *s_T;
-    bool have = find_item((int)blockIdx.x, s_off, ncat, R, P, Hkv, T, a.num_seqs, s_lt, s_nf, lane, it);
-    while (have) {
+    int T = 0;
+    bool order = false;  // the order's tables are visible to this warp
+    auto wait_order = [&]() -> bool {
+      if (order) return true;
+      if (!__all_sync(0xffffffffu, dev::mbar_wait(bar_order, 0))) {
+        if (lane == 0) {
+          raise_error(PKV_DEVERR_TIMEOUT);
+          *s_flag = 1;
+        }
+        return false;
+      }
+      T = *s_T;
+      order = true;
+      return true;
+    };
+    if (!have) {  // no provisional item: the first claim
+      if (wait_order()) {
+        int k0 = 0;
+        if (lane == 0) k0 = (int)atomicAdd(a.sched, 1u);
+        k0 = __shfl_sync(0xffffffffu, k0, 0);
+        have = find_item(k0, s_off, ncat, R, P, Hkv, T, a.num_seqs, Ex, s_lt, s_nf, lane, it);
+      } else {
+        ok = false;
+      }
+    }
+    while (have && ok) {
       int k_next = 0;  // lane 0: the item after this one
       const int32_t *trow = a.block_tables + (int64_t)it.b * a.max_blocks;
       const int lb_last = (it.t_end - 1) >> a.log2_bs;
       int win = it.t_begin >> a.log2_bs;
-      int tb = (win + lane <= lb_last) ? __ldg(trow + win + lane) : 0;
+      int tb = pre ? tb_pre : ((win + lane <= lb_last) ? __ldg(trow + win + lane) : 0);
+      pre = false;
       const int n_chunks = (it.t_end - it.t_begin + kChunk - 1) / kChunk;
       for (int i = 0; i < n_chunks; ++i, ++c) {
         const int s = c % STAGES;
@@ -1150,8 +1218,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         // CTA is about to run out of work: CTAs that finish early take the larger items
         // still left (the order is longest first), and the claim's latency hides behind
         // the stages already queued.
-        if (lane == 0 && i == max(n_chunks - 2, 0))
-          k_next = (int)gridDim.x + (int)atomicAdd(a.sched, 1u);
+        if (lane == 0 && i == max(n_chunks - 2, 0)) k_next = (int)atomicAdd(a.sched, 1u);
         const int k0 = it.t_begin + i * kChunk;
         const int nk = min(kChunk, it.t_end - k0);
         const int nbox = (nk + rb - 1) / rb;
@@ -1197,7 +1264,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       if (!ok) break;
       const int k = __shfl_sync(0xffffffffu, k_next, 0);
-      have = find_item(k, s_off, ncat, R, P, Hkv, T, a.num_seqs, s_lt, s_nf, lane, it);
+      if (!wait_order()) {
+        ok = false;
+        break;
+      }
+      have = find_item(k, s_off, ncat, R, P, Hkv, T, a.num_seqs, Ex, s_lt, s_nf, lane, it);
     }
     if (ok) {  // no item follows: a stop marker in the next stage
       const int s = c % STAGES;
