@@ -847,11 +847,13 @@ __global__ void __launch_bounds__(kThreads, 2)
 // the merges up would put long single-partition items last instead, so a multi-partition
 // last partition only counts its merge: size q + kMergeChunks.  (Measured on batches of
 // 64 to 512 sequences: each rule is the faster one where it is used.)  Each CTA derives the same
-// order from the context lengths (histograms in shared memory), takes item blockIdx.x
-// first and then items gridDim.x + (a global counter), each claimed when the current
-// item is two chunks from its last issue -- so the largest items left go to the CTAs
-// about to run dry (list scheduling).  No CTA waits for another; the last CTA to
-// finish resets the counter for the next call.
+// order from the context lengths (histograms in shared memory, on its consumer warps).
+// So that no CTA's first copy waits for that, CTA c < Ex * Hkv (Ex = gridDim.x / Hkv)
+// first streams a provisional item, partition 0 of unit c, which the order leaves out;
+// after it, and for the other CTAs from the start, items come from a global counter,
+// each claimed when the current item is two chunks from its last issue -- so the
+// largest items left go to the CTAs about to run dry (list scheduling).  No CTA waits
+// for another; the last CTA to finish resets the counter for the next call.
 
 constexpr int kMaxPersistSeqs = 1024;  // sequences per batch (a warp scans 32 x 32 of them)
 constexpr int kMaxCategories = 64;     // full-partition levels + last-partition sizes
