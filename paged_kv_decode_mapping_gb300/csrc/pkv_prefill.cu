@@ -392,6 +392,55 @@ __device__ __forceinline__ float row_regs_exp(const uint32_t (&x)[NCH * 32], int
   return ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
 }
 
+// Pass 2 from registers, without the stores: the rounded weights stay packed in `pk`
+// (column pair e of chunk ch at pk[16 ch + e]) until the P buffer is free; returns their
+// sum, as row_regs_exp.
+template <int NCH, bool kSum = true>
+__device__ __forceinline__ float row_regs_exp_pk(const uint32_t (&x)[NCH * 32], int ch0, int lim,
+                                                 bool whole, float scale_log2, float m_ref,
+                                                 uint32_t (&pk)[NCH * 16]) {
+  float ls[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) ls[u] = 0.f;
+#pragma unroll
+  for (int ch = 0; ch < NCH; ++ch) {
+    const int lc = whole ? 32 : lim - (ch0 + ch) * 32;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      float a0, a1;
+      fma_f32x2(__uint_as_float(x[ch * 32 + 2 * e]), __uint_as_float(x[ch * 32 + 2 * e + 1]),
+                scale_log2, -m_ref, a0, a1);
+      float p0 = dev::ex2(a0), p1 = dev::ex2(a1);
+      if (!whole) {
+        p0 = 2 * e <= lc ? p0 : 0.f;
+        p1 = 2 * e + 1 <= lc ? p1 : 0.f;
+      }
+      pk[ch * 16 + e] = dev::pack_bf16x2(p0, p1);
+      if constexpr (kSum) ls[e & 7] = add_bf16x2(pk[ch * 16 + e], ls[e & 7]);
+    }
+  }
+  return ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+}
+
+// Stores the packed weights of row_regs_exp_pk into row r of the P buffer (K-major,
+// 128-byte swizzle, two 64-column sub-tiles `sub` bytes apart).
+template <int NCH>
+__device__ __forceinline__ void row_store_p(const uint32_t (&pk)[NCH * 16], int ch0, uint8_t *bp,
+                                            uint32_t prow, uint32_t sub, int r) {
+#pragma unroll
+  for (int ch = 0; ch < NCH; ++ch) {
+    const int cha = ch0 + ch;
+    const uint32_t dst = prow + (cha >> 1) * sub;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c16 = (cha & 1) * 4 + u;
+      *reinterpret_cast<uint4 *>(bp + dst + ((c16 ^ (r & 7)) << 4)) =
+          make_uint4(pk[ch * 16 + 4 * u], pk[ch * 16 + 4 * u + 1], pk[ch * 16 + 4 * u + 2],
+                     pk[ch * 16 + 4 * u + 3]);
+    }
+  }
+}
+
 // Whether the softmax reads a row's block from TMEM once into registers (1) or in each
 // of the two passes (0), by head_dim: once at 128 (measured 7% faster), twice at 64,
 // where the extra live registers cost more than the second read.
@@ -403,6 +452,24 @@ __device__ __forceinline__ float row_regs_exp(const uint32_t (&x)[NCH * 32], int
 #endif
 template <int D>
 __host__ __device__ constexpr bool row_once() { return D == 128 ? PKV_PREFILL_ROW_ONCE128 != 0 : PKV_PREFILL_ROW_ONCE64 != 0; }
+
+// Two-tile kernel, rows read once: the softmax releases S_t(j) (s_free) as soon as it
+// holds the block in registers, so S_t(j+1) runs on the tensor core during the block's
+// exponentials instead of after them, and it waits for PV_t(j-1) only once its weights
+// are computed, right before it overwrites the P buffer (1); or S_t(j+1) is issued once
+// P_t(j) is complete and the wait comes before the exponentials (0).
+#ifndef PKV_PREFILL_EARLY_S
+#define PKV_PREFILL_EARLY_S 1
+#endif
+// Two-tile kernel at head_dim 128: the softmax writes P into TMEM over the upper half of
+// its S buffer and P.V reads it from there (A operand in TMEM), so P never passes
+// through shared memory, whose bandwidth the operand reads of both MMAs, the TMA writes
+// and the P stores otherwise share; the freed buffers give V a second stage.  The
+// tensor core then takes PV_t(j) before S_t(j+1) overwrites the buffer (the MMAs of
+// one thread run in issue order).  Takes precedence over PKV_PREFILL_EARLY_S.
+#ifndef PKV_PREFILL_P_TMEM
+#define PKV_PREFILL_P_TMEM 1
+#endif
 
 // ---------------------------------------------------------------------------
 // Tensor-core issue.  A tcgen05.mma returns to the issuing thread only once the tensor
@@ -455,6 +522,31 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint64_t p, uint64_t v
     umma4(d_tmem, desc_add(p, o), desc_add(p, o + 32), desc_add(p, o + 64), desc_add(p, o + 96),
           desc_add(v, vo), desc_add(v, vo + 2048), desc_add(v, vo + 4096), desc_add(v, vo + 6144),
           idesc, g4 > 0 ? 1u : acc_first);
+  }
+}
+
+// The same with P read from TMEM (the A operand in TMEM: row i in lane i, column c
+// holding keys 2c and 2c+1): p_tmem is P's first column; K slice kk is 8 columns on.
+__device__ __forceinline__ void umma4_ts(uint32_t d_tmem, uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint64_t b0, uint64_t b1, uint64_t b2,
+                                         uint64_t b3, uint32_t idesc, uint32_t acc_first) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %10, 0;\n\tsetp.eq.u32 q, 1, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %5, %9, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %6, %9, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %7, %9, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %8, %9, q;\n\t}" ::"r"(d_tmem),
+      "r"(a0), "r"(a1), "r"(a2), "r"(a3), "l"(b0), "l"(b1), "l"(b2), "l"(b3), "r"(idesc),
+      "r"(acc_first)
+      : "memory");
+}
+__device__ __forceinline__ void issue_pv_ts(uint32_t d_tmem, uint32_t p_tmem, uint64_t v,
+                                            uint32_t idesc, uint32_t acc_first) {
+#pragma unroll
+  for (int g4 = 0; g4 < kTcKeys / 64; ++g4) {
+    const uint32_t a = p_tmem + 32u * g4, vo = g4 * 4 * 2048u;
+    umma4_ts(d_tmem, a, a + 8, a + 16, a + 24, desc_add(v, vo), desc_add(v, vo + 2048),
+             desc_add(v, vo + 4096), desc_add(v, vo + 6144), idesc, g4 > 0 ? 1u : acc_first);
   }
 }
 
@@ -765,8 +857,10 @@ __host__ __device__ constexpr int tc2_threads() { return 32 * (8 * H + 2); }
 
 template <int D, int H>
 struct Tc2Smem {
+  // P in TMEM (no P buffers in shared memory)
+  static constexpr bool kPT = D == 128 && H == 1 && row_once<D>() && PKV_PREFILL_P_TMEM != 0;
   static constexpr int KSK = D == 64 ? 3 : 2;        // stages of the K ring
-  static constexpr int KSV = D == 64 ? 3 : 1;        // stages of the V ring
+  static constexpr int KSV = D == 64 ? 3 : (kPT ? 2 : 1);  // stages of the V ring
   static constexpr uint32_t kSub = kTcKeys * 128;    // 128 rows x 128 B (64 dims)
   static constexpr uint32_t kTile = kSub * (D / 64); // one K or V block / one Q tile
   static constexpr uint32_t k = 0;
@@ -775,15 +869,16 @@ struct Tc2Smem {
   static constexpr uint32_t p = q + 2 * kTile;       // two P buffers [2][128 rows][128 B]
   static constexpr uint32_t kP = 2 * kSub;
   // H = 2: the halves' row values, [2 buffers][2 tiles][2 halves][128 rows] fp32
-  static constexpr uint32_t xchg = p + 2 * kP;
+  static constexpr uint32_t xchg = p + (kPT ? 0 : 2 * kP);
   // kOnes: a [128 keys][64] bf16 tile of ones, read by P.V as 16 extra B columns, so that
   // the tensor core also forms each row's sum of the bf16 weights (in O's extra columns)
   static constexpr bool kOnes = D == 64 && H == 1 && PKV_PREFILL_SUM_MMA64 != 0;
   static constexpr uint32_t ones = (xchg + (H == 2 ? 2 * 2 * 2 * kTcRows * 4 : 0) + 1023u) & ~1023u;
   static constexpr uint32_t bars = ones + (kOnes ? kSub : 0);
-  // the rings, s_full/p_full/pv_done per tile, q_ready, mma_done, and with H = 2 one
-  // barrier per (tile, lane quadrant) where the two halves of its rows meet
-  static constexpr int kBars = 2 * KSK + 2 * KSV + 8 + (H == 2 ? 8 : 0);
+  // the rings, s_full/p_full/pv_done per tile, q_ready, mma_done, with H = 2 one
+  // barrier per (tile, lane quadrant) where the two halves of its rows meet, then
+  // s_free per tile
+  static constexpr int kBars = 2 * KSK + 2 * KSV + 8 + (H == 2 ? 8 : 0) + 2;
   static constexpr uint32_t tslot = bars + kBars * 8;
   static constexpr uint32_t flag = tslot + 8;
   static constexpr uint32_t total = flag + 8;
@@ -801,6 +896,8 @@ __global__ void __launch_bounds__(tc2_threads<H>(), 1)
   constexpr int NCH = kTcKeys / 32 / H;    // 32-column chunks of a block per thread
   constexpr bool kOnes = SL::kOnes;        // row sums from the tensor core
   constexpr int kON = D + (kOnes ? 16 : 0);  // O columns per tile (then the row sums)
+  constexpr bool kPT = SL::kPT;           // P in TMEM, over the upper half of S_t
+  constexpr bool kEarlyS = !kPT && PKV_PREFILL_EARLY_S != 0 && row_once<D>();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = dev::smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -817,6 +914,7 @@ __global__ void __launch_bounds__(tc2_threads<H>(), 1)
   const uint32_t q_ready = bars + 8u * (R4 + 6);
   const uint32_t mma_done = bars + 8u * (R4 + 7);
   auto pair_bar = [&](int t, int wq) { return bars + 8u * (R4 + 8 + 4 * t + wq); };
+  auto s_free = [&](int t) { return bars + 8u * (SL::kBars - 2 + t); };
   volatile uint32_t *const s_tmem = reinterpret_cast<volatile uint32_t *>(bp + SL::tslot);
   volatile int *const s_flag = reinterpret_cast<volatile int *>(bp + SL::flag);
 
@@ -859,8 +957,9 @@ __global__ void __launch_bounds__(tc2_threads<H>(), 1)
   if (tid == 0) {
     for (int i = 0; i < SL::kBars; ++i) {
       const uint32_t bar = bars + 8u * i;
-      const bool per_warp = bar == p_full(0) || bar == p_full(1);
-      const bool pair = i >= R4 + 8;  // every thread of the two halves' warps arrives
+      const bool per_warp = bar == p_full(0) || bar == p_full(1) || bar == s_free(0) ||
+                            bar == s_free(1);
+      const bool pair = i >= R4 + 8 && i < SL::kBars - 2;  // every thread of the halves' warps
       dev::mbar_init(bar, pair ? 64u
                                : per_warp ? (uint32_t)kTileWarps
                                           : (bar == q_ready ? (uint32_t)kSoftWarps : 1u));
@@ -956,13 +1055,22 @@ __global__ void __launch_bounds__(tc2_threads<H>(), 1)
         if (nblk_of(1) > 0) issue_s(1, 0);
       }
       for (int j = 0; ok && j < nblk; ++j) {
+        if constexpr (kEarlyS) {  // S_t(j+1) once the softmax holds S_t(j) in registers
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (j + 1 >= nblk_of(t)) continue;
+            if (!(ok = fail(dev::mbar_wait(s_free(t), j & 1)))) break;
+            dev::tc_fence_after();
+            if (!(ok = need_k(j + 1))) break;
+            issue_s(t, j + 1);
+          }
+        }
         bool v_seen = false;
         for (int t = 0; t < 2 && ok; ++t) {
           if (j >= nblk_of(t)) continue;
           if (!(ok = fail(dev::mbar_wait(p_full(t), j & 1)))) break;
           dev::tc_fence_after();
           // S_t(j+1) first: the softmax can start on it while the tensor core runs PV_t(j)
-          if (j + 1 < nblk_of(t)) {
+          if (!kEarlyS && !kPT && j + 1 < nblk_of(t)) {
             if (!(ok = need_k(j + 1))) break;
             issue_s(t, j + 1);
           }
@@ -971,11 +1079,24 @@ __global__ void __launch_bounds__(tc2_threads<H>(), 1)
             v_seen = true;
             dev::tc_fence_after();
           }
-          issue_pv(tmem + 256u + (uint32_t)(kON * t), desc_add(dp0, t * SL::kP), dv(j % KSV),
-                   SL::kSub, id_o, j > 0 ? 1u : 0u);
-          dev::umma_commit(pv_done(t));
+          if constexpr (kPT) {
+            issue_pv_ts(tmem + 256u + (uint32_t)(kON * t), tmem + 128u * t + 64u, dv(j % KSV), id_o,
+                        j > 0 ? 1u : 0u);
+            dev::umma_commit(pv_done(t));
+            // V_j is free once the last tile that reads it has its P.V
+            if (t == 1 || j >= nblk_of(1)) dev::umma_commit(v_empty(j % KSV));
+            // S_t(j+1) over S_t(j) and P_t(j), after the P.V that reads P_t(j)
+            if (j + 1 < nblk_of(t)) {
+              if (!(ok = need_k(j + 1))) break;
+              issue_s(t, j + 1);
+            }
+          } else {
+            issue_pv(tmem + 256u + (uint32_t)(kON * t), desc_add(dp0, t * SL::kP), dv(j % KSV),
+                     SL::kSub, id_o, j > 0 ? 1u : 0u);
+            dev::umma_commit(pv_done(t));
+          }
         }
-        if (ok) dev::umma_commit(v_empty(j % KSV));
+        if (ok && !kPT) dev::umma_commit(v_empty(j % KSV));
       }
       dev::umma_commit(mma_done);
     }
@@ -1043,46 +1164,85 @@ __global__ void __launch_bounds__(tc2_threads<H>(), 1)
       float hmax;
       if constexpr (row_once<D>()) {
         row_block_load<NCH>(sb, hc * NCH, xrow);
+        if constexpr (kEarlyS) {  // S_t(j) is in registers: the tensor core may overwrite it
+          dev::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) dev::mbar_arrive(s_free(t));
+        }
         hmax = row_regs_max<NCH>(xrow, hc * NCH, lim, whole, pos_scale, a.scale_log2);
       } else {
         hmax = row_block_max<NCH>(sb, hc * NCH, lim, whole, pos_scale, a.scale_log2);
       }
       const float bmax = fmaxf(hmax, other_half(hmax, j, ok));
       if (!ok) break;
-      // O_t is stable and the P buffer free once PV_t(j-1) has completed
-      if (j > 0 && !(ok = __all_sync(0xffffffffu, dev::mbar_wait(pv_done(t), (j - 1) & 1)))) break;
+      // Lazy rescaling: the reference max moves only when the block raises it by more
+      // than kTcRescale; then O_t (and its row-sum column) and the row sum scale by f.
+      float f = 1.f;
+      bool resc = false;
       if (j > 0) {
         const bool need = bmax > m_ref + kTcRescale;
-        if (__any_sync(0xffffffffu, need)) {  // each half rescales its D/H columns of O
+        resc = __any_sync(0xffffffffu, need);
+        if (resc) {
           const float m_new = fmaxf(m_ref, bmax);
-          const float f = need ? dev::ex2(m_ref - m_new) : 1.f;
-#pragma unroll 1
-          for (int ch = hc * (D / 32 / H); ch < (hc + 1) * (D / 32 / H); ++ch) {
-            uint32_t o[32];
-            dev::tmem_ld32(ob + ch * 32, o);
-            dev::tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-            dev::tmem_st32(ob + ch * 32, o);
-          }
-          if constexpr (kOnes) {  // the row sum in O's column D
-            const uint32_t sm = tmem_ld1(ob + D);
-            dev::tmem_wait_ld();
-            tmem_st1(ob + D, __float_as_uint(__uint_as_float(sm) * f));
-          }
-          dev::tmem_wait_st();
-          lsum *= f;
+          f = need ? dev::ex2(m_ref - m_new) : 1.f;
           if (need) m_ref = m_new;
         }
       } else {
         m_ref = bmax;
       }
-      if constexpr (row_once<D>())
-        lsum += row_regs_exp<NCH>(xrow, hc * NCH, bp, SL::p + t * SL::kP + r * 128, SL::kSub, r,
-                                  lim, whole, a.scale_log2, m_ref);
-      else
-        lsum += row_block_exp<NCH, !kOnes>(sb, hc * NCH, bp, SL::p + t * SL::kP + r * 128, SL::kSub,
-                                           r, lim, whole, a.scale_log2, m_ref);
+      auto rescale_o = [&]() {  // each half rescales its D/H columns of O
+#pragma unroll 1
+        for (int ch = hc * (D / 32 / H); ch < (hc + 1) * (D / 32 / H); ++ch) {
+          uint32_t o[32];
+          dev::tmem_ld32(ob + ch * 32, o);
+          dev::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+          dev::tmem_st32(ob + ch * 32, o);
+        }
+        if constexpr (kOnes) {  // the row sum in O's column D
+          const uint32_t sm = tmem_ld1(ob + D);
+          dev::tmem_wait_ld();
+          tmem_st1(ob + D, __float_as_uint(__uint_as_float(sm) * f));
+        }
+        dev::tmem_wait_st();
+        lsum *= f;
+      };
+      if constexpr (kPT) {
+        // P_t(j) into TMEM over the upper half of S_t.  PV_t(j-1) was issued before S_t(j)
+        // by the same thread, and s_full tracks every MMA issued before its commit, so
+        // O_t is stable here.
+        uint32_t pk[NCH * 16];
+        const float ls = row_regs_exp_pk<NCH>(xrow, 0, lim, whole, a.scale_log2, m_ref, pk);
+        if (resc) rescale_o();
+        lsum += ls;
+        dev::tmem_st32(sb + 64u, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        dev::tmem_st32(sb + 96u, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        dev::tmem_wait_st();
+      } else if constexpr (kEarlyS) {
+        // the block's weights first, kept in registers; then, once PV_t(j-1) has
+        // completed (O_t stable, P buffer free), the rescale and the P stores
+        uint32_t pk[NCH * 16];
+        const float ls =
+            row_regs_exp_pk<NCH, !kOnes>(xrow, hc * NCH, lim, whole, a.scale_log2, m_ref, pk);
+        if (j > 0) {
+          if (!(ok = __all_sync(0xffffffffu, dev::mbar_wait(pv_done(t), (j - 1) & 1)))) break;
+          dev::tc_fence_after();
+          if (resc) rescale_o();
+        }
+        lsum += ls;
+        row_store_p<NCH>(pk, hc * NCH, bp, SL::p + t * SL::kP + r * 128, SL::kSub, r);
+      } else {
+        // O_t is stable and the P buffer free once PV_t(j-1) has completed
+        if (j > 0 && !(ok = __all_sync(0xffffffffu, dev::mbar_wait(pv_done(t), (j - 1) & 1)))) break;
+        if (resc) rescale_o();
+        if constexpr (row_once<D>())
+          lsum += row_regs_exp<NCH>(xrow, hc * NCH, bp, SL::p + t * SL::kP + r * 128, SL::kSub, r,
+                                    lim, whole, a.scale_log2, m_ref);
+        else
+          lsum += row_block_exp<NCH, !kOnes>(sb, hc * NCH, bp, SL::p + t * SL::kP + r * 128,
+                                             SL::kSub, r, lim, whole, a.scale_log2, m_ref);
+      }
       const int nk = min(kTcKeys, t_end - k0);  // keys the CTA staged in this block
       if (nk < kTcKeys) {  // the CTA's last block: V rows past its keys are stale or unowned
         const int s = j % KSV;
