@@ -108,12 +108,16 @@ __device__ __forceinline__ void tc_load_block(const CUtensorMap *tm, uint32_t ds
     win = k0 >> a.log2_bs;
     tb = (win + lane <= lb_last) ? __ldg(trow + win + lane) : 0;
   }
-  const int key = k0 + lane * rb;
+  // one box per lane: box i = lane / (D / 64), 64-dim half lane % (D / 64), so that every
+  // box of the block leaves from one instruction (block_size >= 8: nbox * D / 64 <= 32)
+  constexpr int kH = D / 64;
+  const int bi = lane / kH, hh = lane % kH;
+  const int key = k0 + bi * rb;
   const int src = min(max((key >> a.log2_bs) - win, 0), 31);
   const int64_t phys_raw = __shfl_sync(0xffffffffu, tb, src);
-  if (lane == 0) dev::mbar_arrive_expect_tx(bar, (uint32_t)nbox * rb * 128u * (D / 64));
+  if (lane == 0) dev::mbar_arrive_expect_tx(bar, (uint32_t)nbox * rb * 128u * kH);
   __syncwarp();
-  if (lane < nbox) {
+  if (bi < nbox) {
     int64_t phys = phys_raw;
     if (phys < 0 || phys >= a.num_blocks) {
       raise_error(PKV_DEVERR_BLOCK_ID);
@@ -121,17 +125,15 @@ __device__ __forceinline__ void tc_load_block(const CUtensorMap *tm, uint32_t ds
     }
     const int off = key & (a.block_size - 1);
     const int32_t row = (int32_t)((phys * a.num_kv_heads + g) * a.block_size + off);
-    const uint32_t d = dst + (uint32_t)(lane * rb) * 128u;
+    const uint32_t d = dst + (uint32_t)(bi * rb) * 128u;
     if constexpr (D == 64) {
       dev::tma_load_2d(d, tm, 0, row, bar, policy);
     } else {
-#pragma unroll
-      for (int hh = 0; hh < D / 64; ++hh)
-        asm volatile(
-            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-            ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(d + hh * TcSmem<D>::kSub),
-            "l"(reinterpret_cast<uint64_t>(tm)), "r"(0), "r"(hh), "r"(row), "r"(bar), "l"(policy)
-            : "memory");
+      asm volatile(
+          "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+          ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(d + hh * TcSmem<D>::kSub),
+          "l"(reinterpret_cast<uint64_t>(tm)), "r"(0), "r"(hh), "r"(row), "r"(bar), "l"(policy)
+          : "memory");
     }
   }
   __syncwarp();
@@ -469,6 +471,13 @@ __host__ __device__ constexpr bool row_once() { return D == 128 ? PKV_PREFILL_RO
 // one thread run in issue order).  Takes precedence over PKV_PREFILL_EARLY_S.
 #ifndef PKV_PREFILL_P_TMEM
 #define PKV_PREFILL_P_TMEM 1
+#endif
+// K and V ring stages of the two-tile kernel at head_dim 128 with P in TMEM.
+#ifndef PKV_PREFILL_KSK128
+#define PKV_PREFILL_KSK128 2
+#endif
+#ifndef PKV_PREFILL_KSV128
+#define PKV_PREFILL_KSV128 2
 #endif
 
 // ---------------------------------------------------------------------------
@@ -840,27 +849,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // prefill_tc2_kernel: two query tiles per CTA in ping-pong.
 //
 // A CTA owns 256 query rows as two 128-row tiles of the same (sequence, kv head):
-// softmax warpgroup t (warps 4t .. 4t+3) owns tile t.  The tensor-core thread issues
-// S_0(j+1), PV_0(j), S_1(j+1), PV_1(j), so while one warpgroup works on its S the tensor
-// core works on the other tile, and every K/V block staged feeds 256 rows.  Each tile
-// has one S buffer and one P buffer: S_t(j+1) is issued once the softmax has released
-// S_t(j) (p_full), ahead of PV_t(j), so the softmax can take the next row max while
-// PV_t(j) runs; it waits for PV_t(j) (pv_done) before it rescales O_t or overwrites P_t.
+// softmax warpgroup t (warps 4t .. 4t+3) owns tile t, and while one warpgroup works on
+// its scores the tensor core works on the other tile; every K/V block staged feeds 256
+// rows.  Each tile has one S buffer in TMEM.
+//  * head_dim 64: one P buffer per tile in shared memory.  The tensor-core thread issues
+//    S_0(j+1), PV_0(j), S_1(j+1), PV_1(j): S_t(j+1) goes out once P_t(j) is complete
+//    (p_full), ahead of PV_t(j), and the softmax waits for PV_t(j) (pv_done) before it
+//    rescales O_t or overwrites P_t.  K and V rings of 3.
+//  * head_dim 128: P_t(j) is written into TMEM over the upper half of S_t(j), and the
+//    tensor-core thread issues PV_0(j), S_0(j+1), PV_1(j), S_1(j+1): the MMAs of one
+//    thread run in issue order, so S_t(j+1) overwrites the buffer only after PV_t(j) has
+//    read it, and s_full(t) (which tracks every MMA issued before it) tells the softmax
+//    that O_t is stable.  K and V rings of 2, each filled by its own producer warp.
 // Row arithmetic (positions, masking, lazy rescale, bf16 row sums) is the one-tile
-// kernel's.  head_dim 64: K and V rings of 3; head_dim 128: K ring of 2, V ring of 1.
-// H softmax threads per query row: with H = 2, two warps share each 32-row lane quadrant,
-// one taking the first 64 columns of every key block, the other the last 64; their row
-// maxima and row sums are combined through shared memory.  Warps 0 .. 8H-1 are the two
-// tiles' softmax warps (tile t: warps 8H/2 t .. ), then the producer and MMA warps.
-template <int H>
-__host__ __device__ constexpr int tc2_threads() { return 32 * (8 * H + 2); }
+// kernel's.  H softmax threads per query row: with H = 2, two warps share each 32-row
+// lane quadrant, one taking the first 64 columns of every key block, the other the last
+// 64; their row maxima and row sums are combined through shared memory.  Warps 0 .. 8H-1
+// are the two tiles' softmax warps (tile t: warps 8H/2 t .. ), then the producer, the
+// MMA warp and (head_dim 128) the V producer.
+// Producer warps of the two-tile kernel: at head_dim 128 one for the K ring and one for
+// the V ring (a block's sixteen 2 KB boxes take a warp ~1800 cycles to issue at
+// block_size 16, as long as the block's tensor-core work: measured +1.3%); at head_dim
+// 64 one for both (measured 1% faster than two).
+#ifndef PKV_PREFILL_TWO_PRODUCERS128
+#define PKV_PREFILL_TWO_PRODUCERS128 1
+#endif
+template <int D>
+__host__ __device__ constexpr int tc2_producers() { return D == 128 && PKV_PREFILL_TWO_PRODUCERS128 ? 2 : 1; }
+template <int D, int H>
+__host__ __device__ constexpr int tc2_threads() { return 32 * (8 * H + 1 + tc2_producers<D>()); }
 
 template <int D, int H>
 struct Tc2Smem {
   // P in TMEM (no P buffers in shared memory)
   static constexpr bool kPT = D == 128 && H == 1 && row_once<D>() && PKV_PREFILL_P_TMEM != 0;
-  static constexpr int KSK = D == 64 ? 3 : 2;        // stages of the K ring
-  static constexpr int KSV = D == 64 ? 3 : (kPT ? 2 : 1);  // stages of the V ring
+  static constexpr int KSK = D == 64 ? 3 : (kPT ? PKV_PREFILL_KSK128 : 2);  // stages of the K ring
+  static constexpr int KSV = D == 64 ? 3 : (kPT ? PKV_PREFILL_KSV128 : 1);  // stages of the V ring
   static constexpr uint32_t kSub = kTcKeys * 128;    // 128 rows x 128 B (64 dims)
   static constexpr uint32_t kTile = kSub * (D / 64); // one K or V block / one Q tile
   static constexpr uint32_t k = 0;
@@ -885,14 +909,14 @@ struct Tc2Smem {
 };
 
 template <int D, int H>
-__global__ void __launch_bounds__(tc2_threads<H>(), 1)
+__global__ void __launch_bounds__(tc2_threads<D, H>(), 1)
     prefill_tc2_kernel(const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, const PrefillArgs a) {
   using SL = Tc2Smem<D, H>;
   constexpr int KSK = SL::KSK, KSV = SL::KSV;
   constexpr int kSoftWarps = 8 * H;        // softmax warps of both tiles
   constexpr int kTileWarps = 4 * H;        // softmax warps of one tile
-  constexpr int kProducer = kSoftWarps, kMma = kSoftWarps + 1;
+  constexpr int kProducer = kSoftWarps, kMma = kSoftWarps + 1, kProducerV = kSoftWarps + 2;
   constexpr int NCH = kTcKeys / 32 / H;    // 32-column chunks of a block per thread
   constexpr bool kOnes = SL::kOnes;        // row sums from the tensor core
   constexpr int kON = D + (kOnes ? 16 : 0);  // O columns per tile (then the row sums)
@@ -968,7 +992,7 @@ __global__ void __launch_bounds__(tc2_threads<H>(), 1)
     dev::fence_mbar_init();
   }
   if constexpr (kOnes) {  // bf16 1.0 everywhere; read by the tensor cores (async proxy)
-    for (int i = tid; i < (int)(SL::kSub / 16); i += tc2_threads<H>())
+    for (int i = tid; i < (int)(SL::kSub / 16); i += tc2_threads<D, H>())
       *reinterpret_cast<uint4 *>(bp + SL::ones + i * 16) =
           make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
     dev::fence_proxy_async_smem();
@@ -988,8 +1012,9 @@ __global__ void __launch_bounds__(tc2_threads<H>(), 1)
   };
   int k_issued = 0, v_issued = 0;
 
-  if (warp == kProducer) {
-    // ------------------------------------------------------------- producer warp
+  if (warp == kProducer || (tc2_producers<D>() == 2 && warp == kProducerV)) {
+    // ---------------------------------------------------------- producer warp(s)
+    const bool do_k = warp == kProducer, do_v = tc2_producers<D>() == 1 || warp == kProducerV;
     const uint64_t policy = dev::policy_evict_last();
     const int32_t *trow = a.block_tables + (int64_t)b * a.max_blocks;
     const int lb_last = (t_end - 1) >> a.log2_bs;
@@ -997,7 +1022,7 @@ __global__ void __launch_bounds__(tc2_threads<H>(), 1)
     int ktb = (lane <= lb_last) ? __ldg(trow + lane) : 0;
     int vtb = ktb;
     for (int j = 0; j <= nblk; ++j) {  // K runs one block ahead of V
-      if (j < nblk) {
+      if (do_k && j < nblk) {
         const int s = j % KSK;
         if (j >= KSK && !__all_sync(0xffffffffu, dev::mbar_wait(k_empty(s), ((j / KSK) - 1) & 1))) {
           if (lane == 0) fail(false);
@@ -1008,7 +1033,7 @@ __global__ void __launch_bounds__(tc2_threads<H>(), 1)
                          policy);
         k_issued = j + 1;
       }
-      if (j >= 1) {
+      if (do_v && j >= 1) {
         const int jv = j - 1, s = jv % KSV;
         if (jv >= KSV && !__all_sync(0xffffffffu, dev::mbar_wait(v_empty(s), ((jv / KSV) - 1) & 1))) {
           if (lane == 0) fail(false);
@@ -1295,7 +1320,7 @@ __global__ void __launch_bounds__(tc2_threads<H>(), 1)
   }
 
   if (tid == 0) (void)dev::mbar_wait(mma_done, 0);
-  if (warp == kProducer && lane == 0 && *s_flag) {
+  if ((warp == kProducer || (tc2_producers<D>() == 2 && warp == kProducerV)) && lane == 0 && *s_flag) {
     for (int s = 0; s < KSK; ++s) {
       const int kl = s + ((k_issued - 1 - s) / KSK) * KSK;
       if (kl >= 0 && kl < k_issued) (void)dev::mbar_wait(k_full(s), (kl / KSK) & 1);
@@ -1415,9 +1440,9 @@ PKV_API int paged_prefill_attention(pkv_bf16 *out, const pkv_bf16 *q, const pkv_
   dim3 grid((unsigned)tiles, (unsigned)cache->num_kv_heads, (unsigned)num_seqs);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (two && D == 64)
-    prefill_tc2_kernel<64, tc2_halves(64)><<<grid, tc2_threads<tc2_halves(64)>(), tc2_smem(64), s>>>(tmk, tmv, a);
+    prefill_tc2_kernel<64, tc2_halves(64)><<<grid, tc2_threads<64, tc2_halves(64)>(), tc2_smem(64), s>>>(tmk, tmv, a);
   else if (two)
-    prefill_tc2_kernel<128, tc2_halves(128)><<<grid, tc2_threads<tc2_halves(128)>(), tc2_smem(128), s>>>(tmk, tmv, a);
+    prefill_tc2_kernel<128, tc2_halves(128)><<<grid, tc2_threads<128, tc2_halves(128)>(), tc2_smem(128), s>>>(tmk, tmv, a);
   else if (D == 64)
     prefill_tc_kernel<64><<<grid, kTcThreads, tc_smem(64), s>>>(tmk, tmv, a);
   else
