@@ -853,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 // after it, and for the other CTAs from the start, items come from a global counter,
 // each claimed when the current item is two chunks from its last issue -- so the
 // largest items left go to the CTAs about to run dry (list scheduling).  No CTA waits
-// for another; the last CTA to finish resets the counter for the next call.
+// for another; the last CTA to stop claiming resets the counter for the next call.
 
 constexpr int kMaxPersistSeqs = 1024;  // sequences per batch (a warp scans 32 x 32 of them)
 constexpr int kMaxCategories = 64;     // full-partition levels + last-partition sizes
@@ -1272,6 +1272,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       have = find_item(k, s_off, ncat, R, P, Hkv, T, a.num_seqs, Ex, s_lt, s_nf, lane, it);
     }
+    // This CTA has made its last claim (or given up): count it done.  The CTA that
+    // completes the count has seen every CTA of this call stop claiming, so it resets
+    // both words for the next call; the atomic's round trip overlaps the last stages.
+    unsigned done_before = 0u;
+    if (lane == 0) done_before = atomicAdd(a.sched + 1, 1u);
     if (ok) {  // no item follows: a stop marker in the next stage
       const int s = c % STAGES;
       if (c >= STAGES &&
@@ -1286,6 +1291,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
     if (lane == 0) *s_issued = c;
+    if (lane == 0 && done_before == gridDim.x - 1) {
+      a.sched[0] = 0u;
+      a.sched[1] = 0u;
+    }
   } else {
     // ----------------------------------------------------------- consumer warps
     WarpAcc<D> acc;
@@ -1341,14 +1350,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int s = 0; s < STAGES; ++s) {
       const int c_last = s + ((issued - 1 - s) / STAGES) * STAGES;  // last chunk on stage s
       if (c_last >= 0 && c_last < issued) (void)dev::mbar_wait(bar_full + 8 * s, (c_last / STAGES) & 1);
-    }
-  }
-  // ---- the last CTA to finish resets the item counter for the next call
-  if (tid == 0) {
-    __threadfence();
-    if (atomicAdd(a.sched + 1, 1u) == gridDim.x - 1) {
-      a.sched[0] = 0u;
-      a.sched[1] = 0u;
     }
   }
 }
