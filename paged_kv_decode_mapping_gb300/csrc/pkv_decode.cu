@@ -555,7 +555,7 @@ __device__ __forceinline__ void finish_partition(const DecodeArgs &a, const Merg
 }
 
 template <int D, int STAGES, bool kFma>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, split_occupancy(D))
     decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const DecodeArgs a) {
   constexpr int kTileBytes = kChunk * D * 2;  // K (or V) bytes of one stage
@@ -986,7 +986,7 @@ __device__ __forceinline__ bool find_item(int k, const int *s_off, int ncat, int
 }
 
 template <int D, int STAGES>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, split_occupancy(D))
     decode_persistent_kernel(const __grid_constant__ CUtensorMap tmk,
                              const __grid_constant__ CUtensorMap tmv, const DecodeArgs a) {
   using SL = PersistSmem<D, STAGES>;

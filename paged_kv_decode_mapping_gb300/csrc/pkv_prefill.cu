@@ -72,7 +72,15 @@ struct PrefillArgs {
 // separate rings so that K runs a block ahead of V.
 constexpr int kTcRows = 128;     // query rows per CTA
 constexpr int kTcKeys = 128;     // keys per block
-constexpr int kTcThreads = 192;  // softmax warps 0-3, producer warp 4, MMA warp 5
+// One-tile kernel: softmax warps 0-3, producer warp 4 (the K ring, and the V ring unless
+// warp 6 fills it), MMA warp 5.  One warp takes ~110 cycles per TMA box, so at block_size
+// 32 a block's sixteen boxes took longer than its tensor-core work; with a second
+// producer workload 5 went from 818 to 967 TFLOP/s.
+#ifndef PKV_PREFILL_TC_TWO_PRODUCERS
+#define PKV_PREFILL_TC_TWO_PRODUCERS 1
+#endif
+constexpr int kTcProducers = PKV_PREFILL_TC_TWO_PRODUCERS ? 2 : 1;
+constexpr int kTcThreads = 32 * (5 + kTcProducers);
 constexpr float kTcRescale = 8.f;
 
 template <int D>
@@ -472,6 +480,10 @@ __host__ __device__ constexpr bool row_once() { return D == 128 ? PKV_PREFILL_RO
 #ifndef PKV_PREFILL_P_TMEM
 #define PKV_PREFILL_P_TMEM 1
 #endif
+// The same at head_dim 64 (there with rows read once, PKV_PREFILL_ROW_ONCE64).
+#ifndef PKV_PREFILL_P_TMEM64
+#define PKV_PREFILL_P_TMEM64 0
+#endif
 // K and V ring stages of the two-tile kernel at head_dim 128 with P in TMEM.
 #ifndef PKV_PREFILL_KSK128
 #define PKV_PREFILL_KSK128 2
@@ -634,8 +646,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   };
   int k_issued = 0, v_issued = 0;  // producer: blocks loaded into each ring
 
-  if (warp == 4) {
-    // ------------------------------------------------------------- producer warp
+  if (warp == 4 || (kTcProducers == 2 && warp == 6)) {
+    // ---------------------------------------------------------- producer warp(s)
+    const bool do_k = warp == 4, do_v = kTcProducers == 1 || warp == 6;
     // every query tile of this (sequence, kv head) reads the same blocks: keep them in L2
     const uint64_t policy = dev::policy_evict_last();
     const int32_t *trow = a.block_tables + (int64_t)b * a.max_blocks;
@@ -644,7 +657,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int ktb = (lane <= lb_last) ? __ldg(trow + lane) : 0;
     int vtb = ktb;
     for (int j = 0; j <= nblk; ++j) {  // K runs one block ahead of V
-      if (j < nblk) {
+      if (do_k && j < nblk) {
         const int s = j % KS;
         if (j >= KS && !__all_sync(0xffffffffu, dev::mbar_wait(k_empty(s), ((j / KS) - 1) & 1))) {
           if (lane == 0) fail(false);
@@ -655,7 +668,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                          policy);
         k_issued = j + 1;
       }
-      if (j >= 1) {
+      if (do_v && j >= 1) {
         const int jv = j - 1, s = jv % KS;
         if (jv >= KS && !__all_sync(0xffffffffu, dev::mbar_wait(v_empty(s), ((jv / KS) - 1) & 1))) {
           if (lane == 0) fail(false);
@@ -831,7 +844,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   // ---- teardown: no tensor-core op or copy may still be in flight when TMEM is freed
   if (tid == 0) (void)dev::mbar_wait(mma_done, 0);
-  if (warp == 4 && lane == 0 && *s_flag) {
+  if ((warp == 4 || (kTcProducers == 2 && warp == 6)) && lane == 0 && *s_flag) {
     for (int s = 0; s < KS; ++s) {
       const int kl = s + ((k_issued - 1 - s) / KS) * KS;
       if (kl >= 0 && kl < k_issued) (void)dev::mbar_wait(k_full(s), (kl / KS) & 1);
@@ -882,7 +895,8 @@ __host__ __device__ constexpr int tc2_threads() { return 32 * (8 * H + 1 + tc2_p
 template <int D, int H>
 struct Tc2Smem {
   // P in TMEM (no P buffers in shared memory)
-  static constexpr bool kPT = D == 128 && H == 1 && row_once<D>() && PKV_PREFILL_P_TMEM != 0;
+  static constexpr bool kPT = H == 1 && row_once<D>() &&
+                              (D == 128 ? PKV_PREFILL_P_TMEM != 0 : PKV_PREFILL_P_TMEM64 != 0);
   static constexpr int KSK = D == 64 ? 3 : (kPT ? PKV_PREFILL_KSK128 : 2);  // stages of the K ring
   static constexpr int KSV = D == 64 ? 3 : (kPT ? PKV_PREFILL_KSV128 : 1);  // stages of the V ring
   static constexpr uint32_t kSub = kTcKeys * 128;    // 128 rows x 128 B (64 dims)
@@ -1238,7 +1252,8 @@ __global__ void __launch_bounds__(tc2_threads<D, H>(), 1)
         // by the same thread, and s_full tracks every MMA issued before its commit, so
         // O_t is stable here.
         uint32_t pk[NCH * 16];
-        const float ls = row_regs_exp_pk<NCH>(xrow, 0, lim, whole, a.scale_log2, m_ref, pk);
+        const float ls =
+            row_regs_exp_pk<NCH, !kOnes>(xrow, 0, lim, whole, a.scale_log2, m_ref, pk);
         if (resc) rescale_o();
         lsum += ls;
         dev::tmem_st32(sb + 64u, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
