@@ -57,8 +57,8 @@ struct PrefillArgs {
 //
 // One CTA owns one (sequence, kv head, tile of 128 query rows) and walks the keys up to
 // the tile's last position in blocks of 128.  Warps 0-3 run the softmax with one thread
-// per row, warp 4 is the TMA producer, and one thread of warp 5 issues the tensor-core
-// instructions:
+// per row, warps 4 and 6 are the TMA producers (K and V), and one thread of warp 5
+// issues the tensor-core instructions:
 //   S_j = Q . K_j^T   tcgen05.mma M=128 N=128 K=D, Q and K_j K-major in shared memory
 //                     (128-byte swizzle), S in TMEM, two buffers: S_{j+1} is computed
 //                     while the softmax works on S_j;
