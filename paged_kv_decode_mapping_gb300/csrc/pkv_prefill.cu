@@ -79,13 +79,36 @@ constexpr int kTcKeys = 128;     // keys per block
 #ifndef PKV_PREFILL_TC_TWO_PRODUCERS
 #define PKV_PREFILL_TC_TWO_PRODUCERS 1
 #endif
+// One-tile kernel at head_dim 128: P in TMEM, two buffers at columns 256 + D and
+// 320 + D (after O), read by P.V as its A operand (1), or in shared memory (0); and then
+// the stages of the K and V rings.
+#ifndef PKV_PREFILL_TC_P_TMEM
+#define PKV_PREFILL_TC_P_TMEM 1
+#endif
+#ifndef PKV_PREFILL_TC_KS128
+#define PKV_PREFILL_TC_KS128 3
+#endif
 constexpr int kTcProducers = PKV_PREFILL_TC_TWO_PRODUCERS ? 2 : 1;
 constexpr int kTcThreads = 32 * (5 + kTcProducers);
 constexpr float kTcRescale = 8.f;
 
+// Whether the softmax reads a row's block from TMEM once into registers (1) or in each
+// of the two passes (0), by head_dim: once at 128 (measured 7% faster), twice at 64,
+// where the extra live registers cost more than the second read.
+#ifndef PKV_PREFILL_ROW_ONCE128
+#define PKV_PREFILL_ROW_ONCE128 1
+#endif
+#ifndef PKV_PREFILL_ROW_ONCE64
+#define PKV_PREFILL_ROW_ONCE64 0
+#endif
+template <int D>
+__host__ __device__ constexpr bool row_once() { return D == 128 ? PKV_PREFILL_ROW_ONCE128 != 0 : PKV_PREFILL_ROW_ONCE64 != 0; }
+
 template <int D>
 struct TcSmem {
-  static constexpr int KS = D == 64 ? 3 : 2;           // stages of each ring
+  // head_dim 128: P in TMEM (two 64-column buffers after O), no P buffers here
+  static constexpr bool kPT = D == 128 && row_once<D>() && PKV_PREFILL_TC_P_TMEM != 0;
+  static constexpr int KS = D == 64 ? 3 : (kPT ? PKV_PREFILL_TC_KS128 : 2);  // stages of each ring
   static constexpr uint32_t kSub = kTcKeys * 128;      // one 64-dim sub-tile of 128 rows
   static constexpr uint32_t kTile = kSub * (D / 64);   // one K or V block / the Q tile
   static constexpr uint32_t k = 0;
@@ -93,7 +116,7 @@ struct TcSmem {
   static constexpr uint32_t q = v + KS * kTile;        // [D/64][128 rows][128 B]
   static constexpr uint32_t p = q + kTile;             // two buffers of [2][128 rows][128 B]
   static constexpr uint32_t kP = 2 * kSub;
-  static constexpr uint32_t bars = p + 2 * kP;
+  static constexpr uint32_t bars = p + (kPT ? 0 : 2 * kP);
   static constexpr int kBars = 4 * KS + 10;
   static constexpr uint32_t tslot = bars + kBars * 8;
   static constexpr uint32_t flag = tslot + 8;
@@ -451,17 +474,6 @@ __device__ __forceinline__ void row_store_p(const uint32_t (&pk)[NCH * 16], int 
   }
 }
 
-// Whether the softmax reads a row's block from TMEM once into registers (1) or in each
-// of the two passes (0), by head_dim: once at 128 (measured 7% faster), twice at 64,
-// where the extra live registers cost more than the second read.
-#ifndef PKV_PREFILL_ROW_ONCE128
-#define PKV_PREFILL_ROW_ONCE128 1
-#endif
-#ifndef PKV_PREFILL_ROW_ONCE64
-#define PKV_PREFILL_ROW_ONCE64 0
-#endif
-template <int D>
-__host__ __device__ constexpr bool row_once() { return D == 128 ? PKV_PREFILL_ROW_ONCE128 != 0 : PKV_PREFILL_ROW_ONCE64 != 0; }
 
 // Two-tile kernel, rows read once: the softmax releases S_t(j) (s_free) as soon as it
 // holds the block in registers, so S_t(j+1) runs on the tensor core during the block's
@@ -709,8 +721,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!(ok = fail(dev::mbar_wait(p_full(j & 1), (j >> 1) & 1)))) break;
         if (!(ok = fail(dev::mbar_wait(v_full(s), (j / KS) & 1)))) break;
         dev::tc_fence_after();
-        issue_pv(tmem + 256u, desc_add(dp0, (j & 1) * SL::kP), desc_add(dv0, s * SL::kTile),
-                 SL::kSub, id_o, j > 0 ? 1u : 0u);
+        if constexpr (SL::kPT)
+          issue_pv_ts(tmem + 256u, tmem + 256u + D + 64u * (j & 1), desc_add(dv0, s * SL::kTile),
+                      id_o, j > 0 ? 1u : 0u);
+        else
+          issue_pv(tmem + 256u, desc_add(dp0, (j & 1) * SL::kP), desc_add(dv0, s * SL::kTile),
+                   SL::kSub, id_o, j > 0 ? 1u : 0u);
         dev::umma_commit(pv_done(j & 1));
         dev::umma_commit(v_empty(s));
       }
@@ -789,8 +805,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (j >= 2 && !(ok = __all_sync(0xffffffffu,
                                       dev::mbar_wait(pv_done(j & 1), ((j - 2) >> 1) & 1))))
         break;
-      // pass 2: P = exp2(S - m_ref) as bf16 into shared memory, and its row sum
-      if constexpr (row_once<D>())
+      // pass 2: P = exp2(S - m_ref) as bf16 into shared memory (or TMEM), and its row sum
+      if constexpr (SL::kPT) {
+        uint32_t pk[kTcKeys / 2];
+        lsum += row_regs_exp_pk<kTcKeys / 32>(xrow, 0, lim, whole, a.scale_log2, m_ref, pk);
+        const uint32_t pb = tmem + lane_base + 256u + D + 64u * (j & 1);
+        dev::tmem_st32(pb, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        dev::tmem_st32(pb + 32u, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        dev::tmem_wait_st();
+      } else if constexpr (row_once<D>())
         lsum += row_regs_exp<kTcKeys / 32>(xrow, 0, bp, SL::p + (j & 1) * SL::kP + r * 128, SL::kSub,
                                            r, lim, whole, a.scale_log2, m_ref);
       else
