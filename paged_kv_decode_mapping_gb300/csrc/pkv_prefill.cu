@@ -63,8 +63,10 @@ struct PrefillArgs {
 //                     (128-byte swizzle), S in TMEM, two buffers: S_{j+1} is computed
 //                     while the softmax works on S_j;
 //   softmax            per row in fp32, base 2, read straight out of TMEM; P_j =
-//                     exp2(S - m) rounded to bf16 into shared memory (K-major);
-//   O += P_j . V_j    tcgen05.mma M=128 N=D K=128, V_j MN-major, O in TMEM.
+//                     exp2(S - m) rounded to bf16, two buffers: at head_dim 128 in
+//                     TMEM after O, at 64 in shared memory (K-major);
+//   O += P_j . V_j    tcgen05.mma M=128 N=D K=128, P_j from TMEM (head_dim 128) or
+//                     shared memory, V_j MN-major, O in TMEM.
 // A row's reference max m moves only when a block raises it by more than 8 (a factor
 // 256): then O and the row sum are rescaled in TMEM.  Otherwise P is taken against the
 // older m, which the final division by the row sum cancels.  The row sum adds the
