@@ -173,6 +173,18 @@ enum { PKV_CONSUMER_TENSOR = 0, PKV_CONSUMER_FMA = 1 };
 int32_t pkv_set_decode_consumer(int32_t consumer);
 
 /*
+ * pkv_decode_ctas_per_sm -- how many CTAs of the decode kernel that `path` (PKV_PATH_*)
+ * launches for this head_dim fit on one SM of the current device, as the CUDA runtime
+ * computes it from the kernel's registers, threads and shared memory (the consumer form
+ * set by pkv_set_decode_consumer for the partition arrangements).  paged_decode_plan
+ * sizes its grids for 3 at head_dim 64 and 2 at 128; a build whose kernels no longer
+ * fit that many would run a second wave.  Returns the count, or PKV_ERR_UNSUPPORTED /
+ * PKV_ERR_CUDA.  Host function; sets the kernel's shared-memory attribute as a launch
+ * would.
+ */
+int32_t pkv_decode_ctas_per_sm(int32_t head_dim, int32_t path);
+
+/*
  * paged_decode_workspace_size -- bytes of workspace paged_decode_attention needs for
  * these sizes on the current device: a completion counter per (sequence, kv head),
  * then the partition results of paged_decode_split's layout for P =

@@ -58,6 +58,8 @@ _lib.paged_decode_path.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
 _lib.paged_decode_path.restype = _i32
 _lib.pkv_set_decode_consumer.argtypes = [_i32]
 _lib.pkv_set_decode_consumer.restype = _i32
+_lib.pkv_decode_ctas_per_sm.argtypes = [_i32, _i32]
+_lib.pkv_decode_ctas_per_sm.restype = _i32
 _lib.paged_decode_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32]
 _lib.paged_decode_workspace_size.restype = _sz
 _lib.paged_decode_split_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32]
@@ -197,6 +199,14 @@ def pkv_set_decode_consumer(consumer: int) -> int:
     if rc < 0:
         _check(rc, "pkv_set_decode_consumer")
     return rc
+
+
+def pkv_decode_ctas_per_sm(head_dim: int, path: int) -> int:
+    """CTAs per SM of the decode kernel of `path` (PATH_*) on the current device."""
+    n = int(_lib.pkv_decode_ctas_per_sm(head_dim, path))
+    if n < 0:
+        _check(n, "pkv_decode_ctas_per_sm")
+    return n
 
 
 def paged_decode_path(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,

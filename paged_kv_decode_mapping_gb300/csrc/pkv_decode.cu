@@ -1715,6 +1715,50 @@ PKV_API int32_t pkv_set_decode_consumer(int32_t consumer) {
   return g_consumer.exchange(consumer);
 }
 
+namespace {
+template <int D>
+int32_t ctas_per_sm(int32_t path) {
+  std::lock_guard<std::mutex> lk(attn_mutex());
+  int dev = 0;
+  int rc = current_device(&dev);
+  if (rc) return rc;
+  const int vi = D == 64 ? 0 : 1;
+  void (*kern)(const CUtensorMap, const CUtensorMap, const DecodeArgs);
+  size_t smem;
+  bool *attr;
+  if (path == PKV_PATH_PERSISTENT) {
+    kern = decode_persistent_kernel<D, persist_stages(D)>;
+    smem = persist_smem(D);
+    attr = &g_persist_attr[dev][vi];
+  } else {
+    const bool fma = g_consumer.load(std::memory_order_relaxed) == PKV_CONSUMER_FMA;
+    kern = fma ? decode_kernel<D, split_stages(D), true> : decode_kernel<D, split_stages(D), false>;
+    smem = split_smem(D);
+    attr = &g_split_attr[dev][vi][fma ? 1 : 0];
+  }
+  if (!*attr) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute");
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(carveout)");
+    *attr = true;
+  }
+  int n = 0;
+  const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem);
+  if (e != cudaSuccess) return cuda_error(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+  clear_error();
+  return n;
+}
+}  // namespace
+
+PKV_API int32_t pkv_decode_ctas_per_sm(int32_t head_dim, int32_t path) {
+  if (path != PKV_PATH_PARTITIONS && path != PKV_PATH_CLUSTER && path != PKV_PATH_PERSISTENT)
+    return set_error(PKV_ERR_UNSUPPORTED, "pkv_decode_ctas_per_sm: unknown path %d", path);
+  if (head_dim == 64) return ctas_per_sm<64>(path);
+  if (head_dim == 128) return ctas_per_sm<128>(path);
+  return set_error(PKV_ERR_UNSUPPORTED, "pkv_decode_ctas_per_sm: head_dim %d", head_dim);
+}
+
 PKV_API int32_t paged_decode_path(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                   int32_t head_dim, int32_t max_context_len, int32_t num_sms) {
   const int32_t mlen = max_context_len > 0 ? max_context_len : 1;

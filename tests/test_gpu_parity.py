@@ -971,3 +971,22 @@ def test_fma_consumer_workloads(B, oracle, fma_consumer, wid, P):
     torch.cuda.synchronize()
     assert_no_device_errors(B)
     check_attention(out, ref, f"{w.name} (fma consumer)")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("path", ["partitions", "persistent"])
+def test_decode_kernels_fit_the_planned_ctas_per_sm(B, D, path):
+    """The launcher sizes grids for 3 decode CTAs per SM at head_dim 64 and 2 at 128; a
+    kernel whose registers or shared memory no longer allow that would run a second wave
+    of CTAs.  Checked against the CUDA runtime's occupancy for the built kernels, both
+    consumer forms of the partition kernel included."""
+    want = 3 if D == 64 else 2
+    p = B.PATH_PERSISTENT if path == "persistent" else B.PATH_PARTITIONS
+    assert B.pkv_decode_ctas_per_sm(D, p) == want
+    if path == "partitions":
+        prev = B.pkv_set_decode_consumer(B.CONSUMER_FMA)
+        try:
+            assert B.pkv_decode_ctas_per_sm(D, p) == want
+        finally:
+            B.pkv_set_decode_consumer(prev)
