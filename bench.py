@@ -25,10 +25,13 @@ in GB/s (whole job: all ranks' bytes / the slowest rank's time).
 
 `roofline` covers the dominant kernel (the decode kernel), timed alone by
 the same method; `e2e` runs the same step through the public API with the step's
-inputs copied from pinned host memory and the output read back each step;
-`cpu_baseline` is the CPU oracle (fp64, all host cores) on the same workload.
-`e2e` replays the whole step -- copies in, paged_decode_step, copy out -- as one CUDA
-graph per step (the eager time is reported beside it).
+inputs in pinned host memory and the output read back into pinned host memory each
+step; `cpu_baseline` is the CPU oracle (fp64, all host cores) on the same workload.
+`e2e` hands paged_decode_step the pinned host buffers themselves (zero-copy: the
+kernels read the inputs and write the output over the host link), one CUDA graph
+replayed and synchronised per step (the eager time is reported beside it); the
+breakdown also gives the same step with an explicit copy in and copy out as graph
+nodes.
 
 `--impl reference` times that oracle as the reference arm (rank 0 only).
 
@@ -428,11 +431,13 @@ def run_ours(args, w) -> None:
     achieved = nb["decode_kernel"] / dec_s / 1e9
 
     # end to end through the public API: pinned host inputs in, output back, every step.
-    # The step -- the host-to-device copy of its inputs, paged_decode_step, the
-    # device-to-host copy of out -- is captured once as a CUDA graph and replayed, then
-    # synchronised, each step; the same step run eagerly is reported beside it.
-    # one pinned staging buffer holds all of the step's inputs (256-byte aligned pieces),
-    # so they cross in a single host-to-device copy
+    # The step's inputs sit in one pinned host buffer and its output in another;
+    # paged_decode_step takes them as they are (zero-copy: the kernels read the inputs and
+    # write the output over the host link), captured once as a CUDA graph and replayed,
+    # then synchronised, each step; the same step run eagerly is reported beside it.  The
+    # same step with a host-to-device copy of the inputs before it and a device-to-host
+    # copy of out after it (three graph nodes) is measured too, for the breakdown.
+    # (256-byte aligned pieces of one buffer: one copy in the copy-node form)
     names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")
     offs, total = [], 0
     for k in names:
@@ -454,7 +459,13 @@ def run_ours(args, w) -> None:
     d2h = out_h.numel() * out_h.element_size()
     e2e_steps = max(20, min(args.steps, 2000))
 
-    def e2e_body(r):
+    hq, hkn, hvn, hsm, hbt, hcl = (view(stage_h, k, o) for k, o in zip(names, offs))
+
+    def e2e_body(r):  # zero-copy
+        B.paged_decode_step(out_h, hq, hkn, hvn, hsm, kcs[r], vcs[r], hbt, hcl, max_len, scale,
+                            workspace=ws)
+
+    def copy_body(r):  # copy nodes
         stage_d.copy_(stage_h, non_blocking=True)
         B.paged_decode_step(out, dq, dkn, dvn, dsm, kcs[r], vcs[r], dbt, dcl, max_len, scale,
                             workspace=ws)
@@ -476,15 +487,35 @@ def run_ours(args, w) -> None:
         torch.cuda.synchronize()
         return reduce_max(e0.elapsed_time(e1) / 1e3 / e2e_steps, world, device)
 
-    e2e_graphs = []
-    for r in range(R):
-        gr = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gr, stream=stream):
-            e2e_body(r)
-        e2e_graphs.append(gr)
+    def graphs_of(body):
+        gs = []
+        for r in range(R):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                body(r)
+            gs.append(gr)
+        return gs
+
+    e2e_graphs = graphs_of(e2e_body)
     t_e2e = time_e2e(lambda r: e2e_graphs[r].replay())
     t_e2e_eager = time_e2e(e2e_body)
     e2e_value = reduce_sum(nb["step"], world, device) / t_e2e / 1e9
+    copy_graphs = graphs_of(copy_body)
+    t_copy_e2e = time_e2e(lambda r: copy_graphs[r].replay())
+
+    def replays_us(gs, n=200) -> float:  # device time per step, replays back to back
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for i in range(R):
+                gs[i].replay()
+            e0.record(stream)
+            for i in range(n):
+                gs[i % R].replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / n
+
+    zc_step_us = replays_us(e2e_graphs)
 
     # Where the end-to-end time goes: the device time of the two copies (each measured
     # as 20 copies in one graph, back to back), the device time of the step (the timed
@@ -516,9 +547,13 @@ def run_ours(args, w) -> None:
             step(r)
         step_graphs.append(gr)
     t_step_sync = time_e2e(lambda r: step_graphs[r].replay())
-    breakdown = {"h2d_us": h2d_us, "step_us": us_step, "d2h_us": d2h_us,
-                 "launch_sync_us": t_e2e * 1e6 - (h2d_us + us_step + d2h_us),
-                 "step_alone_replayed_and_synchronised_us": t_step_sync * 1e6}
+    breakdown = {"zero_copy_step_us": zc_step_us,
+                 "launch_sync_us": t_e2e * 1e6 - zc_step_us,
+                 "step_us": us_step,
+                 "step_alone_replayed_and_synchronised_us": t_step_sync * 1e6,
+                 "copy_nodes_e2e_us": t_copy_e2e * 1e6,
+                 "copy_nodes_h2d_us": h2d_us, "copy_nodes_d2h_us": d2h_us,
+                 "copy_nodes_launch_sync_us": t_copy_e2e * 1e6 - (h2d_us + us_step + d2h_us)}
 
     peaks = measured_peaks()
     peak = peaks.get("hbm_gbs")
@@ -554,8 +589,10 @@ def run_ours(args, w) -> None:
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "us_per_step": t_e2e * 1e6,
-                "how": "one pinned H2D copy of the step's inputs + paged_decode_step + D2H of "
-                       "out, one CUDA graph replayed and synchronised per step",
+                "how": "paged_decode_step on pinned host inputs and a pinned host output "
+                       "(zero-copy: the kernels read and write them over the host link), one CUDA "
+                       "graph replayed and synchronised per step; breakdown copy_nodes_*: the same "
+                       "step with one H2D copy of the inputs and one D2H copy of out as graph nodes",
                 "eager_us_per_step": t_e2e_eager * 1e6, "breakdown": breakdown},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,

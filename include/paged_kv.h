@@ -17,6 +17,13 @@
  *    the caller; the library allocates nothing and keeps no pointer after the
  *    call returns.  `stream` is a cudaStream_t (NULL = the legacy default
  *    stream); all work is enqueued asynchronously on it.
+ *  - Exception, for paged_kv_write, paged_decode_attention and paged_decode_step:
+ *    the per-step inputs and the output -- q, out, k and v (new), slot_mapping,
+ *    block_tables, context_lens -- may instead be page-locked host memory that
+ *    the device addresses directly (cudaHostAlloc / cudaMallocHost, with unified
+ *    addressing the host pointer is the device pointer).  The kernels then read
+ *    and write it over the host link: no copy of its own precedes or follows
+ *    the call.  Caches and workspace are always device memory.
  *  - Layouts are dense and row-major (C order):
  *      k_cache, v_cache : [num_blocks][num_kv_heads][block_size][head_dim]
  *      q, out           : [num_seqs][num_q_heads][head_dim]

@@ -125,13 +125,14 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
-def _need(t: torch.Tensor, name: str, dtype, ndim: int):
+def _need(t: torch.Tensor, name: str, dtype, ndim: int, host_ok: bool = False):
+    """host_ok: a page-locked CPU tensor is accepted too (the kernels address it directly)."""
     if t.dtype != dtype:
         raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
     if t.dim() != ndim:
         raise ValueError(f"{name}: expected {ndim} dims, got shape {tuple(t.shape)}")
-    if not t.is_cuda:
-        raise ValueError(f"{name}: must be a CUDA tensor")
+    if not t.is_cuda and not (host_ok and t.is_pinned()):
+        raise ValueError(f"{name}: must be a CUDA tensor" + (" or pinned host memory" if host_ok else ""))
     if not t.is_contiguous():
         raise ValueError(f"{name}: must be contiguous")
 
@@ -143,10 +144,11 @@ def cache_desc(k_cache: torch.Tensor) -> pkv_cache_desc:
 
 def paged_kv_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
                    k_cache: torch.Tensor, v_cache: torch.Tensor, stream=None) -> None:
-    """k/v [T, Hkv, D] bf16 are copied into k_cache/v_cache [NB, Hkv, BS, D] at their slots."""
-    _need(k, "k", torch.bfloat16, 3)
-    _need(v, "v", torch.bfloat16, 3)
-    _need(slot_mapping, "slot_mapping", torch.int64, 1)
+    """k/v [T, Hkv, D] bf16 are copied into k_cache/v_cache [NB, Hkv, BS, D] at their slots
+    (k, v and slot_mapping may be pinned host tensors)."""
+    _need(k, "k", torch.bfloat16, 3, True)
+    _need(v, "v", torch.bfloat16, 3, True)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1, True)
     _need(k_cache, "k_cache", torch.bfloat16, 4)
     _need(v_cache, "v_cache", torch.bfloat16, 4)
     if k.shape != v.shape or k_cache.shape != v_cache.shape:
@@ -235,12 +237,12 @@ def paged_decode_split_workspace_size(num_seqs: int, num_q_heads: int, head_dim:
                                                       max_context_len, partition_tokens))
 
 
-def _decode_checks(q, k_cache, v_cache, block_tables, context_lens):
-    _need(q, "q", torch.bfloat16, 3)
+def _decode_checks(q, k_cache, v_cache, block_tables, context_lens, host_ok=False):
+    _need(q, "q", torch.bfloat16, 3, host_ok)
     _need(k_cache, "k_cache", torch.bfloat16, 4)
     _need(v_cache, "v_cache", torch.bfloat16, 4)
-    _need(block_tables, "block_tables", torch.int32, 2)
-    _need(context_lens, "context_lens", torch.int32, 1)
+    _need(block_tables, "block_tables", torch.int32, 2, host_ok)
+    _need(context_lens, "context_lens", torch.int32, 1, host_ok)
     if k_cache.shape != v_cache.shape:
         raise ValueError("k_cache and v_cache shapes differ")
     B = q.shape[0]
@@ -256,15 +258,17 @@ def paged_decode_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Te
 
     ``workspace`` (uint8, CUDA, zero-filled before its first use) may be omitted; then a
     zeroed buffer of ``paged_decode_workspace_size`` bytes is taken from torch's allocator.
+    out, q, block_tables and context_lens may be pinned host tensors (read and written
+    by the kernels over the host link).
     """
-    _decode_checks(q, k_cache, v_cache, block_tables, context_lens)
-    _need(out, "out", torch.bfloat16, 3)
+    _decode_checks(q, k_cache, v_cache, block_tables, context_lens, host_ok=True)
+    _need(out, "out", torch.bfloat16, 3, True)
     if out.shape != q.shape:
         raise ValueError("out must have q's shape")
     B, Hq, D = q.shape
     need = paged_decode_workspace_size(B, Hq, k_cache.shape[1], D, max_context_len)
     if workspace is None and need > 0:
-        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=k_cache.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     d = cache_desc(k_cache)
     _check(_lib.paged_decode_attention(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
@@ -279,18 +283,20 @@ def paged_decode_step(out: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: to
                       block_tables: torch.Tensor, context_lens: torch.Tensor,
                       max_context_len: int, scale: float, workspace: Optional[torch.Tensor] = None,
                       stream=None) -> None:
-    """One decode step: the slot write of k/v, then attention over the updated caches."""
-    _decode_checks(q, k_cache, v_cache, block_tables, context_lens)
-    _need(out, "out", torch.bfloat16, 3)
-    _need(k, "k", torch.bfloat16, 3)
-    _need(v, "v", torch.bfloat16, 3)
-    _need(slot_mapping, "slot_mapping", torch.int64, 1)
+    """One decode step: the slot write of k/v, then attention over the updated caches.
+    out, q, k, v, slot_mapping, block_tables and context_lens may be pinned host tensors:
+    the kernels then read and write them over the host link (no copies)."""
+    _decode_checks(q, k_cache, v_cache, block_tables, context_lens, host_ok=True)
+    _need(out, "out", torch.bfloat16, 3, True)
+    _need(k, "k", torch.bfloat16, 3, True)
+    _need(v, "v", torch.bfloat16, 3, True)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1, True)
     if out.shape != q.shape or k.shape != v.shape or k.shape[0] != slot_mapping.shape[0]:
         raise ValueError("out/q, k/v or slot_mapping shapes disagree")
     B, Hq, D = q.shape
     need = paged_decode_workspace_size(B, Hq, k_cache.shape[1], D, max_context_len)
     if workspace is None and need > 0:
-        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=k_cache.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     d = cache_desc(k_cache)
     _check(_lib.paged_decode_step(_ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(slot_mapping),
@@ -326,7 +332,7 @@ def paged_decode_step_rope(out: torch.Tensor, q: torch.Tensor, k: torch.Tensor, 
         raise ValueError("cos_sin must be [max_position, rotary_dim]")
     need = paged_decode_workspace_size(B, Hq, k_cache.shape[1], D, max_context_len)
     if workspace is None and need > 0:
-        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=k_cache.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     d = cache_desc(k_cache)
     _check(_lib.paged_decode_step_rope(_ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(slot_mapping),

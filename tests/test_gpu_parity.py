@@ -583,13 +583,15 @@ def test_block_manager_driven_decode_steps(B, oracle):
 
 
 
-def test_whole_step_graph_replay(B, oracle):
+@pytest.mark.parametrize("zero_copy", [False, True])
+def test_whole_step_graph_replay(B, oracle, zero_copy):
     """The whole decode step -- one host-to-device copy of the step's inputs from pinned
     memory, paged_decode_step, the device-to-host copy of the output -- captured once
     as a CUDA graph and replayed for several steps, the host buffers refilled between
     replays (one new token per sequence per step).  Every replay's output matches the
     oracle, the caches match bit for bit, and the merge counters stay consistent across
-    replays (the lengths need several partitions)."""
+    replays (the lengths need several partitions).  zero_copy: no copies; the kernels
+    read the inputs from, and write the output to, the pinned host buffers."""
     Bn, Hq, Hkv, D, BS, steps = 3, 8, 2, 64, 16, 5
     w = W.small_workload(B=Bn, Hq=Hq, Hkv=Hkv, D=D, BS=BS, lens=(1300, 700, 1517), seed=23,
                          write="none")
@@ -611,6 +613,11 @@ def test_whole_step_graph_replay(B, oracle):
                      device="cuda")
 
     def body():
+        if zero_copy:
+            B.paged_decode_step(out_h, host["q"], host["k_new"], host["v_new"],
+                                host["slot_mapping"], kg, vg, host["block_tables"],
+                                host["context_lens"], max_len, inp["scale"], workspace=ws)
+            return
         for k in names:
             devb[k].copy_(host[k], non_blocking=True)
         B.paged_decode_step(out, devb["q"], devb["k_new"], devb["v_new"], devb["slot_mapping"],
@@ -990,3 +997,32 @@ def test_decode_kernels_fit_the_planned_ctas_per_sm(B, D, path):
             assert B.pkv_decode_ctas_per_sm(D, p) == want
         finally:
             B.pkv_set_decode_consumer(prev)
+
+
+@pytest.mark.parametrize("wid", [2, 3, 4])
+def test_decode_step_zero_copy_matches_device_inputs(B, wid):
+    """paged_decode_step with the step's inputs and output in pinned host memory (the
+    kernels read and write them over the host link) gives bit for bit the output and the
+    caches of the same step on device copies, on the cluster (2) and persistent (3, 4)
+    arrangements."""
+    w = W.WORKLOADS[wid]
+    inp = W.make_inputs(w)
+    names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")
+    host = {k: inp[k].contiguous().pin_memory() for k in names}
+    dev = {k: inp[k].cuda() for k in names}
+    outs, caches = [], []
+    for src in (dev, host):
+        kc, vc = inp["k_cache"].cuda(), inp["v_cache"].cuda()
+        out = (torch.empty(inp["q"].shape, dtype=torch.bfloat16, device="cuda") if src is dev
+               else torch.empty(inp["q"].shape, dtype=torch.bfloat16).pin_memory())
+        B.paged_decode_step(out, src["q"], src["k_new"], src["v_new"], src["slot_mapping"], kc, vc,
+                            src["block_tables"], src["context_lens"], inp["max_context_len"],
+                            inp["scale"])
+        torch.cuda.synchronize()
+        outs.append(out.cpu())
+        caches.append((kc.cpu(), vc.cpu()))
+        del kc, vc
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    assert torch.equal(caches[0][0].view(torch.int16), caches[1][0].view(torch.int16))
+    assert torch.equal(caches[0][1].view(torch.int16), caches[1][1].view(torch.int16))
+    assert_no_device_errors(B)
