@@ -591,27 +591,18 @@ __global__ void __launch_bounds__(kThreads, split_occupancy(D))
   const int win0 = (part * a.partition_tokens) >> a.log2_bs;
   int tb0 = 0;
   if (warp == kConsumerWarps && win0 + lane < a.max_blocks) tb0 = __ldg(trow + win0 + lane);
-  // consumer warps: the group's query rows as mma B fragments (tensor form) or in
-  // shared memory (CUDA-core form; published by the set-up barrier below), loaded up front
+  // consumer warps: the group's query rows, loaded up front into shared memory with one
+  // 16-byte load per thread (published by the set-up barrier below; q may be in host
+  // memory, where few wide reads beat many narrow ones); the tensor form takes its mma B
+  // fragments from there
   uint32_t qb[KS][2];
   if (warp < kConsumerWarps) {
     // In a step whose first kernel rotates q in place, q is read only after that grid.
     if (a.q_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint16_t *qg = a.q + ((int64_t)b * a.num_q_heads + g * a.group) * D;
-    if constexpr (kFma) {
-      if (tid < a.group * D / 8)
-        *reinterpret_cast<uint4 *>(base_ptr + (q_area - base) + tid * 16) =
-            __ldcg(reinterpret_cast<const uint4 *>(qg) + tid);
-    } else {
-      const int gid = lane >> 2, tig = lane & 3;
-      const bool hv = gid < a.group;
-      const uint32_t *qrow = reinterpret_cast<const uint32_t *>(qg + (hv ? gid : 0) * D);
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        qb[ks][0] = hv ? __ldcg(qrow + 8 * ks + tig) : 0u;
-        qb[ks][1] = hv ? __ldcg(qrow + 8 * ks + 4 + tig) : 0u;
-      }
-    }
+    if (tid < a.group * D / 8)
+      *reinterpret_cast<uint4 *>(base_ptr + (q_area - base) + tid * 16) =
+          __ldcg(reinterpret_cast<const uint4 *>(qg) + tid);
   }
 
   int L = __ldg(a.context_lens + b);
@@ -709,10 +700,19 @@ __global__ void __launch_bounds__(kThreads, split_occupancy(D))
     // ----------------------------------------------------------- consumer warps
     WarpAcc<D> acc;    // tensor form
     WarpAccF<D> accf;  // CUDA-core form
-    if constexpr (kFma)
+    if constexpr (kFma) {
       accf_reset(accf);
-    else
+    } else {
       acc_reset(acc);
+      const uint32_t *qs = reinterpret_cast<const uint32_t *>(base_ptr + (q_area - base));
+      const int gid = lane >> 2, tig = lane & 3;
+      const bool hv = gid < a.group;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        qb[ks][0] = hv ? qs[gid * (D / 2) + 8 * ks + tig] : 0u;
+        qb[ks][1] = hv ? qs[gid * (D / 2) + 8 * ks + 4 + tig] : 0u;
+      }
+    }
     for (int c = 0; c < n_chunks; ++c) {
       const int s = c % STAGES;
       if (!__all_sync(0xffffffffu, dev::mbar_wait(bar_full + 8 * s, (c / STAGES) & 1))) {
