@@ -171,3 +171,24 @@ def test_noalloc_refuses_bad_arguments_before_any_device_work(B):
     assert call(_desc(B, hkv=2), 8, n=2, q=ctypes.c_void_p((1 << 20) + 4)) == -5
     assert call(_desc(B, hkv=2), 8, n=2, max_len=100) == -2                       # over the table
     assert call(_desc(B, hkv=2), 8, n=0, out=None, q=None) == 0                   # nothing to do
+
+
+def test_ctas_per_sm_rejects_unknown_shapes_without_a_device(B):
+    """pkv_decode_ctas_per_sm refuses a head_dim or an arrangement it has no kernel for,
+    on the host, before asking the CUDA runtime anything."""
+    lib = B.lib()
+    assert lib.pkv_decode_ctas_per_sm(96, B.PATH_PERSISTENT) == -3
+    assert lib.pkv_decode_ctas_per_sm(64, 7) == -3
+    assert lib.pkv_decode_ctas_per_sm(128, 0) == -3
+
+
+def test_pinned_host_tensors_are_accepted_only_where_documented(B):
+    """The binding lets pinned host tensors through for the per-step decode arguments and
+    nowhere else (the caches stay device memory); pageable host tensors are refused."""
+    import torch
+
+    q = torch.zeros(2, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="pinned host memory"):
+        B._need(q, "q", torch.bfloat16, 3, True)  # pageable
+    with pytest.raises(ValueError, match="must be a CUDA tensor$"):
+        B._need(q, "k_cache", torch.bfloat16, 3)
