@@ -1026,3 +1026,27 @@ def test_decode_step_zero_copy_matches_device_inputs(B, wid):
     assert torch.equal(caches[0][0].view(torch.int16), caches[1][0].view(torch.int16))
     assert torch.equal(caches[0][1].view(torch.int16), caches[1][1].view(torch.int16))
     assert_no_device_errors(B)
+
+
+@pytest.mark.parametrize("wid", [1, 2, 5])
+def test_decode_attention_and_write_zero_copy(B, wid):
+    """paged_kv_write and paged_decode_attention with their per-step arguments in pinned
+    host memory (workload 1: one partition; 2: cluster merge; 5: ticket merge) give bit
+    for bit the caches and output of the same calls on device copies."""
+    w = W.WORKLOADS[wid]
+    inp = W.make_inputs(w)
+    results = []
+    for host in (False, True):
+        put = (lambda t: t.contiguous().pin_memory()) if host else (lambda t: t.cuda())
+        kc, vc = inp["k_cache"].cuda(), inp["v_cache"].cuda()
+        B.paged_kv_write(put(inp["k_new"]), put(inp["v_new"]), put(inp["slot_mapping"]), kc, vc)
+        out = put(torch.empty(inp["q"].shape, dtype=torch.bfloat16))
+        B.paged_decode_attention(out, put(inp["q"]), kc, vc, put(inp["block_tables"]),
+                                 put(inp["context_lens"]), inp["max_context_len"], inp["scale"])
+        torch.cuda.synchronize()
+        results.append((out.cpu().view(torch.int16), kc.cpu().view(torch.int16),
+                        vc.cpu().view(torch.int16)))
+        del kc, vc
+    for a, b in zip(*results):
+        assert torch.equal(a, b)
+    assert_no_device_errors(B)
