@@ -457,6 +457,68 @@ __device__ __forceinline__ float row_regs_exp_pk(const uint32_t (&x)[NCH * 32], 
   return ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
 }
 
+// The body of row_regs_exp_pk_max for one masking mode, the running maxima in mx.
+template <int NCH, bool kSum, int kMode>  // kMode 0: whole, positive scale; 1: whole; 2: masked
+__device__ __forceinline__ float row_regs_exp_pk_max_impl(const uint32_t (&x)[NCH * 32], int ch0,
+                                                          int lim, float sc, float scale_log2,
+                                                          float m_ref, uint32_t (&pk)[NCH * 16],
+                                                          float (&mx)[8]) {
+  float ls[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) ls[u] = 0.f;
+#pragma unroll
+  for (int ch = 0; ch < NCH; ++ch) {
+    const int lc = kMode == 2 ? lim - (ch0 + ch) * 32 : 32;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const float x0 = __uint_as_float(x[ch * 32 + 2 * e]), x1 = __uint_as_float(x[ch * 32 + 2 * e + 1]);
+      if constexpr (kMode == 0)
+        mx[e & 7] = fmax3(mx[e & 7], x0, x1);
+      else if constexpr (kMode == 1)
+        mx[e & 7] = fmax3(mx[e & 7], x0 * sc, x1 * sc);
+      else
+        mx[e & 7] = fmax3(mx[e & 7], 2 * e <= lc ? x0 * sc : -INFINITY,
+                          2 * e + 1 <= lc ? x1 * sc : -INFINITY);
+      float a0, a1;
+      fma_f32x2(x0, x1, scale_log2, -m_ref, a0, a1);
+      float p0 = dev::ex2(a0), p1 = dev::ex2(a1);
+      if constexpr (kMode == 2) {
+        p0 = 2 * e <= lc ? p0 : 0.f;
+        p1 = 2 * e + 1 <= lc ? p1 : 0.f;
+      }
+      pk[ch * 16 + e] = dev::pack_bf16x2(p0, p1);
+      if constexpr (kSum) ls[e & 7] = add_bf16x2(pk[ch * 16 + e], ls[e & 7]);
+    }
+  }
+  return ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+}
+
+// row_regs_exp_pk and row_regs_max in one pass: the weights against a reference m_ref
+// taken before the block's max is known, and that max (as row_regs_max returns it) in
+// *bmax.  Weights of columns far above m_ref may overflow; the caller recomputes them
+// once the max says the reference must move.
+template <int NCH, bool kSum = true>
+__device__ __forceinline__ float row_regs_exp_pk_max(const uint32_t (&x)[NCH * 32], int ch0, int lim,
+                                                     bool whole, bool pos_scale, float scale_log2,
+                                                     float m_ref, uint32_t (&pk)[NCH * 16],
+                                                     float *bmax) {
+  float mx[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
+  const float sc = pos_scale ? 1.f : scale_log2;
+  float ls;
+  if (whole && pos_scale)
+    ls = row_regs_exp_pk_max_impl<NCH, kSum, 0>(x, ch0, lim, sc, scale_log2, m_ref, pk, mx);
+  else if (whole)
+    ls = row_regs_exp_pk_max_impl<NCH, kSum, 1>(x, ch0, lim, sc, scale_log2, m_ref, pk, mx);
+  else
+    ls = row_regs_exp_pk_max_impl<NCH, kSum, 2>(x, ch0, lim, sc, scale_log2, m_ref, pk, mx);
+  const float m = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                        fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+  *bmax = pos_scale ? m * scale_log2 : m;
+  return ls;
+}
+
 // Stores the packed weights of row_regs_exp_pk into row r of the P buffer (K-major,
 // 128-byte swizzle, two 64-column sub-tiles `sub` bytes apart).
 template <int NCH>
@@ -493,6 +555,12 @@ __device__ __forceinline__ void row_store_p(const uint32_t (&pk)[NCH * 16], int 
 // one thread run in issue order).  Takes precedence over PKV_PREFILL_EARLY_S.
 #ifndef PKV_PREFILL_P_TMEM
 #define PKV_PREFILL_P_TMEM 1
+#endif
+// With P in TMEM, blocks after the first take their weights against the reference max
+// they start with and their max in the same pass, recomputing the weights only when the
+// block moves the reference (1); or the max first, then the weights (0).
+#ifndef PKV_PREFILL_ONE_PASS
+#define PKV_PREFILL_ONE_PASS 1
 #endif
 // The same at head_dim 64 (there with rows read once, PKV_PREFILL_ROW_ONCE64).
 #ifndef PKV_PREFILL_P_TMEM64
@@ -960,6 +1028,7 @@ __global__ void __launch_bounds__(tc2_threads<D, H>(), 1)
   constexpr bool kOnes = SL::kOnes;        // row sums from the tensor core
   constexpr int kON = D + (kOnes ? 16 : 0);  // O columns per tile (then the row sums)
   constexpr bool kPT = SL::kPT;           // P in TMEM, over the upper half of S_t
+  constexpr bool kOnePass = kPT && PKV_PREFILL_ONE_PASS != 0;
   constexpr bool kEarlyS = !kPT && PKV_PREFILL_EARLY_S != 0 && row_once<D>();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = dev::smem_addr(smem_raw);
@@ -1225,7 +1294,8 @@ __global__ void __launch_bounds__(tc2_threads<D, H>(), 1)
       // the same for both halves of a row: its rows and the block are the same
       const bool whole = __all_sync(0xffffffffu, lim >= kTcKeys - 1);
       uint32_t xrow[row_once<D>() ? NCH * 32 : 1];
-      float hmax;
+      float hmax = -INFINITY;
+      const bool one_pass = kOnePass && j > 0;  // the max comes with the weights below
       if constexpr (row_once<D>()) {
         row_block_load<NCH>(sb, hc * NCH, xrow);
         if constexpr (kEarlyS) {  // S_t(j) is in registers: the tensor core may overwrite it
@@ -1233,7 +1303,7 @@ __global__ void __launch_bounds__(tc2_threads<D, H>(), 1)
           __syncwarp();
           if (lane == 0) dev::mbar_arrive(s_free(t));
         }
-        hmax = row_regs_max<NCH>(xrow, hc * NCH, lim, whole, pos_scale, a.scale_log2);
+        if (!one_pass) hmax = row_regs_max<NCH>(xrow, hc * NCH, lim, whole, pos_scale, a.scale_log2);
       } else {
         hmax = row_block_max<NCH>(sb, hc * NCH, lim, whole, pos_scale, a.scale_log2);
       }
@@ -1243,7 +1313,9 @@ __global__ void __launch_bounds__(tc2_threads<D, H>(), 1)
       // than kTcRescale; then O_t (and its row-sum column) and the row sum scale by f.
       float f = 1.f;
       bool resc = false;
-      if (j > 0) {
+      if (one_pass) {
+        // decided after the weights, below
+      } else if (j > 0) {
         const bool need = bmax > m_ref + kTcRescale;
         resc = __any_sync(0xffffffffu, need);
         if (resc) {
@@ -1277,8 +1349,24 @@ __global__ void __launch_bounds__(tc2_threads<D, H>(), 1)
         // by the same thread, and s_full tracks every MMA issued before its commit, so
         // O_t is stable here.
         uint32_t pk[NCH * 16];
-        const float ls =
-            row_regs_exp_pk<NCH, !kOnes>(xrow, 0, lim, whole, a.scale_log2, m_ref, pk);
+        float ls;
+        if (one_pass) {
+          float bm;
+          ls = row_regs_exp_pk_max<NCH, !kOnes>(xrow, 0, lim, whole, pos_scale, a.scale_log2,
+                                                m_ref, pk, &bm);
+          const bool need = bm > m_ref + kTcRescale;
+          resc = __any_sync(0xffffffffu, need);
+          if (resc) {  // the reference moves: the weights again, against the new one, from
+                       // S_t(j) read once more (the registers were spent on the first pass)
+            const float m_new = fmaxf(m_ref, bm);
+            f = need ? dev::ex2(m_ref - m_new) : 1.f;
+            if (need) m_ref = m_new;
+            row_block_load<NCH>(sb, hc * NCH, xrow);
+            ls = row_regs_exp_pk<NCH, !kOnes>(xrow, 0, lim, whole, a.scale_log2, m_ref, pk);
+          }
+        } else {
+          ls = row_regs_exp_pk<NCH, !kOnes>(xrow, 0, lim, whole, a.scale_log2, m_ref, pk);
+        }
         if (resc) rescale_o();
         lsum += ls;
         dev::tmem_st32(sb + 64u, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
