@@ -95,13 +95,14 @@ constexpr int kTcThreads = 32 * (5 + kTcProducers);
 constexpr float kTcRescale = 8.f;
 
 // Whether the softmax reads a row's block from TMEM once into registers (1) or in each
-// of the two passes (0), by head_dim: once at 128 (measured 7% faster), twice at 64,
-// where the extra live registers cost more than the second read.
+// of the two passes (0), by head_dim: once at 128 (measured 7% faster).  At 64 twice was
+// faster while P went through shared memory (the extra live registers cost more than
+// the second read); with P in TMEM and the weights and max in one pass, once is.
 #ifndef PKV_PREFILL_ROW_ONCE128
 #define PKV_PREFILL_ROW_ONCE128 1
 #endif
 #ifndef PKV_PREFILL_ROW_ONCE64
-#define PKV_PREFILL_ROW_ONCE64 0
+#define PKV_PREFILL_ROW_ONCE64 1
 #endif
 template <int D>
 __host__ __device__ constexpr bool row_once() { return D == 128 ? PKV_PREFILL_ROW_ONCE128 != 0 : PKV_PREFILL_ROW_ONCE64 != 0; }
@@ -547,8 +548,8 @@ __device__ __forceinline__ void row_store_p(const uint32_t (&pk)[NCH * 16], int 
 #ifndef PKV_PREFILL_EARLY_S
 #define PKV_PREFILL_EARLY_S 1
 #endif
-// Two-tile kernel at head_dim 128: the softmax writes P into TMEM over the upper half of
-// its S buffer and P.V reads it from there (A operand in TMEM), so P never passes
+// Two-tile kernel at head_dim 128: the softmax writes P into TMEM over its S buffer
+// (the columns it has read) and P.V reads it from there (A operand in TMEM), so P never passes
 // through shared memory, whose bandwidth the operand reads of both MMAs, the TMA writes
 // and the P stores otherwise share; the freed buffers give V a second stage.  The
 // tensor core then takes PV_t(j) before S_t(j+1) overwrites the buffer (the MMAs of
@@ -562,9 +563,11 @@ __device__ __forceinline__ void row_store_p(const uint32_t (&pk)[NCH * 16], int 
 #ifndef PKV_PREFILL_ONE_PASS
 #define PKV_PREFILL_ONE_PASS 1
 #endif
-// The same at head_dim 64 (there with rows read once, PKV_PREFILL_ROW_ONCE64).
+// The same at head_dim 64 (there with rows read once, PKV_PREFILL_ROW_ONCE64): alone
+// within 1% of P in shared memory, 10% / 7% faster on the two D = 64 workloads once the
+// one-pass weights came with it.
 #ifndef PKV_PREFILL_P_TMEM64
-#define PKV_PREFILL_P_TMEM64 0
+#define PKV_PREFILL_P_TMEM64 1
 #endif
 // K and V ring stages of the two-tile kernel at head_dim 128 with P in TMEM.
 #ifndef PKV_PREFILL_KSK128
@@ -644,10 +647,11 @@ __device__ __forceinline__ void umma4_ts(uint32_t d_tmem, uint32_t a0, uint32_t 
       : "memory");
 }
 __device__ __forceinline__ void issue_pv_ts(uint32_t d_tmem, uint32_t p_tmem, uint64_t v,
-                                            uint32_t idesc, uint32_t acc_first) {
+                                            uint32_t idesc, uint32_t acc_first,
+                                            uint32_t group_cols = 32u) {
 #pragma unroll
   for (int g4 = 0; g4 < kTcKeys / 64; ++g4) {
-    const uint32_t a = p_tmem + 32u * g4, vo = g4 * 4 * 2048u;
+    const uint32_t a = p_tmem + group_cols * g4, vo = g4 * 4 * 2048u;
     umma4_ts(d_tmem, a, a + 8, a + 16, a + 24, desc_add(v, vo), desc_add(v, vo + 2048),
              desc_add(v, vo + 4096), desc_add(v, vo + 6144), idesc, g4 > 0 ? 1u : acc_first);
   }
@@ -955,43 +959,55 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // prefill_tc2_kernel: two query tiles per CTA in ping-pong.
 //
 // A CTA owns 256 query rows as two 128-row tiles of the same (sequence, kv head):
-// softmax warpgroup t (warps 4t .. 4t+3) owns tile t, and while one warpgroup works on
-// its scores the tensor core works on the other tile; every K/V block staged feeds 256
-// rows.  Each tile has one S buffer in TMEM.
-//  * head_dim 64: one P buffer per tile in shared memory.  The tensor-core thread issues
-//    S_0(j+1), PV_0(j), S_1(j+1), PV_1(j): S_t(j+1) goes out once P_t(j) is complete
-//    (p_full), ahead of PV_t(j), and the softmax waits for PV_t(j) (pv_done) before it
-//    rescales O_t or overwrites P_t.  K and V rings of 3.
-//  * head_dim 128: P_t(j) is written into TMEM over the upper half of S_t(j), and the
-//    tensor-core thread issues PV_0(j), S_0(j+1), PV_1(j), S_1(j+1): the MMAs of one
-//    thread run in issue order, so S_t(j+1) overwrites the buffer only after PV_t(j) has
-//    read it, and s_full(t) (which tracks every MMA issued before it) tells the softmax
-//    that O_t is stable.  K and V rings of 2, each filled by its own producer warp.
+// softmax warps of tile t own its rows, and while one tile's warps work on its scores
+// the tensor core works on the other tile; every K/V block staged feeds 256 rows.  Each
+// tile has one S buffer in TMEM.
+//  * P in TMEM (the default at both head dims): P_t(j) is written into TMEM over
+//    columns of S_t(j) that the softmax has read, and the tensor-core thread issues
+//    PV_0(j), S_0(j+1), PV_1(j), S_1(j+1): the MMAs of one thread run in issue order, so
+//    S_t(j+1) overwrites the buffer only after PV_t(j) has read it, and s_full(t) (which
+//    tracks every MMA issued before it) tells the softmax that O_t is stable.  K and V
+//    rings of 2 at head_dim 128, each filled by its own producer warp; of 3 at 64, one
+//    producer for both.
+//  * P in shared memory (build options): one P buffer per tile.  The tensor-core thread
+//    issues S_0(j+1), PV_0(j), S_1(j+1), PV_1(j): S_t(j+1) goes out once P_t(j) is
+//    complete (p_full), ahead of PV_t(j), and the softmax waits for PV_t(j) (pv_done)
+//    before it rescales O_t or overwrites P_t.
 // Row arithmetic (positions, masking, lazy rescale, bf16 row sums) is the one-tile
-// kernel's.  H softmax threads per query row: with H = 2, two warps share each 32-row
-// lane quadrant, one taking the first 64 columns of every key block, the other the last
-// 64; their row maxima and row sums are combined through shared memory.  Warps 0 .. 8H-1
-// are the two tiles' softmax warps (tile t: warps 8H/2 t .. ), then the producer, the
-// MMA warp and (head_dim 128) the V producer.
+// kernel's.  H softmax threads per query row (2 at head_dim 128, 1 at 64): with H = 2,
+// two warps share each 32-row lane quadrant, one taking the first 64 columns of every
+// key block, the other the last 64; their row maxima and row sums are combined through
+// shared memory.  Warps 0 .. 8H-1 are the two tiles' softmax warps (tile t: warps
+// 4H t .. 4H t + 4H - 1), then the producer, the MMA warp and (head_dim 128) the V
+// producer.
 // Producer warps of the two-tile kernel: at head_dim 128 one for the K ring and one for
 // the V ring (a block's sixteen 2 KB boxes take a warp ~1800 cycles to issue at
 // block_size 16, as long as the block's tensor-core work: measured +1.3%); at head_dim
-// 64 one for both (measured 1% faster than two).
+// 64 one for both (two, and rings of 4, measured within 1%: the softmax sets the pace).
 #ifndef PKV_PREFILL_TWO_PRODUCERS128
 #define PKV_PREFILL_TWO_PRODUCERS128 1
 #endif
+#ifndef PKV_PREFILL_TWO_PRODUCERS64
+#define PKV_PREFILL_TWO_PRODUCERS64 0
+#endif
+// K and V ring stages of the two-tile kernel at head_dim 64.
+#ifndef PKV_PREFILL_KS64
+#define PKV_PREFILL_KS64 3
+#endif
 template <int D>
-__host__ __device__ constexpr int tc2_producers() { return D == 128 && PKV_PREFILL_TWO_PRODUCERS128 ? 2 : 1; }
+__host__ __device__ constexpr int tc2_producers() {
+  return (D == 128 ? PKV_PREFILL_TWO_PRODUCERS128 : PKV_PREFILL_TWO_PRODUCERS64) ? 2 : 1;
+}
 template <int D, int H>
 __host__ __device__ constexpr int tc2_threads() { return 32 * (8 * H + 1 + tc2_producers<D>()); }
 
 template <int D, int H>
 struct Tc2Smem {
   // P in TMEM (no P buffers in shared memory)
-  static constexpr bool kPT = H == 1 && row_once<D>() &&
+  static constexpr bool kPT = row_once<D>() &&
                               (D == 128 ? PKV_PREFILL_P_TMEM != 0 : PKV_PREFILL_P_TMEM64 != 0);
-  static constexpr int KSK = D == 64 ? 3 : (kPT ? PKV_PREFILL_KSK128 : 2);  // stages of the K ring
-  static constexpr int KSV = D == 64 ? 3 : (kPT ? PKV_PREFILL_KSV128 : 1);  // stages of the V ring
+  static constexpr int KSK = D == 64 ? PKV_PREFILL_KS64 : (kPT ? PKV_PREFILL_KSK128 : 2);  // K ring stages
+  static constexpr int KSV = D == 64 ? PKV_PREFILL_KS64 : (kPT ? PKV_PREFILL_KSV128 : 1);  // V ring stages
   static constexpr uint32_t kSub = kTcKeys * 128;    // 128 rows x 128 B (64 dims)
   static constexpr uint32_t kTile = kSub * (D / 64); // one K or V block / one Q tile
   static constexpr uint32_t k = 0;
@@ -1003,7 +1019,7 @@ struct Tc2Smem {
   static constexpr uint32_t xchg = p + (kPT ? 0 : 2 * kP);
   // kOnes: a [128 keys][64] bf16 tile of ones, read by P.V as 16 extra B columns, so that
   // the tensor core also forms each row's sum of the bf16 weights (in O's extra columns)
-  static constexpr bool kOnes = D == 64 && H == 1 && PKV_PREFILL_SUM_MMA64 != 0;
+  static constexpr bool kOnes = D == 64 && PKV_PREFILL_SUM_MMA64 != 0;
   static constexpr uint32_t ones = (xchg + (H == 2 ? 2 * 2 * 2 * kTcRows * 4 : 0) + 1023u) & ~1023u;
   static constexpr uint32_t bars = ones + (kOnes ? kSub : 0);
   // the rings, s_full/p_full/pv_done per tile, q_ready, mma_done, with H = 2 one
@@ -1027,7 +1043,11 @@ __global__ void __launch_bounds__(tc2_threads<D, H>(), 1)
   constexpr int NCH = kTcKeys / 32 / H;    // 32-column chunks of a block per thread
   constexpr bool kOnes = SL::kOnes;        // row sums from the tensor core
   constexpr int kON = D + (kOnes ? 16 : 0);  // O columns per tile (then the row sums)
-  constexpr bool kPT = SL::kPT;           // P in TMEM, over the upper half of S_t
+  constexpr bool kPT = SL::kPT;           // P in TMEM, over S_t
+  // P_t's columns within S_t: one thread a row reads the whole row before it writes,
+  // so P takes the upper 64 columns (keys 0-63 then 64-127); with two threads a row,
+  // each half writes its 32 columns of P over the first 32 of the 64 it has read
+  constexpr uint32_t kPCol = H == 1 ? 64u : 0u, kPGroup = H == 1 ? 32u : 64u;
   constexpr bool kOnePass = kPT && PKV_PREFILL_ONE_PASS != 0;
   constexpr bool kEarlyS = !kPT && PKV_PREFILL_EARLY_S != 0 && row_once<D>();
   extern __shared__ uint8_t smem_raw[];
@@ -1213,8 +1233,8 @@ __global__ void __launch_bounds__(tc2_threads<D, H>(), 1)
             dev::tc_fence_after();
           }
           if constexpr (kPT) {
-            issue_pv_ts(tmem + 256u + (uint32_t)(kON * t), tmem + 128u * t + 64u, dv(j % KSV), id_o,
-                        j > 0 ? 1u : 0u);
+            issue_pv_ts(tmem + 256u + (uint32_t)(kON * t), tmem + 128u * t + kPCol, dv(j % KSV),
+                        id_o, j > 0 ? 1u : 0u, kPGroup);
             dev::umma_commit(pv_done(t));
             // V_j is free once the last tile that reads it has its P.V
             if (t == 1 || j >= nblk_of(1)) dev::umma_commit(v_empty(j % KSV));
@@ -1307,8 +1327,11 @@ __global__ void __launch_bounds__(tc2_threads<D, H>(), 1)
       } else {
         hmax = row_block_max<NCH>(sb, hc * NCH, lim, whole, pos_scale, a.scale_log2);
       }
-      const float bmax = fmaxf(hmax, other_half(hmax, j, ok));
-      if (!ok) break;
+      float bmax = hmax;
+      if (!one_pass) {  // with one_pass the halves exchange their maxima after the weights
+        bmax = fmaxf(hmax, other_half(hmax, j, ok));
+        if (!ok) break;
+      }
       // Lazy rescaling: the reference max moves only when the block raises it by more
       // than kTcRescale; then O_t (and its row-sum column) and the row sum scale by f.
       float f = 1.f;
@@ -1336,24 +1359,30 @@ __global__ void __launch_bounds__(tc2_threads<D, H>(), 1)
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
           dev::tmem_st32(ob + ch * 32, o);
         }
-        if constexpr (kOnes) {  // the row sum in O's column D
-          const uint32_t sm = tmem_ld1(ob + D);
-          dev::tmem_wait_ld();
-          tmem_st1(ob + D, __float_as_uint(__uint_as_float(sm) * f));
+        if constexpr (kOnes) {  // the row sum in O's column D (the first half's)
+          if (hc == 0) {
+            const uint32_t sm = tmem_ld1(ob + D);
+            dev::tmem_wait_ld();
+            tmem_st1(ob + D, __float_as_uint(__uint_as_float(sm) * f));
+          }
         }
         dev::tmem_wait_st();
         lsum *= f;
       };
       if constexpr (kPT) {
-        // P_t(j) into TMEM over the upper half of S_t.  PV_t(j-1) was issued before S_t(j)
-        // by the same thread, and s_full tracks every MMA issued before its commit, so
-        // O_t is stable here.
+        // P_t(j) into TMEM over S_t, in columns this thread has read.  PV_t(j-1) was
+        // issued before S_t(j) by the same thread, and s_full tracks every MMA issued
+        // before its commit, so O_t is stable here.
         uint32_t pk[NCH * 16];
         float ls;
         if (one_pass) {
           float bm;
-          ls = row_regs_exp_pk_max<NCH, !kOnes>(xrow, 0, lim, whole, pos_scale, a.scale_log2,
-                                                m_ref, pk, &bm);
+          ls = row_regs_exp_pk_max<NCH, !kOnes>(xrow, hc * NCH, lim, whole, pos_scale,
+                                                a.scale_log2, m_ref, pk, &bm);
+          if constexpr (H == 2) {
+            bm = fmaxf(bm, other_half(bm, j, ok));
+            if (!ok) break;
+          }
           const bool need = bm > m_ref + kTcRescale;
           resc = __any_sync(0xffffffffu, need);
           if (resc) {  // the reference moves: the weights again, against the new one, from
@@ -1362,15 +1391,18 @@ __global__ void __launch_bounds__(tc2_threads<D, H>(), 1)
             f = need ? dev::ex2(m_ref - m_new) : 1.f;
             if (need) m_ref = m_new;
             row_block_load<NCH>(sb, hc * NCH, xrow);
-            ls = row_regs_exp_pk<NCH, !kOnes>(xrow, 0, lim, whole, a.scale_log2, m_ref, pk);
+            ls = row_regs_exp_pk<NCH, !kOnes>(xrow, hc * NCH, lim, whole, a.scale_log2, m_ref,
+                                              pk);
           }
         } else {
-          ls = row_regs_exp_pk<NCH, !kOnes>(xrow, 0, lim, whole, a.scale_log2, m_ref, pk);
+          ls = row_regs_exp_pk<NCH, !kOnes>(xrow, hc * NCH, lim, whole, a.scale_log2, m_ref, pk);
         }
         if (resc) rescale_o();
         lsum += ls;
-        dev::tmem_st32(sb + 64u, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        dev::tmem_st32(sb + 96u, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+#pragma unroll
+        for (int i = 0; i < NCH / 2; ++i)
+          dev::tmem_st32(sb + kPCol + kPGroup * hc + 32u * i,
+                         *reinterpret_cast<uint32_t(*)[32]>(&pk[32 * i]));
         dev::tmem_wait_st();
       } else if constexpr (kEarlyS) {
         // the block's weights first, kept in registers; then, once PV_t(j-1) has
@@ -1468,13 +1500,17 @@ cudaError_t read_prefill_errors(uint32_t *flags, int clear) { return read_tu_err
 
 constexpr size_t tc_smem(int d) { return 1024 + (d == 64 ? TcSmem<64>::total : TcSmem<128>::total); }
 static_assert(tc_smem(64) <= 227 * 1024 && tc_smem(128) <= 227 * 1024, "prefill tile fits a CTA");
-// Softmax threads per query row of the two-tile kernel, by head_dim.  Two at head_dim 64
-// (where the softmax bounds the kernel) measured within a few percent of one (+3.5% on a
-// 256-sequence batch, -1% on 16 long sequences), so one is kept at both.
+// Softmax threads per query row of the two-tile kernel, by head_dim.  At head_dim 128 two
+// (16 softmax warps, 96 registers a thread, each half of a row in its own warp) measured
+// 1% faster than one.  At 64 one: with P in TMEM two ran 4-5% slower (the kernel is held
+// to 96 registers there and spills).
 #ifndef PKV_PREFILL_HALVES64
 #define PKV_PREFILL_HALVES64 1
 #endif
-constexpr int tc2_halves(int d) { return d == 64 ? PKV_PREFILL_HALVES64 : 1; }
+#ifndef PKV_PREFILL_HALVES128
+#define PKV_PREFILL_HALVES128 2
+#endif
+constexpr int tc2_halves(int d) { return d == 64 ? PKV_PREFILL_HALVES64 : PKV_PREFILL_HALVES128; }
 constexpr size_t tc2_smem(int d) {
   return 1024 + (d == 64 ? Tc2Smem<64, tc2_halves(64)>::total : Tc2Smem<128, tc2_halves(128)>::total);
 }
