@@ -58,7 +58,8 @@ struct PrefillArgs {
 // One CTA owns one (sequence, kv head, tile of 128 query rows) and walks the keys up to
 // the tile's last position in blocks of 128.  Warps 0-3 run the softmax with one thread
 // per row, warps 4 and 6 are the TMA producers (K and V), and one thread of warp 5
-// issues the tensor-core instructions:
+// issues the tensor-core instructions (with the build option of two softmax threads per
+// row: warps 0-7, 8 and 10, and 9):
 //   S_j = Q . K_j^T   tcgen05.mma M=128 N=128 K=D, Q and K_j K-major in shared memory
 //                     (128-byte swizzle), S in TMEM, two buffers: S_{j+1} is computed
 //                     while the softmax works on S_j;
@@ -74,24 +75,34 @@ struct PrefillArgs {
 // separate rings so that K runs a block ahead of V.
 constexpr int kTcRows = 128;     // query rows per CTA
 constexpr int kTcKeys = 128;     // keys per block
-// One-tile kernel: softmax warps 0-3, producer warp 4 (the K ring, and the V ring unless
-// warp 6 fills it), MMA warp 5.  One warp takes ~110 cycles per TMA box, so at block_size
-// 32 a block's sixteen boxes took longer than its tensor-core work; with a second
-// producer workload 5 went from 818 to 967 TFLOP/s.
+// One-tile kernel: softmax warps 0 .. 4H-1 (H threads per query row), producer warp 4H
+// (the K ring, and the V ring unless warp 4H+2 fills it), MMA warp 4H+1.  One warp takes
+// ~110 cycles per TMA box, so at block_size 32 a block's sixteen boxes took longer than
+// its tensor-core work; with a second producer workload 5 went from 818 to 967 TFLOP/s.
 #ifndef PKV_PREFILL_TC_TWO_PRODUCERS
 #define PKV_PREFILL_TC_TWO_PRODUCERS 1
 #endif
 // One-tile kernel at head_dim 128: P in TMEM, two buffers at columns 256 + D and
 // 320 + D (after O), read by P.V as its A operand (1), or in shared memory (0); and then
-// the stages of the K and V rings.
+// the stages of the K and V rings: 2 (with the one-pass softmax, rings of 3 measured 8%
+// slower on 4 sequences of 32K at block_size 32 and 64, 1% at 16).
 #ifndef PKV_PREFILL_TC_P_TMEM
 #define PKV_PREFILL_TC_P_TMEM 1
 #endif
 #ifndef PKV_PREFILL_TC_KS128
-#define PKV_PREFILL_TC_KS128 3
+#define PKV_PREFILL_TC_KS128 2
+#endif
+// One-tile kernel at head_dim 128 (P in TMEM): softmax threads per query row (two
+// measured 2% below one, with rings of 2), and with two the stages of the V ring.
+#ifndef PKV_PREFILL_TC_HALVES128
+#define PKV_PREFILL_TC_HALVES128 1
+#endif
+#ifndef PKV_PREFILL_TC_KSV128_H2
+#define PKV_PREFILL_TC_KSV128_H2 2
 #endif
 constexpr int kTcProducers = PKV_PREFILL_TC_TWO_PRODUCERS ? 2 : 1;
-constexpr int kTcThreads = 32 * (5 + kTcProducers);
+template <int H>
+__host__ __device__ constexpr int tc_threads() { return 32 * (4 * H + 1 + kTcProducers); }
 constexpr float kTcRescale = 8.f;
 
 // Whether the softmax reads a row's block from TMEM once into registers (1) or in each
@@ -107,20 +118,26 @@ constexpr float kTcRescale = 8.f;
 template <int D>
 __host__ __device__ constexpr bool row_once() { return D == 128 ? PKV_PREFILL_ROW_ONCE128 != 0 : PKV_PREFILL_ROW_ONCE64 != 0; }
 
-template <int D>
+template <int D, int H = 1>
 struct TcSmem {
   // head_dim 128: P in TMEM (two 64-column buffers after O), no P buffers here
   static constexpr bool kPT = D == 128 && row_once<D>() && PKV_PREFILL_TC_P_TMEM != 0;
-  static constexpr int KS = D == 64 ? 3 : (kPT ? PKV_PREFILL_TC_KS128 : 2);  // stages of each ring
+  static_assert(H == 1 || kPT, "two threads per row only with P in TMEM");
+  static constexpr int KSK = D == 64 ? 3 : (kPT ? PKV_PREFILL_TC_KS128 : 2);  // K ring stages
+  static constexpr int KSV = H == 2 ? PKV_PREFILL_TC_KSV128_H2 : KSK;         // V ring stages
   static constexpr uint32_t kSub = kTcKeys * 128;      // one 64-dim sub-tile of 128 rows
   static constexpr uint32_t kTile = kSub * (D / 64);   // one K or V block / the Q tile
   static constexpr uint32_t k = 0;
-  static constexpr uint32_t v = k + KS * kTile;
-  static constexpr uint32_t q = v + KS * kTile;        // [D/64][128 rows][128 B]
+  static constexpr uint32_t v = k + KSK * kTile;
+  static constexpr uint32_t q = v + KSV * kTile;       // [D/64][128 rows][128 B]
   static constexpr uint32_t p = q + kTile;             // two buffers of [2][128 rows][128 B]
   static constexpr uint32_t kP = 2 * kSub;
-  static constexpr uint32_t bars = p + (kPT ? 0 : 2 * kP);
-  static constexpr int kBars = 4 * KS + 10;
+  // H = 2: the halves' row values, [2 buffers][2 halves][128 rows] fp32
+  static constexpr uint32_t xchg = p + (kPT ? 0 : 2 * kP);
+  static constexpr uint32_t bars = xchg + (H == 2 ? 2 * 2 * kTcRows * 4 : 0);
+  // the rings, s_full/s_free/p_full/pv_done per buffer, q_ready, mma_done, and with
+  // H = 2 one barrier per lane quadrant where the two halves of its rows meet
+  static constexpr int kBars = 2 * KSK + 2 * KSV + 10 + (H == 2 ? 4 : 0);
   static constexpr uint32_t tslot = bars + kBars * 8;
   static constexpr uint32_t flag = tslot + 8;
   static constexpr uint32_t total = flag + 8;
@@ -657,29 +674,35 @@ __device__ __forceinline__ void issue_pv_ts(uint32_t d_tmem, uint32_t p_tmem, ui
   }
 }
 
-template <int D>
-__global__ void __launch_bounds__(kTcThreads, 1)
+template <int D, int H>
+__global__ void __launch_bounds__(tc_threads<H>(), 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv, const PrefillArgs a) {
-  using SL = TcSmem<D>;
-  constexpr int KS = SL::KS;
+  using SL = TcSmem<D, H>;
+  constexpr int KSK = SL::KSK, KSV = SL::KSV;
+  constexpr int kSoftWarps = 4 * H;
+  constexpr int kProducer = kSoftWarps, kMma = kSoftWarps + 1, kProducerV = kSoftWarps + 2;
+  constexpr int NCH = kTcKeys / 32 / H;  // 32-column chunks of a block per thread
+  constexpr bool kOnePass = SL::kPT && PKV_PREFILL_ONE_PASS != 0;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = dev::smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *const bp = smem_raw + (base - raw);
   const uint32_t bars = base + SL::bars;
+  constexpr int R4 = 2 * KSK + 2 * KSV;  // barriers of the two rings
   auto k_full = [&](int s) { return bars + 8u * s; };
-  auto k_empty = [&](int s) { return bars + 8u * (KS + s); };
-  auto v_full = [&](int s) { return bars + 8u * (2 * KS + s); };
-  auto v_empty = [&](int s) { return bars + 8u * (3 * KS + s); };
+  auto k_empty = [&](int s) { return bars + 8u * (KSK + s); };
+  auto v_full = [&](int s) { return bars + 8u * (2 * KSK + s); };
+  auto v_empty = [&](int s) { return bars + 8u * (2 * KSK + KSV + s); };
   // two of each of these, one per S (and P) buffer, so that no barrier can run two
   // phases ahead of its waiter
-  auto s_full = [&](int i) { return bars + 8u * (4 * KS + i); };
-  auto s_free = [&](int i) { return bars + 8u * (4 * KS + 2 + i); };
-  auto p_full = [&](int i) { return bars + 8u * (4 * KS + 4 + i); };
-  auto pv_done = [&](int i) { return bars + 8u * (4 * KS + 6 + i); };
-  const uint32_t q_ready = bars + 8u * (4 * KS + 8);
-  const uint32_t mma_done = bars + 8u * (4 * KS + 9);
+  auto s_full = [&](int i) { return bars + 8u * (R4 + i); };
+  auto s_free = [&](int i) { return bars + 8u * (R4 + 2 + i); };
+  auto p_full = [&](int i) { return bars + 8u * (R4 + 4 + i); };
+  auto pv_done = [&](int i) { return bars + 8u * (R4 + 6 + i); };
+  const uint32_t q_ready = bars + 8u * (R4 + 8);
+  const uint32_t mma_done = bars + 8u * (R4 + 9);
+  auto pair_bar = [&](int wq) { return bars + 8u * (R4 + 10 + wq); };
   volatile uint32_t *const s_tmem = reinterpret_cast<volatile uint32_t *>(bp + SL::tslot);
   volatile int *const s_flag = reinterpret_cast<volatile int *>(bp + SL::flag);
 
@@ -707,12 +730,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (tid == 0) {
     // one arrival each (the producer, or a tensor-core commit), except s_free, p_full and
-    // q_ready: one arrival per softmax warp
+    // q_ready: one arrival per softmax warp; and the pair barriers: every thread of the
+    // two warps that share a lane quadrant
     for (int i = 0; i < SL::kBars; ++i) {
       const uint32_t bar = bars + 8u * i;
       const bool per_warp = bar == s_free(0) || bar == s_free(1) || bar == p_full(0) ||
                             bar == p_full(1) || bar == q_ready;
-      dev::mbar_init(bar, per_warp ? 4u : 1u);
+      dev::mbar_init(bar, i >= R4 + 10 ? 64u : per_warp ? (uint32_t)kSoftWarps : 1u);
     }
     *s_flag = 0;
     dev::fence_mbar_init();
@@ -732,9 +756,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   };
   int k_issued = 0, v_issued = 0;  // producer: blocks loaded into each ring
 
-  if (warp == 4 || (kTcProducers == 2 && warp == 6)) {
+  if (warp == kProducer || (kTcProducers == 2 && warp == kProducerV)) {
     // ---------------------------------------------------------- producer warp(s)
-    const bool do_k = warp == 4, do_v = kTcProducers == 1 || warp == 6;
+    const bool do_k = warp == kProducer, do_v = kTcProducers == 1 || warp == kProducerV;
     // every query tile of this (sequence, kv head) reads the same blocks: keep them in L2
     const uint64_t policy = dev::policy_evict_last();
     const int32_t *trow = a.block_tables + (int64_t)b * a.max_blocks;
@@ -744,8 +768,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int vtb = ktb;
     for (int j = 0; j <= nblk; ++j) {  // K runs one block ahead of V
       if (do_k && j < nblk) {
-        const int s = j % KS;
-        if (j >= KS && !__all_sync(0xffffffffu, dev::mbar_wait(k_empty(s), ((j / KS) - 1) & 1))) {
+        const int s = j % KSK;
+        if (j >= KSK && !__all_sync(0xffffffffu, dev::mbar_wait(k_empty(s), ((j / KSK) - 1) & 1))) {
           if (lane == 0) fail(false);
           break;
         }
@@ -755,8 +779,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         k_issued = j + 1;
       }
       if (do_v && j >= 1) {
-        const int jv = j - 1, s = jv % KS;
-        if (jv >= KS && !__all_sync(0xffffffffu, dev::mbar_wait(v_empty(s), ((jv / KS) - 1) & 1))) {
+        const int jv = j - 1, s = jv % KSV;
+        if (jv >= KSV && !__all_sync(0xffffffffu, dev::mbar_wait(v_empty(s), ((jv / KSV) - 1) & 1))) {
           if (lane == 0) fail(false);
           break;
         }
@@ -766,7 +790,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         v_issued = jv + 1;
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMma) {
     // ------------------------------------------------- tensor-core issue (one thread)
     if (lane == 0) {
       constexpr uint32_t id_s = dev::idesc_bf16_f32(kTcRows, kTcKeys, 0);
@@ -779,8 +803,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint64_t dp0 = dev::smem_desc(base + SL::p, 16, 1024);
       bool ok = fail(dev::mbar_wait(q_ready, 0));
       auto issue_s = [&](int j) {
-        const int s = j % KS;
-        if (!fail(dev::mbar_wait(k_full(s), (j / KS) & 1))) return false;
+        const int s = j % KSK;
+        if (!fail(dev::mbar_wait(k_full(s), (j / KSK) & 1))) return false;
         if (j >= 2 && !fail(dev::mbar_wait(s_free(j & 1), ((j >> 1) - 1) & 1))) return false;
         dev::tc_fence_after();
         issue_qk<D>(tmem + 128u * (j & 1), dq, desc_add(dk0, s * SL::kTile), SL::kSub, id_s);
@@ -791,9 +815,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (ok) ok = issue_s(0);
       for (int j = 0; ok && j < nblk; ++j) {
         if (j + 1 < nblk && !(ok = issue_s(j + 1))) break;
-        const int s = j % KS;
+        const int s = j % KSV;
         if (!(ok = fail(dev::mbar_wait(p_full(j & 1), (j >> 1) & 1)))) break;
-        if (!(ok = fail(dev::mbar_wait(v_full(s), (j / KS) & 1)))) break;
+        if (!(ok = fail(dev::mbar_wait(v_full(s), (j / KSV) & 1)))) break;
         dev::tc_fence_after();
         if constexpr (SL::kPT)
           issue_pv_ts(tmem + 256u, tmem + 256u + D + 64u * (j & 1), desc_add(dv0, s * SL::kTile),
@@ -807,20 +831,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       dev::umma_commit(mma_done);  // arrives once everything issued above has completed
     }
   } else {
-    // ------------------------------------------------------ softmax warps (row = tid)
-    const int r = tid;
+    // ---------------------------------------- softmax warps: row r, half hc of each block
+    const int wq = warp & 3;    // TMEM lane quadrant of this warp
+    const int hc = warp >> 2;   // which H-th of the columns
+    const int r = 32 * wq + lane;
     const int gr = row0 + r;
     const bool valid = gr < rows;
     const int qi = valid ? gr / G : last_row / G;
     const int h = valid ? gr - (gr / G) * G : 0;
     const int pos = L - n + qi;                    // keys t <= pos are seen
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-    // the tile's query rows into shared memory (K-major, 128-byte swizzle); zeros past the end
+    const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
+    // The two halves of a row exchange a value through shared memory: exchange k writes
+    // buffer k & 1 and arrives on the quadrant's pair barrier (every thread of both
+    // warps), whose phase k then publishes both values.  A half is at most one phase ahead
+    // of the other, so it never overwrites a buffer its partner has yet to read.  The wait
+    // is bounded; if it gives up, the row keeps its own value and the error is raised.
+    float *const xchg = reinterpret_cast<float *>(bp + SL::xchg);  // [buf][half][row]
+    int xuse = 0;
+    auto other_half = [&](float v, bool &good) -> float {
+      if constexpr (H == 2) {
+        const int use = xuse++;
+        xchg[((use & 1) * 2 + hc) * kTcRows + r] = v;
+        dev::mbar_arrive(pair_bar(wq));
+        if (!__all_sync(0xffffffffu, dev::mbar_wait(pair_bar(wq), use & 1))) {
+          good = false;
+          return v;
+        }
+        return xchg[((use & 1) * 2 + (hc ^ 1)) * kTcRows + r];
+      } else {
+        return v;
+      }
+    };
+    // the tile's query rows into shared memory (K-major, 128-byte swizzle); zeros past the
+    // end; this half's chunks [hc D/8/H, (hc+1) D/8/H)
     {
       const uint4 *src = reinterpret_cast<const uint4 *>(
           a.q + ((int64_t)(q0 + qi) * a.num_q_heads + g * G + h) * D);
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
+      for (int cc = 0; cc < D / 8 / H; ++cc) {
+        const int c = hc * (D / 8 / H) + cc;
         const uint4 v = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
         *reinterpret_cast<uint4 *>(bp + SL::q + (c >> 3) * SL::kSub + r * 128 +
                                    (((c & 7) ^ (r & 7)) << 4)) = v;
@@ -838,70 +887,104 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int lim = min(pos, t_end - 1) - k0;  // columns c <= lim are seen by this row
       if (!(ok = __all_sync(0xffffffffu, dev::mbar_wait(s_full(j & 1), (j >> 1) & 1)))) break;
       dev::tc_fence_after();
-      // S row of this block: four chunks of 32 columns, read from TMEM in each pass
+      // this thread's part of the S row: NCH chunks of 32 columns
       const uint32_t sbase = tmem + lane_base + 128u * (j & 1);
+      // the same for both halves of a row: its rows and the block are the same
       const bool whole = __all_sync(0xffffffffu, lim >= kTcKeys - 1);  // no column masked
-      // pass 1: the block's row max
-      uint32_t xrow[row_once<D>() ? kTcKeys : 1];
-      float bmax;
+      uint32_t xrow[row_once<D>() ? NCH * 32 : 1];
+      const bool one_pass = kOnePass && j > 0;  // the max comes with the weights below
+      float hmax = -INFINITY;
       if constexpr (row_once<D>()) {
-        row_block_load<kTcKeys / 32>(sbase, 0, xrow);
-        bmax = row_regs_max<kTcKeys / 32>(xrow, 0, lim, whole, pos_scale, a.scale_log2);
+        row_block_load<NCH>(sbase, hc * NCH, xrow);
+        if (!one_pass) hmax = row_regs_max<NCH>(xrow, hc * NCH, lim, whole, pos_scale, a.scale_log2);
       } else {
-        bmax = row_block_max<kTcKeys / 32>(sbase, 0, lim, whole, pos_scale, a.scale_log2);
+        hmax = row_block_max<NCH>(sbase, hc * NCH, lim, whole, pos_scale, a.scale_log2);
       }
-      if (j > 0) {
-        const bool need = bmax > m_ref + kTcRescale;
-        if (__any_sync(0xffffffffu, need)) {  // O moves: wait until the previous P.V is in
-          if (!(ok = __all_sync(0xffffffffu,
-                                dev::mbar_wait(pv_done((j - 1) & 1), ((j - 1) >> 1) & 1))))
-            break;
-          dev::tc_fence_after();
-          const float m_new = fmaxf(m_ref, bmax);
-          const float f = need ? dev::ex2(m_ref - m_new) : 1.f;
+      // O_t moves by f (and the row sum with it) once the previous P.V is in
+      auto rescale_o = [&](float f) {
+        if (!__all_sync(0xffffffffu, dev::mbar_wait(pv_done((j - 1) & 1), ((j - 1) >> 1) & 1)))
+          return false;
+        dev::tc_fence_after();
 #pragma unroll 1
-          for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t o[32];
-            dev::tmem_ld32(tmem + lane_base + 256u + ch * 32, o);
-            dev::tmem_wait_ld();
+        for (int ch = hc * (D / 32 / H); ch < (hc + 1) * (D / 32 / H); ++ch) {
+          uint32_t o[32];
+          dev::tmem_ld32(tmem + lane_base + 256u + ch * 32, o);
+          dev::tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-            dev::tmem_st32(tmem + lane_base + 256u + ch * 32, o);
-          }
-          dev::tmem_wait_st();
-          lsum *= f;
-          if (need) m_ref = m_new;
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+          dev::tmem_st32(tmem + lane_base + 256u + ch * 32, o);
         }
-      } else {
-        m_ref = bmax;  // block 0 holds key 0, which every row sees
-      }
-      // this P buffer is free once the P.V of two blocks back has completed
-      if (j >= 2 && !(ok = __all_sync(0xffffffffu,
-                                      dev::mbar_wait(pv_done(j & 1), ((j - 2) >> 1) & 1))))
-        break;
-      // pass 2: P = exp2(S - m_ref) as bf16 into shared memory (or TMEM), and its row sum
-      if constexpr (SL::kPT) {
-        uint32_t pk[kTcKeys / 2];
-        lsum += row_regs_exp_pk<kTcKeys / 32>(xrow, 0, lim, whole, a.scale_log2, m_ref, pk);
-        const uint32_t pb = tmem + lane_base + 256u + D + 64u * (j & 1);
-        dev::tmem_st32(pb, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        dev::tmem_st32(pb + 32u, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
         dev::tmem_wait_st();
-      } else if constexpr (row_once<D>())
-        lsum += row_regs_exp<kTcKeys / 32>(xrow, 0, bp, SL::p + (j & 1) * SL::kP + r * 128, SL::kSub,
-                                           r, lim, whole, a.scale_log2, m_ref);
-      else
-        lsum += row_block_exp<kTcKeys / 32>(sbase, 0, bp, SL::p + (j & 1) * SL::kP + r * 128,
-                                            SL::kSub, r, lim, whole, a.scale_log2, m_ref);
+        lsum *= f;
+        return true;
+      };
+      if (!one_pass) {
+        const float bmax = fmaxf(hmax, other_half(hmax, ok));
+        if (!ok) break;
+        if (j > 0) {
+          const bool need = bmax > m_ref + kTcRescale;
+          if (__any_sync(0xffffffffu, need)) {
+            const float m_new = fmaxf(m_ref, bmax);
+            if (!(ok = rescale_o(need ? dev::ex2(m_ref - m_new) : 1.f))) break;
+            if (need) m_ref = m_new;
+          }
+        } else {
+          m_ref = bmax;  // block 0 holds key 0, which every row sees
+        }
+      }
+      // P = exp2(S - m_ref) as bf16 into TMEM (or shared memory), and its row sum
+      if constexpr (SL::kPT) {
+        uint32_t pk[NCH * 16];
+        float ls;
+        if (one_pass) {
+          float bm;
+          ls = row_regs_exp_pk_max<NCH>(xrow, hc * NCH, lim, whole, pos_scale, a.scale_log2,
+                                        m_ref, pk, &bm);
+          bm = fmaxf(bm, other_half(bm, ok));
+          if (!ok) break;
+          const bool need = bm > m_ref + kTcRescale;
+          if (__any_sync(0xffffffffu, need)) {  // the reference moves: the weights again,
+                                                // from S_j read once more
+            const float m_new = fmaxf(m_ref, bm);
+            if (!(ok = rescale_o(need ? dev::ex2(m_ref - m_new) : 1.f))) break;
+            if (need) m_ref = m_new;
+            row_block_load<NCH>(sbase, hc * NCH, xrow);
+            ls = row_regs_exp_pk<NCH>(xrow, hc * NCH, lim, whole, a.scale_log2, m_ref, pk);
+          }
+        } else {
+          ls = row_regs_exp_pk<NCH>(xrow, hc * NCH, lim, whole, a.scale_log2, m_ref, pk);
+        }
+        lsum += ls;
+        // this P buffer is free once the P.V of two blocks back has completed
+        if (j >= 2 && !(ok = __all_sync(0xffffffffu,
+                                        dev::mbar_wait(pv_done(j & 1), ((j - 2) >> 1) & 1))))
+          break;
+        const uint32_t pb = tmem + lane_base + 256u + D + 64u * (j & 1) + 32u * (hc * NCH / 2);
+#pragma unroll
+        for (int i = 0; i < NCH / 2; ++i)
+          dev::tmem_st32(pb + 32u * i, *reinterpret_cast<uint32_t(*)[32]>(&pk[32 * i]));
+        dev::tmem_wait_st();
+      } else {
+        // this P buffer is free once the P.V of two blocks back has completed
+        if (j >= 2 && !(ok = __all_sync(0xffffffffu,
+                                        dev::mbar_wait(pv_done(j & 1), ((j - 2) >> 1) & 1))))
+          break;
+        if constexpr (row_once<D>())
+          lsum += row_regs_exp<kTcKeys / 32>(xrow, 0, bp, SL::p + (j & 1) * SL::kP + r * 128,
+                                             SL::kSub, r, lim, whole, a.scale_log2, m_ref);
+        else
+          lsum += row_block_exp<kTcKeys / 32>(sbase, 0, bp, SL::p + (j & 1) * SL::kP + r * 128,
+                                              SL::kSub, r, lim, whole, a.scale_log2, m_ref);
+      }
       // S read: the MMA warp may refill this buffer
       dev::tc_fence_before();
       __syncwarp();
       if (lane == 0) dev::mbar_arrive(s_free(j & 1));
       if (nk < kTcKeys) {  // last block: V rows past the keys hold stale or unowned data
-        const int s = j % KS;
-        if (!(ok = __all_sync(0xffffffffu, dev::mbar_wait(v_full(s), (j / KS) & 1)))) break;
+        const int s = j % KSV;
+        if (!(ok = __all_sync(0xffffffffu, dev::mbar_wait(v_full(s), (j / KSV) & 1)))) break;
         const uint32_t vt = SL::v + s * SL::kTile;
-        for (int idx = r; idx < (kTcKeys - nk) * (D / 8); idx += kTcRows) {
+        for (int idx = hc * kTcRows + r; idx < (kTcKeys - nk) * (D / 8); idx += H * kTcRows) {
           const int row = nk + idx / (D / 8), c = idx % (D / 8);
           *reinterpret_cast<uint4 *>(bp + vt + (c >> 3) * SL::kSub + row * 128 +
                                      (((c & 7) ^ (row & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
@@ -913,14 +996,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0) dev::mbar_arrive(p_full(j & 1));
     }
     if (!ok && lane == 0) fail(false);
-    // epilogue: O / l as bf16
+    // the row sum: both halves' parts
+    float ltot = lsum;
+    if (H == 2 && ok) ltot = lsum + other_half(lsum, ok);
+    // epilogue: O / l as bf16, this half's D/H columns
     if (ok && __all_sync(0xffffffffu, dev::mbar_wait(pv_done((nblk - 1) & 1), ((nblk - 1) >> 1) & 1))) {
       dev::tc_fence_after();
-      const float inv = 1.f / lsum;
+      const float inv = 1.f / ltot;
       uint4 *dst = reinterpret_cast<uint4 *>(
           a.out + ((int64_t)(q0 + qi) * a.num_q_heads + g * G + h) * D);
 #pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
+      for (int ch = hc * (D / 32 / H); ch < (hc + 1) * (D / 32 / H); ++ch) {
         uint32_t o[32];
         dev::tmem_ld32(tmem + lane_base + 256u + ch * 32, o);
         dev::tmem_wait_ld();
@@ -936,17 +1022,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       }
+    } else if (ok && lane == 0) {
+      fail(false);
     }
   }
 
   // ---- teardown: no tensor-core op or copy may still be in flight when TMEM is freed
   if (tid == 0) (void)dev::mbar_wait(mma_done, 0);
-  if ((warp == 4 || (kTcProducers == 2 && warp == 6)) && lane == 0 && *s_flag) {
-    for (int s = 0; s < KS; ++s) {
-      const int kl = s + ((k_issued - 1 - s) / KS) * KS;
-      if (kl >= 0 && kl < k_issued) (void)dev::mbar_wait(k_full(s), (kl / KS) & 1);
-      const int vl = s + ((v_issued - 1 - s) / KS) * KS;
-      if (vl >= 0 && vl < v_issued) (void)dev::mbar_wait(v_full(s), (vl / KS) & 1);
+  if ((warp == kProducer || (kTcProducers == 2 && warp == kProducerV)) && lane == 0 && *s_flag) {
+    for (int s = 0; s < KSK; ++s) {
+      const int kl = s + ((k_issued - 1 - s) / KSK) * KSK;
+      if (kl >= 0 && kl < k_issued) (void)dev::mbar_wait(k_full(s), (kl / KSK) & 1);
+    }
+    for (int s = 0; s < KSV; ++s) {
+      const int vl = s + ((v_issued - 1 - s) / KSV) * KSV;
+      if (vl >= 0 && vl < v_issued) (void)dev::mbar_wait(v_full(s), (vl / KSV) & 1);
     }
   }
   dev::tc_fence_before();
@@ -1498,7 +1588,10 @@ __global__ void __launch_bounds__(tc2_threads<D, H>(), 1)
 
 cudaError_t read_prefill_errors(uint32_t *flags, int clear) { return read_tu_errors(flags, clear); }
 
-constexpr size_t tc_smem(int d) { return 1024 + (d == 64 ? TcSmem<64>::total : TcSmem<128>::total); }
+constexpr int tc_halves(int d) { return d == 64 ? 1 : PKV_PREFILL_TC_HALVES128; }
+constexpr size_t tc_smem(int d) {
+  return 1024 + (d == 64 ? TcSmem<64, tc_halves(64)>::total : TcSmem<128, tc_halves(128)>::total);
+}
 static_assert(tc_smem(64) <= 227 * 1024 && tc_smem(128) <= 227 * 1024, "prefill tile fits a CTA");
 // Softmax threads per query row of the two-tile kernel, by head_dim.  At head_dim 128 two
 // (16 softmax warps, 96 registers a thread, each half of a row in its own warp) measured
@@ -1575,10 +1668,10 @@ PKV_API int paged_prefill_attention(pkv_bf16 *out, const pkv_bf16 *q, const pkv_
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)tc2_smem(128));
       else
-        e = D == 64 ? cudaFuncSetAttribute(prefill_tc_kernel<64>,
+        e = D == 64 ? cudaFuncSetAttribute(prefill_tc_kernel<64, tc_halves(64)>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)tc_smem(64))
-                    : cudaFuncSetAttribute(prefill_tc_kernel<128>,
+                    : cudaFuncSetAttribute(prefill_tc_kernel<128, tc_halves(128)>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)tc_smem(128));
       if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute");
@@ -1608,9 +1701,9 @@ PKV_API int paged_prefill_attention(pkv_bf16 *out, const pkv_bf16 *q, const pkv_
   else if (two)
     prefill_tc2_kernel<128, tc2_halves(128)><<<grid, tc2_threads<128, tc2_halves(128)>(), tc2_smem(128), s>>>(tmk, tmv, a);
   else if (D == 64)
-    prefill_tc_kernel<64><<<grid, kTcThreads, tc_smem(64), s>>>(tmk, tmv, a);
+    prefill_tc_kernel<64, tc_halves(64)><<<grid, tc_threads<tc_halves(64)>(), tc_smem(64), s>>>(tmk, tmv, a);
   else
-    prefill_tc_kernel<128><<<grid, kTcThreads, tc_smem(128), s>>>(tmk, tmv, a);
+    prefill_tc_kernel<128, tc_halves(128)><<<grid, tc_threads<tc_halves(128)>(), tc_smem(128), s>>>(tmk, tmv, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "prefill_tc_kernel launch");
   clear_error();
