@@ -728,6 +728,12 @@ __global__ void __launch_bounds__(tc_threads<H>(), 1)
   const int t_end = L - n + last_row / G + 1;  // keys the tile needs: [0, t_end)
   const int nblk = (t_end + kTcKeys - 1) / kTcKeys;
 
+  // the producers' first window of block-table entries, under the set-up below
+  const bool is_producer = warp == kProducer || (kTcProducers == 2 && warp == kProducerV);
+  const int32_t *const trow = a.block_tables + (int64_t)b * a.max_blocks;
+  const int lb_last = (t_end - 1) >> a.log2_bs;
+  const int tb_first = (is_producer && lane <= lb_last) ? __ldg(trow + lane) : 0;
+
   if (tid == 0) {
     // one arrival each (the producer, or a tensor-core commit), except s_free, p_full and
     // q_ready: one arrival per softmax warp; and the pair barriers: every thread of the
@@ -761,10 +767,8 @@ __global__ void __launch_bounds__(tc_threads<H>(), 1)
     const bool do_k = warp == kProducer, do_v = kTcProducers == 1 || warp == kProducerV;
     // every query tile of this (sequence, kv head) reads the same blocks: keep them in L2
     const uint64_t policy = dev::policy_evict_last();
-    const int32_t *trow = a.block_tables + (int64_t)b * a.max_blocks;
-    const int lb_last = (t_end - 1) >> a.log2_bs;
     int kwin = 0, vwin = 0;
-    int ktb = (lane <= lb_last) ? __ldg(trow + lane) : 0;
+    int ktb = tb_first;
     int vtb = ktb;
     for (int j = 0; j <= nblk; ++j) {  // K runs one block ahead of V
       if (do_k && j < nblk) {
@@ -1196,6 +1200,15 @@ __global__ void __launch_bounds__(tc2_threads<D, H>(), 1)
   const int nblk = max(nblk_t[0], nblk_t[1]);
   auto nblk_of = [&](int t) { return t ? nblk_t[1] : nblk_t[0]; };
 
+  // The producers' first window of block-table entries goes out before the set-up, so
+  // that its latency runs under the barrier initialisation and the TMEM allocation.  (The
+  // softmax threads' query rows wait until after it: loaded before the barrier they held
+  // every warp, the producers too, behind their latency: -3% on workload 3.)
+  const bool is_producer = warp == kProducer || (tc2_producers<D>() == 2 && warp == kProducerV);
+  const int32_t *const trow = a.block_tables + (int64_t)b * a.max_blocks;
+  const int lb_last = (t_end - 1) >> a.log2_bs;
+  const int tb_first = (is_producer && lane <= lb_last) ? __ldg(trow + lane) : 0;
+
   if (tid == 0) {
     for (int i = 0; i < SL::kBars; ++i) {
       const uint32_t bar = bars + 8u * i;
@@ -1234,10 +1247,8 @@ __global__ void __launch_bounds__(tc2_threads<D, H>(), 1)
     // ---------------------------------------------------------- producer warp(s)
     const bool do_k = warp == kProducer, do_v = tc2_producers<D>() == 1 || warp == kProducerV;
     const uint64_t policy = dev::policy_evict_last();
-    const int32_t *trow = a.block_tables + (int64_t)b * a.max_blocks;
-    const int lb_last = (t_end - 1) >> a.log2_bs;
     int kwin = 0, vwin = 0;
-    int ktb = (lane <= lb_last) ? __ldg(trow + lane) : 0;
+    int ktb = tb_first;
     int vtb = ktb;
     for (int j = 0; j <= nblk; ++j) {  // K runs one block ahead of V
       if (do_k && j < nblk) {
