@@ -724,9 +724,31 @@ def run_kernel(args, w) -> None:
             g.replay()
         e1.record(stream)
     torch.cuda.synchronize()
-    clk = clocks.stop()
+    clk_timed = clocks.stop()
     t = e0.elapsed_time(e1) / 1e3 / (reps * R)
     value = per / t
+    # Clock record: the timed region can be shorter than nvidia-smi's sampling period, so
+    # the same graph is replayed back to back for about 1.5 s more (outside the timed
+    # region) while the clocks are sampled; that window's own time per call is reported
+    # beside them as a cross-check.
+    sampler = ClockSampler(0)
+    time.sleep(0.25)  # let nvidia-smi start before the load
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wreps, t0 = 0, time.perf_counter()
+    with torch.cuda.stream(stream):
+        w0.record(stream)
+        while time.perf_counter() - t0 < 1.5:
+            for _ in range(20):
+                g.replay()
+            wreps += 20
+            stream.synchronize()
+        w1.record(stream)
+    torch.cuda.synchronize()
+    clk = sampler.stop()
+    clk["window_s"] = round(time.perf_counter() - t0, 3)
+    clk["window_ms_per_call"] = w0.elapsed_time(w1) / (wreps * R)
+    clk["timed_region_samples"] = clk_timed.get("samples", 0)
+    clk["timed_region_reasons"] = clk_timed.get("reasons", [])
     assert B.pkv_device_errors() == 0
     line.update({"metric": metric, "value": value, "unit": unit, "ms_per_step": t * 1e3,
                  "steps": reps * R, "higher_is_better": True,
