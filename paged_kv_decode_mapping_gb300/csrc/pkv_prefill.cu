@@ -10,7 +10,10 @@
 #include "pkv_exp2.cuh"
 
 // Of the 16 column pairs of each 32-column chunk of a score row, how many take their
-// exponentials on the FMA pipe (exp2_fma) rather than the special-function unit.
+// exponentials on the FMA pipe (exp2_fma) rather than the special-function unit, in
+// row_block_exp and in the one-pass weights.  0: every fraction tried measured slower
+// (2 pairs: -4 to -6%, 4 pairs: -8 to -15% on the four prefill workloads): the softmax
+// waits on latency and issue, not on the special-function unit.
 #ifndef PKV_PREFILL_POLY_PAIRS
 #define PKV_PREFILL_POLY_PAIRS 0
 #endif
@@ -499,7 +502,14 @@ __device__ __forceinline__ float row_regs_exp_pk_max_impl(const uint32_t (&x)[NC
                           2 * e + 1 <= lc ? x1 * sc : -INFINITY);
       float a0, a1;
       fma_f32x2(x0, x1, scale_log2, -m_ref, a0, a1);
-      float p0 = dev::ex2(a0), p1 = dev::ex2(a1);
+      float p0, p1;
+      if (e < PKV_PREFILL_POLY_PAIRS) {
+        p0 = dev::exp2_fma(a0);
+        p1 = dev::exp2_fma(a1);
+      } else {
+        p0 = dev::ex2(a0);
+        p1 = dev::ex2(a1);
+      }
       if constexpr (kMode == 2) {
         p0 = 2 * e <= lc ? p0 : 0.f;
         p1 = 2 * e + 1 <= lc ? p1 : 0.f;
